@@ -1,0 +1,211 @@
+"""KDA oracle -- TEST INFRASTRUCTURE ONLY.
+
+Plain, slow, obviously-correct CPU implementations of the Kimi Delta Attention
+(KDA) operator, used to check the GPU library.  Only the test suite,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import
+this package.  It shares no code with the GPU library and never imports it.
+
+Contents
+--------
+``fwd`` / ``decode_step``
+    ctypes front end of ``kda_oracle.c``: the token-by-token fp64 recurrence
+    (decay -> old = Sbar^T k -> erase + write -> read the updated state), as
+    written in "Kimi K3 的 KDA" sections 3-4, "Kimi K3" (gentlecold) section 3.2
+    and "Kimi Delta Attention 完全拆解" (KDA equations and the decode-order listing).
+``bruteforce``
+    For tiny T: builds each d_k x d_k transition matrix
+    A_t = (I - beta_t k_t k_t^T) Diag(alpha_t) explicitly and iterates
+    S_t = A_t S_{t-1} + beta_t k_t v_t^T ("完全拆解", the state-space form in the
+    section on why a plain prefix scan is not used).  numpy, independent code.
+``expanded_outputs``
+    For tiny T: the fully expanded output
+    o_t = (A_t...A_1 S_0)^T q_t + sum_{i<=t} beta_i [q_t^T A_t...A_{i+1} k_i] v_i
+    ("完全拆解", the expansion in the comparison with GDN; the page's display drops
+    beta_i and the S_0 term; both are restored here, since unrolling the
+    recurrence S_t = A_t S_{t-1} + beta_t k_t v_t^T produces them).
+
+Parity status of every function is pinned by ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD_DIR, "libkda_oracle.so")
+_lock = threading.Lock()
+_handle = None
+
+# Planted-mistake codes understood by kda_oracle.c (tests only).
+PLANTS = {
+    "no_decay": 1,
+    "erase_then_decay": 2,
+    "erase_sign": 3,
+    "read_before_write": 4,
+    "transposed_old": 5,
+    "decay_value_axis": 6,
+    "beta_on_erase_only": 7,
+    "stale_gate": 8,
+}
+
+
+def build(force: bool = False) -> str:
+    """Compile kda_oracle.c into a shared library with gcc (-O2, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_SO)
+            and os.path.getmtime(_SO) >= os.path.getmtime(_SRC)):
+        return _SO
+    tmp = _SO + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _lib():
+    global _handle
+    with _lock:
+        if _handle is None:
+            path = build()
+            lib = ctypes.CDLL(path)
+            dp = ctypes.POINTER(ctypes.c_double)
+            lp = ctypes.POINTER(ctypes.c_int64)
+            ci = ctypes.c_int
+            lib.kda_oracle_fwd.restype = ci
+            lib.kda_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, lp, ci, ci, ci, ci,
+                                           ci, ci, dp, dp]
+            lib.kda_oracle_decode_step.restype = ci
+            lib.kda_oracle_decode_step.argtypes = [dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, dp]
+            lib.kda_oracle_max_threads.restype = ci
+            lib.kda_oracle_max_threads.argtypes = []
+            _handle = lib
+    return _handle
+
+
+def _f64(x) -> np.ndarray:
+    """Exact upcast to a contiguous float64 numpy array (accepts torch tensors)."""
+    if hasattr(x, "detach"):  # torch tensor: upcast exactly on the CPU
+        import torch
+        x = x.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def max_threads() -> int:
+    """Number of OpenMP threads the oracle runs with."""
+    return int(_lib().kda_oracle_max_threads())
+
+
+def fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, erase: bool = True,
+        plant: int = 0):
+    """Token-by-token fp64 KDA forward.
+
+    Shapes (either a fixed-length batch or a packed varlen batch):
+      q, k, log_alpha : [B, T, H, dk] or [Ttot, H, dk]
+      v               : [B, T, H, dv] or [Ttot, H, dv]
+      beta            : [B, T, H]     or [Ttot, H]
+      S0              : [N, H, dv, dk] (memory layout mem[v][c] = S[c][v]) or None
+      cu_seqlens      : [N+1] int offsets into the packed token axis, or None
+                        (then N = B and sequence b is tokens b*T..(b+1)*T-1)
+    Returns (o, S_T) as float64 arrays, o shaped like v, S_T [N, H, dv, dk].
+    """
+    q, k, v, g, b = (_f64(x) for x in (q, k, v, log_alpha, beta))
+    lead = v.shape[:-2]
+    H, dk = q.shape[-2], q.shape[-1]
+    dv = v.shape[-1]
+    Ttot = int(np.prod(lead)) if len(lead) else 0
+    if cu_seqlens is None:
+        if q.ndim == 4:
+            Bsz, T = q.shape[0], q.shape[1]
+        else:
+            Bsz, T = 1, q.shape[0]
+        cu = np.arange(Bsz + 1, dtype=np.int64) * T
+    else:
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu() if hasattr(cu_seqlens, "cpu") else cu_seqlens, dtype=np.int64))
+    N = cu.shape[0] - 1
+    if int(cu[-1]) != Ttot:
+        raise ValueError("cu_seqlens[-1] must equal the number of packed tokens")
+    s0 = None if S0 is None else _f64(S0).reshape(N, H, dv, dk)
+    o = np.zeros(lead + (H, dv), dtype=np.float64)
+    ST = np.zeros((N, H, dv, dk), dtype=np.float64)
+    rc = _lib().kda_oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(s0),
+                               cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                               N, H, dk, dv, int(bool(erase)), int(plant), _ptr(o), _ptr(ST))
+    if rc != 0:
+        raise ValueError("kda_oracle_fwd rejected its arguments")
+    return o, ST
+
+
+def decode_step(q, k, v, log_alpha, beta, S):
+    """One fp64 decode step for every (session, head).
+
+    q, k, log_alpha [N, H, dk]; v [N, H, dv]; beta [N, H]; S [N, H, dv, dk].
+    Returns (o [N, H, dv], S_new); the inputs are not modified.
+    """
+    q, k, v, g, b = (_f64(x) for x in (q, k, v, log_alpha, beta))
+    S = _f64(S).copy()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((N, H, dv), dtype=np.float64)
+    rc = _lib().kda_oracle_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(S),
+                                       N, H, dk, dv, _ptr(o))
+    if rc != 0:
+        raise ValueError("kda_oracle_decode_step rejected its arguments")
+    return o, S
+
+
+def bruteforce(q, k, v, log_alpha, beta, S0=None):
+    """Single head, tiny T: explicit d_k x d_k transitions.
+
+    q, k, log_alpha [T, dk]; v [T, dv]; beta [T]; S0 logical [dk, dv] or None.
+    Returns (o [T, dv], S_T logical [dk, dv]).
+    """
+    q, k, v, g, b = (_f64(x) for x in (q, k, v, log_alpha, beta))
+    T, dk = q.shape
+    dv = v.shape[1]
+    S = np.zeros((dk, dv)) if S0 is None else _f64(S0).copy()
+    eye = np.eye(dk)
+    o = np.zeros((T, dv))
+    for t in range(T):
+        A = (eye - b[t] * np.outer(k[t], k[t])) @ np.diag(np.exp(g[t]))
+        S = A @ S + b[t] * np.outer(k[t], v[t])
+        o[t] = S.T @ q[t]
+    return o, S
+
+
+def expanded_outputs(q, k, v, log_alpha, beta, S0=None):
+    """Single head, tiny T: o_t from the fully expanded sum over earlier writes.
+
+    o_t = (P_{t,0} S_0)^T q_t + sum_{i<=t} beta_i (q_t^T P_{t,i} k_i) v_i,
+    with P_{t,i} = A_t A_{t-1} ... A_{i+1} (identity when i = t) and
+    A_j = (I - beta_j k_j k_j^T) Diag(alpha_j).
+    """
+    q, k, v, g, b = (_f64(x) for x in (q, k, v, log_alpha, beta))
+    T, dk = q.shape
+    dv = v.shape[1]
+    S0 = np.zeros((dk, dv)) if S0 is None else _f64(S0)
+    eye = np.eye(dk)
+    A = [(eye - b[j] * np.outer(k[j], k[j])) @ np.diag(np.exp(g[j])) for j in range(T)]
+    o = np.zeros((T, dv))
+    for t in range(T):
+        P = eye.copy()          # P_{t,t}
+        acc = np.zeros(dv)
+        for i in range(t, -1, -1):
+            acc += b[i] * (q[t] @ P @ k[i]) * v[i]
+            P = P @ A[i]        # becomes P_{t,i-1} = A_t ... A_i
+        acc += (P @ S0).T @ q[t]  # P is now A_t ... A_1 (all transitions)
+        o[t] = acc
+    return o

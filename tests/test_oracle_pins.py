@@ -1,0 +1,189 @@
+"""The fp64 oracle against what the pages and mathematics fix (CPU only)."""
+import numpy as np
+import pytest
+
+import oracle
+from tests import oracle_pins as P
+
+
+@pytest.mark.parametrize("pin", P.INDEPENDENT_PINS, ids=lambda f: f.__name__)
+def test_c_oracle_pins(pin):
+    assert pin(P.c_oracle()) < P.tol(pin)
+
+
+# The numpy brute force and the expanded sum are pinned by the same closed forms
+# (the pins that need no-erase mode or the final state skip themselves there).
+@pytest.mark.parametrize("pin", [P.pin_identity_transition, P.pin_unit_key_recall,
+                                 P.pin_orthonormal_keys_linear_attention,
+                                 P.pin_worked_example_with_erase, P.pin_sgd_step,
+                                 P.pin_norm_nonincreasing],
+                         ids=lambda f: f.__name__)
+@pytest.mark.parametrize("impl", [P.bruteforce_impl, P.expanded_impl],
+                         ids=["bruteforce", "expanded"])
+def test_tiny_restatements_pins(pin, impl):
+    assert pin(impl) < P.tol(pin)
+
+
+@pytest.mark.parametrize("name,code", sorted(oracle.PLANTS.items()))
+def test_planted_mistakes_are_caught(name, code):
+    """Every planted slip in the C oracle breaks at least one independent pin."""
+    impl = P.c_oracle(plant=code)
+    failures = []
+    for pin in P.INDEPENDENT_PINS:
+        try:
+            err = pin(impl)
+        except ValueError:
+            continue  # this mistake needs dk == dv; the pin uses other sizes
+        if not err < P.tol(pin):
+            failures.append(pin.__name__)
+    assert failures, f"planted mistake '{name}' passed every pin"
+
+
+def _rand_packed(rng, lengths, H, dk, dv, s0=True):
+    T = int(sum(lengths))
+    q = P.unit(rng.standard_normal((T, H, dk)))
+    k = P.unit(rng.standard_normal((T, H, dk)))
+    v = rng.standard_normal((T, H, dv))
+    g = rng.uniform(-0.5, -0.001, (T, H, dk))
+    b = 1 / (1 + np.exp(-rng.standard_normal((T, H))))
+    S0 = 0.1 * rng.standard_normal((len(lengths), H, dv, dk)) if s0 else None
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    return q, k, v, g, b, S0, cu
+
+
+def test_segment_split_equals_whole():
+    """Running T1 tokens, then T2 tokens from the returned state, equals one run
+    over T1 + T2 ("完全拆解", validation advice: two segments with a nonzero
+    initial state against the whole).  The oracle is sequential: bit-identical."""
+    rng = np.random.default_rng(11)
+    q, k, v, g, b, S0, _ = _rand_packed(rng, [50], 3, 8, 6)
+    o, ST = oracle.fwd(q, k, v, g, b, S0, np.array([0, 50]))
+    o1, S1 = oracle.fwd(q[:20], k[:20], v[:20], g[:20], b[:20], S0, np.array([0, 20]))
+    o2, S2 = oracle.fwd(q[20:], k[20:], v[20:], g[20:], b[20:], S1, np.array([0, 30]))
+    assert np.array_equal(np.concatenate([o1, o2]), o)
+    assert np.array_equal(S2, ST)
+
+
+def test_varlen_isolation():
+    """Packing other sequences next to a sequence, or reordering them, leaves
+    its output and final state bit-identical ("完全拆解", validation advice on
+    varlen batches)."""
+    rng = np.random.default_rng(12)
+    lengths = [5, 17, 1, 9]
+    q, k, v, g, b, S0, cu = _rand_packed(rng, lengths, 2, 6, 6)
+    o, ST = oracle.fwd(q, k, v, g, b, S0, cu)
+    for i, L in enumerate(lengths):
+        sl = slice(cu[i], cu[i + 1])
+        oi, Si = oracle.fwd(q[sl], k[sl], v[sl], g[sl], b[sl], S0[i:i + 1], np.array([0, L]))
+        assert np.array_equal(oi, o[sl])
+        assert np.array_equal(Si[0], ST[i])
+    perm = [2, 0, 3, 1]
+    parts = [slice(cu[i], cu[i + 1]) for i in perm]
+    cat = lambda x: np.concatenate([x[s] for s in parts])
+    cu_p = np.concatenate([[0], np.cumsum([lengths[i] for i in perm])])
+    op, Sp = oracle.fwd(cat(q), cat(k), cat(v), cat(g), cat(b), S0[perm], cu_p)
+    assert np.array_equal(Sp, ST[perm])
+    assert np.array_equal(op, cat(o))
+
+
+def test_empty_sequences():
+    """Zero-length sequences return their initial state and produce no output."""
+    rng = np.random.default_rng(13)
+    q, k, v, g, b, S0, cu = _rand_packed(rng, [0, 4, 0], 2, 4, 4)
+    o, ST = oracle.fwd(q, k, v, g, b, S0, cu)
+    assert np.array_equal(ST[0], S0[0]) and np.array_equal(ST[2], S0[2])
+    assert o.shape == (4, 2, 4)
+
+
+def test_prefill_equals_decode_steps():
+    """The prefill path and T single-token decode steps give the same outputs
+    and state: the output of a token reads the state after its own write in
+    both ("完全拆解": the parallel and recurrent paths must share the causal
+    mask)."""
+    rng = np.random.default_rng(14)
+    q, k, v, g, b, S0, _ = _rand_packed(rng, [12], 3, 8, 8)
+    o, ST = oracle.fwd(q, k, v, g, b, S0, np.array([0, 12]))
+    S = S0.copy()
+    for t in range(12):
+        ot, S = oracle.decode_step(q[t][None], k[t][None], v[t][None], g[t][None],
+                                   b[t][None], S)
+        np.testing.assert_allclose(ot[0], o[t], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(S, ST, rtol=0, atol=1e-13)
+
+
+def test_scalar_gate_is_gated_deltanet():
+    """All channels of alpha_t equal: KDA reduces to Gated DeltaNet,
+    S_t = a_t (I - b_t k_t k_t^T) S_{t-1} + b_t k_t v_t^T ("完全拆解", GDN and
+    the degenerate cases of KDA).  GDN is written here as its own loop."""
+    rng = np.random.default_rng(15)
+    T, d, dv = 9, 6, 5
+    q, k, v, _, b, S0 = P.random_head(rng, T, d, dv)
+    s = rng.uniform(-0.5, -0.01, T)
+    g = np.repeat(s[:, None], d, axis=1)
+    S = S0.T.copy()
+    ref = np.zeros((T, dv))
+    for t in range(T):
+        S = np.exp(s[t]) * (S - b[t] * np.outer(k[t], k[t] @ S)) + b[t] * np.outer(k[t], v[t])
+        ref[t] = S.T @ q[t]
+    o, ST = P.c_oracle()(q, k, v, g, b, S0)
+    assert P.relerr(o, ref) < P.TOL and P.relerr(ST, S.T) < P.TOL
+
+
+def test_unit_gate_is_deltanet():
+    """alpha = 1: KDA reduces to DeltaNet, S_t = S_{t-1} - b_t k_t (S_{t-1}^T k_t - v_t)^T
+    ("完全拆解", the DeltaNet update written as a gradient step)."""
+    rng = np.random.default_rng(16)
+    T, d, dv = 9, 7, 4
+    q, k, v, _, b, S0 = P.random_head(rng, T, d, dv)
+    S = S0.T.copy()
+    ref = np.zeros((T, dv))
+    for t in range(T):
+        S = S - b[t] * np.outer(k[t], S.T @ k[t] - v[t])
+        ref[t] = S.T @ q[t]
+    o, ST = P.c_oracle()(q, k, v, np.zeros((T, d)), b, S0)
+    assert P.relerr(o, ref) < P.TOL and P.relerr(ST, S.T) < P.TOL
+
+
+def test_segment_map_is_affine_and_composes():
+    """For a fixed segment the map S_in -> S_out is affine, S_out = M S_in + S~
+    (M and S~ depending only on the segment's tokens), and two segment maps
+    compose as (M2, b2) o (M1, b1) = (M2 M1, M2 b1 + b2) ("Kimi K3" (gentlecold)
+    section 3.6, KDA context parallelism)."""
+    rng = np.random.default_rng(17)
+    d = 5
+    q, k, v, g, b, _ = P.random_head(rng, 14, d, d)
+
+    def seg(lo, hi, S_in_logical):
+        _, ST = P.c_oracle()(q[lo:hi], k[lo:hi], v[lo:hi], g[lo:hi], b[lo:hi],
+                             S_in_logical.T)
+        return ST.T
+
+    def affine(lo, hi):
+        b0 = seg(lo, hi, np.zeros((d, d)))
+        # the linear part acts on the key axis: column j of S_in maps
+        # independently, so M is recovered from unit inputs e_i e_j^T.
+        M = np.zeros((d, d))
+        for i in range(d):
+            E = np.zeros((d, d))
+            E[i, 0] = 1.0
+            M[:, i] = (seg(lo, hi, E) - b0)[:, 0]
+        return M, b0
+
+    X = rng.standard_normal((d, d))
+    M1, b1 = affine(0, 6)
+    M2, b2 = affine(6, 14)
+    assert P.relerr(seg(0, 6, X), M1 @ X + b1) < 1e-12
+    M12, b12 = M2 @ M1, M2 @ b1 + b2
+    whole = seg(0, 14, X)
+    assert P.relerr(whole, M12 @ X + b12) < 1e-12
+    Mw, bw = affine(0, 14)
+    assert P.relerr(Mw, M12) < 1e-12 and P.relerr(bw, b12) < 1e-12
+
+
+def test_rejects_bad_arguments():
+    rng = np.random.default_rng(18)
+    q, k, v, g, b, S0, cu = _rand_packed(rng, [3, 3], 1, 4, 4)
+    with pytest.raises(ValueError):
+        oracle.fwd(q, k, v, g, b, S0, np.array([0, 7, 6]))      # decreasing offsets
+    with pytest.raises(ValueError):
+        oracle.fwd(q, k, v, g, b, S0, np.array([0, 3, 5]))      # does not cover all tokens
