@@ -1,0 +1,520 @@
+"""Benchmark of the KDA operator on one node (one process per GPU).
+
+Default workload (the headline): chunkwise prefill, B=1, H=96, T=8192,
+d_k=d_v=128, bf16 q/k/v, fp32 log_alpha/beta, fp32 state, S0 = 0 -- metric
+tokens/s.  The same JSON line carries a ``decode`` object: one decode step for
+64 sessions x 96 heads (fp32 state [64, 96, 128, 128], 403 MB, in place) --
+metric state-GB/s = 2 * state bytes / step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload prefill|decode|long|varlen]
+
+A step is one kda_fwd over the whole workload (the set-up kernel plus the
+prefill kernel).  Inputs are generated on the device before timing and are
+larger than L2, so no L2 flush is needed between steps.  Timing: CUDA events
+on the launching stream, barrier + synchronize on both sides, max over ranks.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_attention_recurrence_chunkwise_gb300 import inputs as I  # noqa: E402
+
+METRIC = "KDA prefill tokens/s and decode state GB/s (H=96,d=128) vs roofline"
+KERNEL_SOURCES = {
+    "prefill_tc": "linear_attention_recurrence_chunkwise_gb300/csrc/kda_prefill_tc.cu",
+    "prefill_simt": "linear_attention_recurrence_chunkwise_gb300/csrc/kda_prefill_simt.cu",
+    "decode": "linear_attention_recurrence_chunkwise_gb300/csrc/kda_decode.cu",
+}
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def source_hash(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel_key, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(kernel_key, {}).get(workload)
+    if not rec or rec.get("source_sha256_16") != source_hash(KERNEL_SOURCES[kernel_key]):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background (200 ms period)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.tmp is None:
+            return None
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r.strip().split(",") for r in f if r.strip()]
+        os.unlink(self.tmp.name)
+        rows = [[c.strip() for c in r] for r in rows if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def nbytes(*ts):
+    return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+# ------------------------------------------------------------------ workloads
+
+def make_workload(name, seed, device):
+    if name == "decode":
+        p = I.PRESETS["decode"]
+        S = I.decode_state(p["N"], p["H"], p["d"], p["d"], p["s0_std"], seed, device)
+        steps = [I.decode_token(p["N"], p["H"], p["d"], p["d"], p["dtype"], p["la"], seed, s,
+                                device) for s in range(8)]
+        return dict(kind="decode", S=S, tokens=steps, N=p["N"], H=p["H"], d=p["d"],
+                    label=f"decode step N={p['N']} H={p['H']} d={p['d']} {p['dtype']} "
+                          f"fp32 state (in place)")
+    prob = I.preset_problem(name, seed=seed, device=device)
+    Ttot = prob.q.shape[0] * prob.q.shape[1] if prob.q.dim() == 4 else prob.q.shape[0]
+    H, d = prob.q.shape[-2], prob.q.shape[-1]
+    lab = {"prefill": "prefill B=1 H=96 T=8192 d=128 bf16, S0=0",
+           "long": "long prefill B=1 H=96 T=131072 d=128 bf16, S0~N(0,0.02)",
+           "varlen": f"varlen prefill 16 seqs (sum T={Ttot}) H=96 d=128 bf16",
+           "tiny": "tiny prefill B=1 H=2 T=256 d=64 fp32"}[name]
+    return dict(kind="prefill", prob=prob, Ttot=Ttot, H=H, d=d, label=lab)
+
+
+def prefill_alg_bytes(w):
+    p = w["prob"]
+    return nbytes(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0, p.cu_seqlens) + \
+        nbytes(p.v) + p.n_seq * w["H"] * w["d"] * w["d"] * 4  # o and S_T
+
+
+def prefill_flops(w):
+    """Chunk-kernel FLOPs per head 6 T d^2 + 3 T C d + T C^2 (C = 64), as the
+    pages give them ("Kimi Delta Attention 完全拆解", prefill complexity)."""
+    T, d, C = w["Ttot"], w["d"], 64
+    return w["H"] * (6 * T * d * d + 3 * T * C * d + T * C * C)
+
+
+def decode_alg_bytes(w):
+    S = w["S"]
+    x = w["tokens"][0]
+    return 2 * nbytes(S) + nbytes(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"]) + \
+        nbytes(x["v"])
+
+
+# ------------------------------------------------------------------ our arm
+
+def time_prefill(kda, w, steps, warmup, stream):
+    p = w["prob"]
+    o = torch.empty_like(p.v)
+    ST = torch.empty((p.n_seq, w["H"], w["d"], w["d"]), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.kda_fwd_workspace_bytes(p.n_seq), dtype=torch.uint8, device="cuda")
+
+    def call():
+        kda.kda_fwd(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0, p.cu_seqlens, o=o, S_T=ST,
+                    workspace=ws, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    return call, ev, (o, ST, ws)
+
+
+def run_ours(args, world, rank):
+    from linear_attention_recurrence_chunkwise_gb300 import build as kbuild
+    kbuild.build()
+    from linear_attention_recurrence_chunkwise_gb300 import kda
+    kda.load()
+    pk = peaks()
+    stream = torch.cuda.Stream()
+    w = make_workload(args.workload, seed=args.seed + rank, device="cuda")
+    torch.cuda.synchronize()
+
+    if w["kind"] == "prefill":
+        call, ev, bufs = time_prefill(kda, w, args.steps, args.warmup, stream)
+        launches_per_step = 2
+    else:
+        S = w["S"]
+        toks = w["tokens"]
+        o = torch.empty_like(toks[0]["v"])
+        ctr = [0]
+
+        def call():
+            x = toks[ctr[0] % len(toks)]
+            ctr[0] += 1
+            kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S, o=o,
+                                stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        launches_per_step = 1
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        time.sleep(0.25)  # let the sampler see the idle->busy edge
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(args.steps):
+                ev[i][0].record(stream)
+                call()
+                ev[i][1].record(stream)
+            stop.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = start.elapsed_time(stop)
+    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+
+    if w["kind"] == "prefill":
+        units = w["Ttot"]
+        value = units * world / (ms_step / 1e3)
+        unit = "tokens/s"
+        alg = prefill_alg_bytes(w)
+        flops = prefill_flops(w)
+        kernel_key = "prefill_tc" if (w["prob"].q.dtype == torch.bfloat16 and w["d"] == 128) \
+            else "prefill_simt"
+    else:
+        value = 2 * nbytes(w["S"]) * world / (ms_step / 1e3) / 1e9
+        unit = "GB/s"
+        alg = decode_alg_bytes(w)
+        flops = None
+        kernel_key = "decode"
+    achieved_gbs = alg / (per_launch_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm"],
+                "unit": "GB/s", "frac": round(achieved_gbs / pk["hbm"], 4),
+                "traffic": traffic_for(kernel_key, args.workload),
+                "peak_source": f"{pk['source']} (MEASURED_PEAKS.json hbm_gbs)"
+                if pk["source"] == "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": alg, "kernel": kernel_key,
+                "avg_launch_ms": round(per_launch_ms, 4)}
+    if flops is not None:
+        tf = flops / (per_launch_ms / 1e3) / 1e12
+        roofline["tensor"] = {"achieved_tflops": round(tf, 2), "peak_tflops": pk["bf16"],
+                              "frac": round(tf / pk["bf16"], 4),
+                              "flops_per_launch": flops,
+                              "flop_count": "6Td^2+3TCd+TC^2 per head (pages' formula)"}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if args.workload != "tiny" else "f32",
+            "data": "synthetic (seeded, device-generated)",
+            "config": {"workload": w["label"], "l2": "inputs larger than L2, no flush",
+                       "parallelism": f"replicas x{world} (independent problems per rank)"},
+            "roofline": roofline, "clocks": clk.summary(),
+            "gpu_launches": launches_per_step * args.steps}
+    if w["kind"] == "prefill":
+        line["config"].update(tokens_per_step=w["Ttot"], heads=w["H"], d=w["d"])
+        line["e2e"] = e2e_prefill(kda, w, max(2, min(args.steps, 5)), stream, world)
+        if args.workload == "prefill" and not args.no_decode:
+            line["decode"] = decode_sub(kda, args, stream, pk)
+    else:
+        line["e2e"] = e2e_decode(kda, w, max(2, min(args.steps, 20)), stream, world)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w, args)
+    return line
+
+
+def decode_sub(kda, args, stream, pk):
+    w = make_workload("decode", seed=args.seed, device="cuda")
+    S, toks = w["S"], w["tokens"]
+    o = torch.empty_like(toks[0]["v"])
+    steps = 100
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            x = toks[i % len(toks)]
+            kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S, o=o,
+                                stream=stream)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for i in range(steps):
+            x = toks[i % len(toks)]
+            kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S, o=o,
+                                stream=stream)
+        b.record(stream)
+    stream.synchronize()
+    ms = a.elapsed_time(b) / steps
+    alg = decode_alg_bytes(w)
+    gbs = alg / (ms / 1e3) / 1e9
+    return {"metric": "decode state GB/s", "value": round(2 * nbytes(S) / (ms / 1e3) / 1e9, 1),
+            "unit": "GB/s", "us_per_step": round(ms * 1e3, 2), "steps": steps,
+            "workload": w["label"],
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
+                         "traffic": traffic_for("decode", "decode"),
+                         "algorithmic_bytes_per_launch": alg}}
+
+
+def e2e_prefill(kda, w, steps, stream, world):
+    """Same metric through the public API with pinned host buffers: H2D of the
+    step's inputs, kda_fwd, D2H of o and S_T, all inside the timed region."""
+    p = w["prob"]
+    host = {n: getattr(p, n).to("cpu").pin_memory()
+            for n in ("q", "k", "v", "log_alpha", "beta")}
+    host_S0 = None if p.S0 is None else p.S0.to("cpu").pin_memory()
+    host_cu = None if p.cu_seqlens is None else p.cu_seqlens.to("cpu").pin_memory()
+    o_h = torch.empty(p.v.shape, dtype=p.v.dtype).pin_memory()
+    ST_h = torch.empty((p.n_seq, w["H"], w["d"], w["d"]), dtype=torch.float32).pin_memory()
+    h2d = nbytes(*host.values(), host_S0, host_cu)
+    d2h = nbytes(o_h, ST_h)
+
+    def step():
+        dev = {n: t.to("cuda", non_blocking=True) for n, t in host.items()}
+        S0 = None if host_S0 is None else host_S0.to("cuda", non_blocking=True)
+        cu = None if host_cu is None else host_cu.to("cuda", non_blocking=True)
+        o, ST = kda.kda_fwd(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"], S0,
+                            cu, stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        ST_h.copy_(ST, non_blocking=True)
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+    stream.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / steps, world)
+    return {"value": round(w["Ttot"] * world / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3)}
+
+
+def e2e_decode(kda, w, steps, stream, world):
+    S_dev = w["S"]
+    host = [{n: t.to("cpu").pin_memory() for n, t in x.items()} for x in w["tokens"]]
+    o_h = torch.empty(w["tokens"][0]["v"].shape, dtype=w["tokens"][0]["v"].dtype).pin_memory()
+    h2d = nbytes(*host[0].values())
+    d2h = nbytes(o_h)
+
+    def step(i):
+        x = {n: t.to("cuda", non_blocking=True) for n, t in host[i % len(host)].items()}
+        o = kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S_dev,
+                                stream=stream)
+        o_h.copy_(o, non_blocking=True)
+    with torch.cuda.stream(stream):
+        step(0)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for i in range(steps):
+            step(i)
+        b.record(stream)
+    stream.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / steps, world)
+    return {"value": round(2 * nbytes(S_dev) * world / (ms / 1e3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, budget_heads=None):
+    """Bounded sample of the workload for the fp64 oracle and its scale factor."""
+    import oracle
+    cores = oracle.max_threads()
+    if w["kind"] == "prefill":
+        p = w["prob"]
+        H = w["H"]
+        nh = min(H, budget_heads or max(1, 2 * cores))
+        idx = torch.arange(nh, device=p.q.device)
+        q, k, v = (t.index_select(-2, idx) for t in (p.q, p.k, p.v))
+        g = p.log_alpha.index_select(-2, idx)
+        b = p.beta.index_select(-1, idx)
+        S0 = None if p.S0 is None else p.S0.index_select(1, idx)
+        cu = None if p.cu_seqlens is None else p.cu_seqlens.cpu().numpy()
+        args = [oracle._f64(x) for x in (q, k, v, g, b)]
+        s0 = None if S0 is None else oracle._f64(S0)
+
+        def run():
+            oracle.fwd(*args, s0, cu)
+        return run, nh / H, f"{nh} of {H} heads, all {w['Ttot']} tokens", cores
+    S = w["S"]
+    x = w["tokens"][0]
+    nsess = min(S.shape[0], max(1, cores))
+    args = [oracle._f64(t[:nsess]) for t in (x["q"], x["k"], x["v"], x["log_alpha"],
+                                              x["beta"])]
+    S_h = oracle._f64(S[:nsess])
+
+    def run():
+        oracle.decode_step(*args, S_h)
+    return run, nsess / S.shape[0], f"{nsess} of {S.shape[0]} sessions, all heads", cores
+
+
+def cpu_baseline(w, args, steps=1):
+    run, frac, sample, cores = oracle_sample(w)
+    run()  # warm (and builds the oracle library if needed)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        run()
+    dt = (time.perf_counter() - t0) / steps / frac  # seconds for the whole workload
+    if w["kind"] == "prefill":
+        return {"value": round(w["Ttot"] / dt, 2), "unit": "tokens/s", "cores": cores,
+                "kind": "oracle", "sample": sample,
+                "seconds_sampled": round(dt * frac, 2)}
+    return {"value": round(2 * nbytes(w["S"]) / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "sample": sample, "seconds_sampled": round(dt * frac, 2)}
+
+
+def run_reference(args, world, rank):
+    """The oracle, as it stands, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    w = make_workload(args.workload, seed=args.seed,
+                      device="cuda" if torch.cuda.is_available() else "cpu")
+    run, frac, sample, cores = oracle_sample(w)
+    run()  # one untimed call (builds and warms the oracle library)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps / frac
+    if w["kind"] == "prefill":
+        value, unit = w["Ttot"] / dt, "tokens/s"
+    else:
+        value, unit = 2 * nbytes(w["S"]) / dt / 1e9, "GB/s"
+    return {"metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded)", "impl": "reference",
+            "config": {"workload": w["label"]},
+            "cpu_baseline": {"value": round(value, 3), "unit": unit, "cores": cores,
+                             "kind": "oracle",
+                             "sample": sample + " per step, scaled to the workload"},
+            "e2e": {"value": round(value, 3), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["prefill", "decode", "long", "varlen", "tiny"],
+                    default="prefill")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode sub-benchmark")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, _ = dist_setup(args.gpus)
+    line = run_reference(args, world, rank) if args.impl == "reference" else \
+        run_ours(args, world, rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,154 @@
+/*
+ * kda.h -- C ABI of libkda, a single-GPU (sm_103a) implementation of the
+ * Kimi Delta Attention (KDA) operator.
+ *
+ * The operator, per sequence and head, with state S in R^{d_k x d_v}:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t                       (the read sees the token's own write)
+ *
+ * defined in "Kimi K3 的 KDA：1M context 不必把所有 KV 都留下" section 3,
+ * "Kimi K3模型架构详解" section 3.2 and "Kimi Delta Attention 完全拆解" (the KDA
+ * equations with the decayed state Diag(alpha) S and the per-token decode order).
+ * alpha_t = exp(log_alpha_t) is a per-key-channel gate; the library takes the
+ * gate in the log domain, as the pages' implementations do ("完全拆解": g holds
+ * log alpha and is accumulated with a cumulative sum before exponentiation).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is caller-owned DEVICE memory (cudaMalloc, a caching
+ *    allocator, ...), contiguous, row-major, 16-byte aligned.  The library
+ *    never allocates, frees or synchronises, except kda_read_device_status,
+ *    which synchronises the given stream to read the status word.
+ *  - `stream` is a cudaStream_t passed as void*; NULL selects the legacy
+ *    default stream.  All work is enqueued asynchronously on it.
+ *  - The state is fp32 and laid out [N, H, d_v, d_k] (key channel innermost):
+ *    memory element [n][h][v][c] holds the logical S[c][v].  This is the
+ *    [batch, heads, value_dim, key_dim] layout "Kimi K3 混合线性注意力" section 3
+ *    reports for FlashKDA.
+ *  - log_alpha and beta are fp32.  q, k, v and o are all of one dtype
+ *    (kda_dtype_t).  q and k are used as given; the pages put the L2
+ *    normalisation of q and k in the parameterisation before the operator
+ *    ("完全拆解", KDA layer parameterisation), so the caller applies it.
+ *  - Preconditions: log_alpha finite and <= 0 (alpha in (0, 1]); beta finite.
+ *  - Argument errors are reported by the return code before anything is
+ *    enqueued.  A failed kernel launch returns KDA_ERR_CUDA.  Conditions only
+ *    the GPU can see (see kda_fwd) set a status word in the workspace, read
+ *    with kda_read_device_status; the kernels never trap.
+ *  - Supported: d_k = d_v in {64, 128}.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, bad size, bad dtype */
+    KDA_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. d_k != d_v) */
+    KDA_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
+    KDA_ERR_CUDA = 4,             /* a CUDA call or kernel launch failed */
+    KDA_ERR_DOMAIN = 5            /* device status: input outside the supported domain */
+} kda_status_t;
+
+typedef enum {
+    KDA_F32 = 0,  /* q, k, v, o are float */
+    KDA_BF16 = 1  /* q, k, v, o are bfloat16 (round-to-nearest-even output) */
+} kda_dtype_t;
+
+typedef enum {
+    KDA_ENGINE_AUTO = 0,        /* tensor-core kernel where supported, else CUDA-core kernel */
+    KDA_ENGINE_TENSORCORE = 1,  /* tcgen05/TMEM/TMA kernel: bf16, d = 128 only */
+    KDA_ENGINE_CUDACORE = 2     /* fp32 CUDA-core chunkwise kernel: any supported dtype/d */
+} kda_engine_t;
+
+/* Bytes of workspace kda_fwd needs for N sequences (status word and the
+ * longest-first launch order).  Never zero; independent of T. */
+size_t kda_fwd_workspace_bytes(int N);
+
+/*
+ * kda_fwd -- chunkwise-parallel forward (prefill) over whole sequences.
+ *
+ * Computes o_t for every token and the final state S_T of every (sequence,
+ * head), starting from S0.  Execution form: 64-token chunks; within a chunk the
+ * cumulative log-decay, the WY/UT-style lower-triangular solve and the
+ * intra-chunk masked contractions run in parallel; between chunks the state
+ * is handed on, S <- Diag(gamma_C) S + (Gamma^{i->C} . K)^T (U - W S)
+ * ("完全拆解", chunkwise parallelism and the hardware-aware kernel;
+ * "Kimi K3 的 KDA" section 5; "Kimi K3模型架构详解" section 3.5).
+ *
+ * Layout (Ttot = B*T tokens, or the packed total with cu_seqlens):
+ *   q, k       [Ttot, H, d_k]   dtype          v, o  [Ttot, H, d_v]  dtype
+ *   log_alpha  [Ttot, H, d_k]   fp32           beta  [Ttot, H]       fp32
+ *   S0         [N, H, d_v, d_k] fp32, or NULL for a zero initial state
+ *   S_T        [N, H, d_v, d_k] fp32, or NULL to skip; may alias S0 exactly
+ *   cu_seqlens [N+1] int32 device offsets (cu_seqlens[0] = 0, non-decreasing,
+ *              cu_seqlens[N] = Ttot), or NULL for a fixed-length batch, in which
+ *              case N must equal B and sequence b owns tokens b*T .. b*T+T-1.
+ *   With cu_seqlens, pass B = 1 and T = Ttot.  Zero-length sequences are
+ *   allowed (S_T = S0).  Sequences never interact.
+ *   workspace  device memory of at least kda_fwd_workspace_bytes(N) bytes,
+ *              16-byte aligned; its contents on entry do not matter.
+ *
+ * Device status (kda_read_device_status): KDA_ERR_DOMAIN when, within some
+ * 64-token chunk, the cumulative log-decay of a channel leaves [-80, 80]
+ * (the chunk form scales keys by exp(-G) and would overflow fp32 there); the
+ * outputs of that head are then undefined.  KDA_ERR_INVALID_ARGUMENT when the
+ * device-side cu_seqlens is not non-decreasing or does not end at Ttot; no
+ * output is written then.
+ */
+kda_status_t kda_fwd(const void *q, const void *k, const void *v,
+                     const float *log_alpha, const float *beta, const float *S0,
+                     const int32_t *cu_seqlens, int B, int T, int H, int d_k, int d_v,
+                     int N, kda_dtype_t dtype, void *o, float *S_T,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* kda_fwd with an explicit engine choice (for tests and benchmarks).
+ * KDA_ERR_UNSUPPORTED if the engine cannot run this dtype/size. */
+kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
+                            const float *log_alpha, const float *beta, const float *S0,
+                            const int32_t *cu_seqlens, int B, int T, int H, int d_k,
+                            int d_v, int N, kda_dtype_t dtype, void *o, float *S_T,
+                            void *workspace, size_t workspace_bytes, void *stream,
+                            kda_engine_t engine);
+
+/*
+ * kda_decode_step -- one token for each of N sessions (the fused recurrent
+ * form "完全拆解" recommends for decode, in its per-token order: decay,
+ * old = Sbar^T k, S = Sbar + beta k (v - old)^T, o = S^T q).
+ *
+ *   q, k       [N, H, d_k] dtype      v, o  [N, H, d_v] dtype
+ *   log_alpha  [N, H, d_k] fp32       beta  [N, H]      fp32
+ *   S          [N, H, d_v, d_k] fp32, read and updated in place
+ * Reads and writes the state exactly once.  No workspace.
+ */
+kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta, float *S,
+                             int N, int H, int d_k, int d_v, kda_dtype_t dtype,
+                             void *o, void *stream);
+
+/* Synchronise `stream`, read the status word kda_fwd left in `workspace` and
+ * return it (KDA_OK if no condition was raised).  KDA_ERR_CUDA if the copy or
+ * the synchronisation fails. */
+kda_status_t kda_read_device_status(const void *workspace, size_t workspace_bytes,
+                                    void *stream);
+
+/* Bytes of recurrent state for `layers` KDA layers, N sessions, H heads and
+ * elem_bytes per element: layers * N * H * d_k * d_v * elem_bytes ("Kimi K3
+ * 混合线性注意力" section 3: 69 x 96 x 128 x 128 x 2 B per session).
+ * Returns 0 if any argument is negative or the product overflows. */
+size_t kda_state_bytes(int layers, int N, int H, int d_k, int d_v, int elem_bytes);
+
+/* Static, human-readable name of a status code. */
+const char *kda_status_string(kda_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,161 @@
+// Host side of the libkda C ABI: argument validation, engine choice and
+// launches.  Nothing here allocates, frees or synchronises (except
+// kda_read_device_status, whose job is to read a device word).
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "kda_internal.h"
+
+namespace {
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool fault_injected() {
+    // Host-only failure injection for tests of the error path: with
+    // KDA_FAULT_INJECT=launch the entry points report a launch failure
+    // without enqueueing anything.
+    const char *e = getenv("KDA_FAULT_INJECT");
+    return e && strcmp(e, "launch") == 0;
+}
+
+bool supported_dims(int dk, int dv) { return dk == dv && (dk == 64 || dk == 128); }
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_fwd_workspace_bytes(int N) {
+    const size_t n = N > 0 ? (size_t)N : 1;
+    return (kda::kWsOrderOffset + 4 * n + 15) & ~(size_t)15;
+}
+
+const char *kda_status_string(kda_status_t s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARGUMENT: return "KDA_ERR_INVALID_ARGUMENT";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_DOMAIN: return "KDA_ERR_DOMAIN";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+size_t kda_state_bytes(int layers, int N, int H, int d_k, int d_v, int elem_bytes) {
+    const int f[6] = {layers, N, H, d_k, d_v, elem_bytes};
+    size_t total = 1;
+    for (int i = 0; i < 6; ++i) {
+        if (f[i] < 0) return 0;
+        if (f[i] != 0 && total > SIZE_MAX / (size_t)f[i]) return 0;
+        total *= (size_t)f[i];
+    }
+    return total;
+}
+
+kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
+                            const float *log_alpha, const float *beta, const float *S0,
+                            const int32_t *cu_seqlens, int B, int T, int H, int d_k,
+                            int d_v, int N, kda_dtype_t dtype, void *o, float *S_T,
+                            void *workspace, size_t workspace_bytes, void *stream,
+                            kda_engine_t engine) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (engine != KDA_ENGINE_AUTO && engine != KDA_ENGINE_TENSORCORE &&
+        engine != KDA_ENGINE_CUDACORE)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (B < 0 || T < 0 || N < 0 || H <= 0 || d_k <= 0 || d_v <= 0)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (!supported_dims(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
+    if (cu_seqlens) {
+        if (B != 1) return KDA_ERR_INVALID_ARGUMENT;
+        if (((uintptr_t)cu_seqlens & 3u) != 0) return KDA_ERR_INVALID_ARGUMENT;
+    } else if (N != B) {
+        return KDA_ERR_INVALID_ARGUMENT;
+    }
+    const int64_t Ttot = (int64_t)B * T;
+    if ((int64_t)N * H > INT32_MAX) return KDA_ERR_INVALID_ARGUMENT;
+    if (Ttot > 0) {
+        if (!q || !k || !v || !log_alpha || !beta || !o) return KDA_ERR_INVALID_ARGUMENT;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+            !aligned16(beta) || !aligned16(o))
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T))) return KDA_ERR_INVALID_ARGUMENT;
+    if (!workspace || workspace_bytes < kda_fwd_workspace_bytes(N)) return KDA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return KDA_ERR_INVALID_ARGUMENT;
+
+    const bool tc_ok = kda::prefill_tc_supported(dtype, d_k, d_v);
+    if (engine == KDA_ENGINE_TENSORCORE && !tc_ok) return KDA_ERR_UNSUPPORTED;
+    const bool use_tc = engine == KDA_ENGINE_TENSORCORE || (engine == KDA_ENGINE_AUTO && tc_ok);
+    if (fault_injected()) return KDA_ERR_CUDA;
+
+    kda::FwdParams p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.log_alpha = log_alpha;
+    p.beta = beta;
+    p.S0 = S0;
+    p.cu_seqlens = cu_seqlens;
+    p.o = o;
+    p.S_T = S_T;
+    p.status = static_cast<int32_t *>(workspace);
+    p.order = cu_seqlens ? reinterpret_cast<const int32_t *>(
+                               static_cast<char *>(workspace) + kda::kWsOrderOffset)
+                         : nullptr;
+    p.Ttot = Ttot;
+    p.T = T;
+    p.H = H;
+    p.N = N;
+    p.dk = d_k;
+    p.dv = d_v;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (kda::launch_schedule(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (N == 0) return KDA_OK;
+    const cudaError_t e = use_tc ? kda::launch_prefill_tc(p, s)
+                                 : kda::launch_prefill_simt(p, dtype, s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                     const float *beta, const float *S0, const int32_t *cu_seqlens, int B,
+                     int T, int H, int d_k, int d_v, int N, kda_dtype_t dtype, void *o,
+                     float *S_T, void *workspace, size_t workspace_bytes, void *stream) {
+    return kda_fwd_engine(q, k, v, log_alpha, beta, S0, cu_seqlens, B, T, H, d_k, d_v, N,
+                          dtype, o, S_T, workspace, workspace_bytes, stream,
+                          KDA_ENGINE_AUTO);
+}
+
+kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta, float *S, int N,
+                             int H, int d_k, int d_v, kda_dtype_t dtype, void *o,
+                             void *stream) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (N < 0 || H <= 0 || d_k <= 0 || d_v <= 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!supported_dims(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)N * H > INT32_MAX) return KDA_ERR_INVALID_ARGUMENT;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !S || !o) return KDA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+        !aligned16(beta) || !aligned16(S) || !aligned16(o))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (fault_injected()) return KDA_ERR_CUDA;
+    const cudaError_t e = kda::launch_decode(q, k, v, log_alpha, beta, S, N, H, d_k, dtype, o,
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_read_device_status(const void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+    if (!workspace || workspace_bytes < 4) return KDA_ERR_WORKSPACE;
+    int32_t word = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    return static_cast<kda_status_t>(word);
+}
+
+}  // extern "C"

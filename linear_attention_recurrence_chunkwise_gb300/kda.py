@@ -1,0 +1,203 @@
+"""Thin Python binding of libkda: argument marshalling only.
+
+Every function here has the name of the C entry point it wraps and only turns
+torch tensors into device pointers (plus the current CUDA stream).  All of the
+operator's work runs in libkda's CUDA kernels; there is no other code path, and
+if the library is missing the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARGUMENT = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_WORKSPACE = 3
+KDA_ERR_CUDA = 4
+KDA_ERR_DOMAIN = 5
+
+KDA_F32, KDA_BF16 = 0, 1
+ENGINES = {"auto": 0, "tensorcore": 1, "cudacore": 2}
+
+# every symbol include/kda.h declares
+EXPORTED = ["kda_fwd_workspace_bytes", "kda_fwd", "kda_fwd_engine", "kda_decode_step",
+            "kda_read_device_status", "kda_state_bytes", "kda_status_string"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {kda_status_string(status)} ({status})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libkda.so (built by ``build.build()``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libkda.so not built at {LIB_PATH}; run "
+                               "linear_attention_recurrence_chunkwise_gb300.build.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, sz, ci, fp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p
+        lib.kda_fwd_workspace_bytes.restype = sz
+        lib.kda_fwd_workspace_bytes.argtypes = [ci]
+        fwd_args = [vp, vp, vp, fp, fp, fp, vp, ci, ci, ci, ci, ci, ci, ci, vp, fp, vp, sz, vp]
+        lib.kda_fwd.restype = ci
+        lib.kda_fwd.argtypes = fwd_args
+        lib.kda_fwd_engine.restype = ci
+        lib.kda_fwd_engine.argtypes = fwd_args + [ci]
+        lib.kda_decode_step.restype = ci
+        lib.kda_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, ci, ci, ci, ci, ci, vp, vp]
+        lib.kda_read_device_status.restype = ci
+        lib.kda_read_device_status.argtypes = [vp, sz, vp]
+        lib.kda_state_bytes.restype = sz
+        lib.kda_state_bytes.argtypes = [ci] * 6
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_status_string.argtypes = [ci]
+        _lib = lib
+        return lib
+
+
+def kda_status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def kda_state_bytes(layers: int, N: int, H: int, d_k: int, d_v: int, elem_bytes: int) -> int:
+    return int(load().kda_state_bytes(layers, N, H, d_k, d_v, elem_bytes))
+
+
+def kda_fwd_workspace_bytes(N: int) -> int:
+    return int(load().kda_fwd_workspace_bytes(N))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(dt) -> int:
+    if dt == torch.bfloat16:
+        return KDA_BF16
+    if dt == torch.float32:
+        return KDA_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {dt}")
+
+
+def _check(t, name, dtype=None, device=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def kda_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, o=None, S_T=None,
+            workspace=None, return_state: bool = True, engine: str = "auto", stream=None):
+    """Chunkwise KDA forward (prefill).
+
+    q, k, log_alpha [B, T, H, d_k] or packed [Ttot, H, d_k]; v [.., H, d_v];
+    beta [.., H]; S0 [N, H, d_v, d_k] fp32 or None; cu_seqlens int32 [N+1]
+    (device) or None.  Returns (o, S_T) (S_T None when return_state is False).
+    Output tensors and the workspace are allocated with torch unless given.
+    """
+    dev = q.device
+    dt = q.dtype
+    _check(q, "q", dt), _check(k, "k", dt, dev), _check(v, "v", dt, dev)
+    _check(log_alpha, "log_alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    _check(S0, "S0", torch.float32, dev)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    H, d_k = q.shape[-2], q.shape[-1]
+    d_v = v.shape[-1]
+    if cu_seqlens is not None:
+        if q.dim() != 3:
+            raise ValueError("with cu_seqlens, q must be packed [Ttot, H, d_k]")
+        B, T = 1, q.shape[0]
+        N = cu_seqlens.numel() - 1
+    else:
+        if q.dim() == 4:
+            B, T = q.shape[0], q.shape[1]
+        elif q.dim() == 3:
+            B, T = 1, q.shape[0]
+        else:
+            raise ValueError("q must be [B, T, H, d_k] or [Ttot, H, d_k]")
+        N = B
+    if k.shape != q.shape or log_alpha.shape != q.shape or v.shape[:-1] != q.shape[:-1] \
+            or beta.shape != q.shape[:-1]:
+        raise ValueError("q, k, v, log_alpha, beta shapes disagree")
+    if o is None:
+        o = torch.empty(v.shape, dtype=dt, device=dev)
+    _check(o, "o", dt, dev)
+    if S_T is None and return_state:
+        S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=dev)
+    _check(S_T, "S_T", torch.float32, dev)
+    if workspace is None:
+        workspace = torch.empty(kda_fwd_workspace_bytes(N), dtype=torch.uint8, device=dev)
+    _check(workspace, "workspace", None, dev)
+    lib = load()
+    rc = lib.kda_fwd_engine(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                            _ptr(S0), _ptr(cu_seqlens), B, T, H, d_k, d_v, N,
+                            _dtype_code(dt), _ptr(o), _ptr(S_T), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream),
+                            ENGINES[engine])
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_fwd")
+    return o, S_T
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, S, *, o=None, stream=None):
+    """One decode token per session; S [N, H, d_v, d_k] fp32 is updated in place.
+
+    q, k, log_alpha [N, H, d_k]; v [N, H, d_v]; beta [N, H].  Returns o [N, H, d_v].
+    """
+    dev = q.device
+    dt = q.dtype
+    _check(q, "q", dt), _check(k, "k", dt, dev), _check(v, "v", dt, dev)
+    _check(log_alpha, "log_alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    _check(S, "S", torch.float32, dev)
+    N, H, d_k = q.shape
+    d_v = v.shape[-1]
+    if S.shape != (N, H, d_v, d_k):
+        raise ValueError(f"S must be [N, H, d_v, d_k] = {(N, H, d_v, d_k)}")
+    if o is None:
+        o = torch.empty((N, H, d_v), dtype=dt, device=dev)
+    _check(o, "o", dt, dev)
+    rc = load().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                _ptr(S), N, H, d_k, d_v, _dtype_code(dt), _ptr(o),
+                                _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step")
+    return o
+
+
+def kda_read_device_status(workspace, stream=None) -> int:
+    """Synchronise the stream and return the status word left by kda_fwd."""
+    rc = load().kda_read_device_status(_ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream))
+    return int(rc)

@@ -1,0 +1,134 @@
+"""libkda host-side checks that need no GPU: symbols, accounting, argument errors.
+
+No call here reaches a CUDA API: every call is rejected by host validation (or
+by the host-only failure-injection hook) before anything would be enqueued.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_recurrence_chunkwise_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kda():
+    kbuild.build()
+    from linear_attention_recurrence_chunkwise_gb300 import kda as mod
+    mod.load()
+    return mod
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(kda):
+    declared = header_functions()
+    assert declared, "no functions parsed from include/kda.h"
+    lib = kda.load()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(kda.EXPORTED) == declared
+
+
+def test_state_bytes_matches_pages(kda):
+    for line in open(os.path.join(ROOT, "tests", "golden", "state_bytes.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = dict(kv.split("=") for kv in line.split())
+        got = kda.kda_state_bytes(int(f["layers"]), int(f["N"]), int(f["H"]), int(f["dk"]),
+                                  int(f["dv"]), int(f["elem"]))
+        assert got == int(f["bytes"]), line
+
+
+def test_state_bytes_edge_cases(kda):
+    assert kda.kda_state_bytes(69, 1, 96, 128, 128, 4) == 2 * 217055232
+    assert kda.kda_state_bytes(0, 5, 96, 128, 128, 4) == 0
+    assert kda.kda_state_bytes(-1, 1, 1, 1, 1, 1) == 0
+    assert kda.kda_state_bytes(2**31 - 1, 2**31 - 1, 2**31 - 1, 2**31 - 1, 2**31 - 1, 4) == 0
+
+
+def test_status_strings(kda):
+    for code, name in [(0, "KDA_OK"), (1, "KDA_ERR_INVALID_ARGUMENT"), (2, "KDA_ERR_UNSUPPORTED"),
+                       (3, "KDA_ERR_WORKSPACE"), (4, "KDA_ERR_CUDA"), (5, "KDA_ERR_DOMAIN")]:
+        assert kda.kda_status_string(code) == name
+
+
+def test_workspace_bytes(kda):
+    assert kda.kda_fwd_workspace_bytes(0) >= 16
+    for n in (1, 16, 1000):
+        b = kda.kda_fwd_workspace_bytes(n)
+        assert b >= 16 + 4 * n and b % 16 == 0
+
+
+# fake, never dereferenced, 16-byte aligned device addresses
+P = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(12)]
+
+
+def fwd_call(lib, **kw):
+    a = dict(q=P[0], k=P[1], v=P[2], la=P[3], beta=P[4], S0=None, cu=None, B=1, T=64, H=2,
+             dk=64, dv=64, N=1, dt=0, o=P[5], ST=P[6], ws=P[7], wsb=4096, stream=None,
+             engine=0)
+    a.update(kw)
+    return lib.kda_fwd_engine(a["q"], a["k"], a["v"], a["la"], a["beta"], a["S0"], a["cu"],
+                              a["B"], a["T"], a["H"], a["dk"], a["dv"], a["N"], a["dt"],
+                              a["o"], a["ST"], a["ws"], a["wsb"], a["stream"], a["engine"])
+
+
+def test_fwd_argument_errors(kda):
+    lib = kda.load()
+    E_INV, E_UNS, E_WS = 1, 2, 3
+    assert fwd_call(lib, q=None) == E_INV
+    assert fwd_call(lib, q=ctypes.c_void_p(0x10008)) == E_INV          # misaligned
+    assert fwd_call(lib, S0=ctypes.c_void_p(0x10004)) == E_INV
+    assert fwd_call(lib, dt=7) == E_INV
+    assert fwd_call(lib, H=0) == E_INV
+    assert fwd_call(lib, T=-1) == E_INV
+    assert fwd_call(lib, N=2) == E_INV                                # N != B without cu_seqlens
+    assert fwd_call(lib, cu=P[8], B=2, N=2) == E_INV                   # varlen needs B = 1
+    assert fwd_call(lib, cu=ctypes.c_void_p(0x10002)) == E_INV         # misaligned offsets
+    assert fwd_call(lib, dk=96, dv=96) == E_UNS
+    assert fwd_call(lib, dk=64, dv=128) == E_UNS
+    assert fwd_call(lib, ws=None) == E_WS
+    assert fwd_call(lib, wsb=8) == E_WS
+    assert fwd_call(lib, engine=9) == E_INV
+    assert fwd_call(lib, engine=1, dt=0) == E_UNS                      # tensor cores: bf16 only
+
+
+def test_decode_argument_errors(kda):
+    lib = kda.load()
+
+    def call(**kw):
+        a = dict(q=P[0], k=P[1], v=P[2], la=P[3], beta=P[4], S=P[5], N=4, H=2, dk=128, dv=128,
+                 dt=1, o=P[6], stream=None)
+        a.update(kw)
+        return lib.kda_decode_step(a["q"], a["k"], a["v"], a["la"], a["beta"], a["S"], a["N"],
+                                   a["H"], a["dk"], a["dv"], a["dt"], a["o"], a["stream"])
+    assert call(S=None) == 1
+    assert call(o=ctypes.c_void_p(0x10001)) == 1
+    assert call(dk=32, dv=32) == 2
+    assert call(N=-1) == 1
+    assert call(N=0, S=None) == 0  # nothing to do
+
+
+def test_failure_injection_reports_cuda_error(kda, monkeypatch):
+    """The host-only injection hook turns a valid call into KDA_ERR_CUDA
+    without enqueueing anything."""
+    lib = kda.load()
+    monkeypatch.setenv("KDA_FAULT_INJECT", "launch")
+    assert fwd_call(lib) == 4
+    assert lib.kda_decode_step(P[0], P[1], P[2], P[3], P[4], P[5], 1, 1, 64, 64, 0, P[6],
+                               None) == 4
+
+
+def test_binding_rejects_cpu_tensors(kda):
+    import torch
+    x = torch.zeros(1, 64, 2, 64)
+    with pytest.raises(ValueError):
+        kda.kda_fwd(x, x, x, x, torch.zeros(1, 64, 2))

@@ -1,0 +1,303 @@
+"""GPU parity: libkda against the fp64 oracle on the same seeded inputs.
+
+Small cases span several 64-token chunks and a ragged tail; the workload
+cases run the full problem sizes on the GPU and compare the heads (or
+sessions) the oracle can afford, sampled by a seeded permutation.
+Tolerances (max-abs error / max |reference|): fp32 inputs 1e-4 on o and S;
+bf16 inputs 2e-2 on o and 1e-2 on the final state.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_recurrence_chunkwise_gb300 import build as kbuild
+from linear_attention_recurrence_chunkwise_gb300 import inputs as I
+from tests.gpu_util import oracle_on_heads, rel_err, tol_o, tol_s
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+ENGINES = ["cudacore", "tensorcore"]
+
+
+@pytest.fixture(scope="module")
+def kda():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    kbuild.build()
+    from linear_attention_recurrence_chunkwise_gb300 import kda as mod
+    mod.load()
+    return mod
+
+
+def engine_ok(engine, dtype, d):
+    return engine != "tensorcore" or (dtype == "bf16" and d == 128)
+
+
+def run_fwd(kda, prob, engine, **kw):
+    o, ST = kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0,
+                        prob.cu_seqlens, engine=engine, **kw)
+    torch.cuda.synchronize()
+    return o, ST
+
+
+# --------------------------------------------------------------- prefill, small
+
+@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 333])
+def test_prefill_small(kda, engine, dtype, d, T):
+    if not engine_ok(engine, dtype, d):
+        pytest.skip("engine does not take this dtype/size")
+    prob = I.prefill_problem(2, T, 3, d, d, dtype, (-0.5, -0.001), 0.05, seed=T + d,
+                             device=DEV)
+    o, ST = run_fwd(kda, prob, engine)
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2])
+    dt = prob.q.dtype
+    assert rel_err(o, o_ref) < tol_o(dt)
+    assert rel_err(ST, S_ref) < tol_s(dt)
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_prefill_varlen_small(kda, engine):
+    lengths = [0, 1, 64, 130, 7, 0, 257, 63]
+    prob = I.prefill_problem(1, 0, 4, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=3,
+                             device=DEV, lengths=lengths)
+    o, ST = run_fwd(kda, prob, engine)
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2, 3])
+    assert rel_err(o, o_ref) < 2e-2
+    assert rel_err(ST, S_ref) < 1e-2
+    # empty sequences hand their initial state straight through
+    for i, L in enumerate(lengths):
+        if L == 0:
+            assert torch.equal(ST[i], prob.S0[i])
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_varlen_isolation_bit_identical(kda, engine):
+    """Reordering the packed sequences leaves each one's o and S_T bit-identical."""
+    lengths = [100, 5, 64, 300]
+    prob = I.prefill_problem(1, 0, 2, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=4,
+                             device=DEV, lengths=lengths)
+    o, ST = run_fwd(kda, prob, engine)
+    cu = prob.cu_seqlens.cpu().tolist()
+    perm = [3, 1, 0, 2]
+    cat = lambda t: torch.cat([t[cu[i]:cu[i + 1]] for i in perm])
+    cu_p = torch.tensor([0] + list(np.cumsum([lengths[i] for i in perm])), dtype=torch.int32,
+                        device=DEV)
+    prob_p = I.Problem(cat(prob.q), cat(prob.k), cat(prob.v), cat(prob.log_alpha),
+                       cat(prob.beta), prob.S0[perm].contiguous(), cu_p)
+    o_p, ST_p = run_fwd(kda, prob_p, engine)
+    assert torch.equal(ST_p, ST[perm])
+    assert torch.equal(o_p, cat(o))
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_split_run_matches_whole(kda, engine):
+    """fwd(T1) then fwd(T2, S0 = S_T1) agrees with fwd(T1 + T2)."""
+    prob = I.prefill_problem(1, 500, 3, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=5,
+                             device=DEV)
+    o, ST = run_fwd(kda, prob, engine)
+    a = I.Problem(prob.q[:, :170].contiguous(), prob.k[:, :170].contiguous(),
+                  prob.v[:, :170].contiguous(), prob.log_alpha[:, :170].contiguous(),
+                  prob.beta[:, :170].contiguous(), prob.S0, None)
+    o1, S1 = run_fwd(kda, a, engine)
+    b = I.Problem(prob.q[:, 170:].contiguous(), prob.k[:, 170:].contiguous(),
+                  prob.v[:, 170:].contiguous(), prob.log_alpha[:, 170:].contiguous(),
+                  prob.beta[:, 170:].contiguous(), S1, None)
+    o2, S2 = run_fwd(kda, b, engine)
+    assert rel_err(torch.cat([o1, o2], 1), o.double().cpu().numpy()) < 2e-2
+    assert rel_err(S2, ST.double().cpu().numpy()) < 1e-2
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_state_in_place_and_optional_outputs(kda, engine):
+    prob = I.prefill_problem(2, 150, 2, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=6,
+                             device=DEV)
+    o, ST = run_fwd(kda, prob, engine)
+    S = prob.S0.clone()
+    o2, S_ret = kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, S, None,
+                            S_T=S, engine=engine)        # S_T aliases S0
+    torch.cuda.synchronize()
+    assert S_ret.data_ptr() == S.data_ptr()
+    assert torch.equal(S, ST) and torch.equal(o2, o)
+    o3, none = kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0, None,
+                           return_state=False, engine=engine)
+    torch.cuda.synchronize()
+    assert none is None and torch.equal(o3, o)
+    zero = I.Problem(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, None, None)
+    oz, Sz = run_fwd(kda, zero, engine)
+    zref = I.Problem(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta,
+                     torch.zeros_like(prob.S0), None)
+    oz2, Sz2 = run_fwd(kda, zref, engine)
+    assert torch.equal(oz, oz2) and torch.equal(Sz, Sz2)
+
+
+def test_prefill_equals_decode_steps(kda):
+    """The chunkwise prefill and T single-token decode steps agree (same causal
+    semantics: a token reads the state after its own write)."""
+    prob = I.prefill_problem(1, 96, 2, 128, 128, "f32", (-0.5, -0.001), 0.05, seed=7,
+                             device=DEV)
+    o, ST = run_fwd(kda, prob, "cudacore")
+    S = prob.S0.clone()
+    outs = []
+    for t in range(96):
+        outs.append(kda.kda_decode_step(prob.q[:, t].contiguous(), prob.k[:, t].contiguous(),
+                                        prob.v[:, t].contiguous(),
+                                        prob.log_alpha[:, t].contiguous(),
+                                        prob.beta[:, t].contiguous(), S))
+    torch.cuda.synchronize()
+    assert rel_err(torch.stack(outs, 1), o.double().cpu().numpy()) < 1e-4
+    assert rel_err(S, ST.double().cpu().numpy()) < 1e-4
+
+
+def test_zero_sizes(kda):
+    e = torch.empty(0, 2, 64, device=DEV)
+    o, ST = kda.kda_fwd(e, e, e, e, torch.empty(0, 2, device=DEV), None,
+                        torch.zeros(1, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    assert o.numel() == 0 and ST.shape == (0, 2, 64, 64)
+
+
+def test_domain_status(kda):
+    """A gate far below the supported chunk log-decay range is reported."""
+    prob = I.prefill_problem(1, 128, 1, 128, 128, "bf16", (-5.0, -4.0), None, seed=8,
+                             device=DEV)
+    ws = torch.zeros(kda.kda_fwd_workspace_bytes(1), dtype=torch.uint8, device=DEV)
+    kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, workspace=ws)
+    assert kda.kda_read_device_status(ws) == kda.KDA_ERR_DOMAIN
+    ok = I.prefill_problem(1, 128, 1, 128, 128, "bf16", (-0.5, -0.001), None, seed=8,
+                           device=DEV)
+    kda.kda_fwd(ok.q, ok.k, ok.v, ok.log_alpha, ok.beta, workspace=ws)
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK
+
+
+def test_bad_device_offsets_write_nothing(kda):
+    prob = I.prefill_problem(1, 0, 2, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=9,
+                             device=DEV, lengths=[50, 50])
+    bad = torch.tensor([0, 70, 60], dtype=torch.int32, device=DEV)   # decreasing
+    o = torch.full_like(prob.v, 7.0)
+    ST = torch.full_like(prob.S0, 7.0)
+    ws = torch.zeros(kda.kda_fwd_workspace_bytes(2), dtype=torch.uint8, device=DEV)
+    kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0, bad, o=o, S_T=ST,
+                workspace=ws)
+    assert kda.kda_read_device_status(ws) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert bool((o == 7.0).all()) and bool((ST == 7.0).all())
+    short = torch.tensor([0, 50, 90], dtype=torch.int32, device=DEV)  # does not end at Ttot
+    kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0, short, o=o,
+                S_T=ST, workspace=ws)
+    assert kda.kda_read_device_status(ws) == kda.KDA_ERR_INVALID_ARGUMENT
+
+
+# --------------------------------------------------------------- decode, small
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_small(kda, dtype, d):
+    N, H, steps = 3, 5, 20
+    S = I.decode_state(N, H, d, d, 0.05, seed=d, device=DEV)
+    S_ref = S.double().cpu().numpy()
+    for s in range(steps):
+        x = I.decode_token(N, H, d, d, dtype, (-0.1, -0.0005), seed=d, step=s, device=DEV)
+        o = kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S)
+        o_ref, S_ref = oracle.decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                          S_ref)
+        torch.cuda.synchronize()
+        assert rel_err(o, o_ref) < tol_o(x["q"].dtype)
+    assert rel_err(S, S_ref) < (1e-4 if dtype == "f32" else 1e-2)
+
+
+# --------------------------------------------------------------- workload sizes
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_workload_tiny_fp32(kda, engine):
+    """B=1, H=2, T=256, d=64, fp32: every element against the oracle at 1e-4."""
+    if not engine_ok(engine, "f32", 64):
+        pytest.skip("tensor-core engine takes bf16, d = 128 only")
+    prob = I.preset_problem("tiny", seed=0, device=DEV)
+    o, ST = run_fwd(kda, prob, engine)
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1])
+    assert rel_err(o, o_ref) < 1e-4
+    assert rel_err(ST, S_ref) < 1e-4
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_workload_prefill_sampled_heads(kda, engine):
+    """B=1, H=96, T=8192, d=128, bf16: 6 sampled heads against the oracle."""
+    prob = I.preset_problem("prefill", seed=0, device=DEV)
+    o, ST = run_fwd(kda, prob, engine)
+    heads = I.sampled_heads(96, 6, seed=0)
+    o_ref, S_ref = oracle_on_heads(prob, heads)
+    idx = torch.tensor(heads, device=DEV)
+    assert rel_err(o.index_select(2, idx), o_ref) < 2e-2
+    assert rel_err(ST.index_select(1, idx), S_ref) < 1e-2
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(ST).all())
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_workload_long_sampled_heads(kda, engine):
+    """B=1, H=96, T=131072, nonzero S0, long-memory gates: 4 sampled heads."""
+    prob = I.preset_problem("long", seed=0, device=DEV)
+    o, ST = run_fwd(kda, prob, engine)
+    heads = I.sampled_heads(96, 4, seed=0)
+    o_ref, S_ref = oracle_on_heads(prob, heads)
+    idx = torch.tensor(heads, device=DEV)
+    assert rel_err(o.index_select(2, idx), o_ref) < 2e-2
+    assert rel_err(ST.index_select(1, idx), S_ref) < 1e-2
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(ST).all())
+
+
+def test_workload_decode_sampled_sessions(kda):
+    """64 sessions x 96 heads, fp32 state, 1000 in-place steps: 12 sampled
+    (session, head) pairs follow the oracle step by step."""
+    p = I.PRESETS["decode"]
+    N, H, d = p["N"], p["H"], p["d"]
+    S = I.decode_state(N, H, d, d, p["s0_std"], seed=0, device=DEV)
+    g = torch.Generator().manual_seed(1)
+    pairs = [(int(n), int(h)) for n, h in zip(torch.randint(0, N, (12,), generator=g),
+                                              torch.randint(0, H, (12,), generator=g))]
+    ns = torch.tensor([a for a, _ in pairs], device=DEV)
+    hs = torch.tensor([b for _, b in pairs], device=DEV)
+    S_ref = S[ns, hs].double().cpu().numpy()[:, None]          # [12, 1, d, d]
+    worst = 0.0
+    for s in range(p["steps"]):
+        x = I.decode_token(N, H, d, d, p["dtype"], p["la"], seed=0, step=s, device=DEV)
+        o = kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S)
+        pick = lambda t: t[ns, hs][:, None]
+        o_ref, S_ref = oracle.decode_step(pick(x["q"]), pick(x["k"]), pick(x["v"]),
+                                          pick(x["log_alpha"]), pick(x["beta"]), S_ref)
+        worst = max(worst, rel_err(o[ns, hs], o_ref[:, 0]))
+    torch.cuda.synchronize()
+    assert worst < 2e-2
+    assert rel_err(S[ns, hs], S_ref[:, 0]) < 1e-2
+    assert bool(torch.isfinite(S).all())
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_workload_varlen_then_decode(kda, engine):
+    """16 packed sequences (lengths log-uniform in [1024, 65536]), H=96, bf16,
+    per-sequence S0; then 256 decode steps per sequence from the returned
+    states.  Two sampled heads of every sequence follow the oracle."""
+    p = I.PRESETS["varlen"]
+    prob = I.preset_problem("varlen", seed=0, device=DEV)
+    o, ST = run_fwd(kda, prob, engine)
+    heads = I.sampled_heads(p["H"], 2, seed=0)
+    o_ref, S_ref = oracle_on_heads(prob, heads)
+    idx = torch.tensor(heads, device=DEV)
+    assert rel_err(o.index_select(1, idx), o_ref) < 2e-2
+    assert rel_err(ST.index_select(1, idx), S_ref) < 1e-2
+    N, H, d = p["n_seq"], p["H"], p["d"]
+    S = ST.clone()
+    S_o = S_ref
+    worst = 0.0
+    for s in range(p["decode_steps"]):
+        x = I.decode_token(N, H, d, d, p["dtype"], p["la"], seed=1, step=s, device=DEV)
+        od = kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S)
+        pick = lambda t: t.index_select(1, idx)
+        od_ref, S_o = oracle.decode_step(pick(x["q"]), pick(x["k"]), pick(x["v"]),
+                                         pick(x["log_alpha"]), pick(x["beta"]), S_o)
+        worst = max(worst, rel_err(od.index_select(1, idx), od_ref))
+    torch.cuda.synchronize()
+    assert worst < 2e-2
+    assert rel_err(S.index_select(1, idx), S_o) < 1e-2
