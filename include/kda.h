@@ -17,7 +17,10 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every tensor pointer is caller-owned DEVICE memory (cudaMalloc, a caching
- *    allocator, ...), contiguous, row-major, 16-byte aligned.  The library
+ *    allocator, ...), contiguous and row-major.  kda_fwd needs q, k, v,
+ *    log_alpha, o, S0, S_T and the workspace 16-byte aligned; beta and
+ *    cu_seqlens need their natural (4-byte) alignment.  kda_decode_step needs
+ *    S 16-byte aligned and the per-token vectors naturally aligned.  The library
  *    never allocates, frees or synchronises, except kda_read_device_status,
  *    which synchronises the given stream to read the status word.
  *  - `stream` is a cudaStream_t passed as void*; NULL selects the legacy

@@ -10,6 +10,7 @@
 namespace {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned(const void *p, unsigned bytes) { return ((uintptr_t)p & (bytes - 1)) == 0; }
 
 bool fault_injected() {
     // Host-only failure injection for tests of the error path: with
@@ -77,7 +78,7 @@ kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
     if (Ttot > 0) {
         if (!q || !k || !v || !log_alpha || !beta || !o) return KDA_ERR_INVALID_ARGUMENT;
         if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
-            !aligned16(beta) || !aligned16(o))
+            !aligned(beta, 4) || !aligned16(o))
             return KDA_ERR_INVALID_ARGUMENT;
     }
     if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T))) return KDA_ERR_INVALID_ARGUMENT;
@@ -137,8 +138,9 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
     if ((int64_t)N * H > INT32_MAX) return KDA_ERR_INVALID_ARGUMENT;
     if (N == 0) return KDA_OK;
     if (!q || !k || !v || !log_alpha || !beta || !S || !o) return KDA_ERR_INVALID_ARGUMENT;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
-        !aligned16(beta) || !aligned16(S) || !aligned16(o))
+    const unsigned elem = dtype == KDA_BF16 ? 2u : 4u;
+    if (!aligned(q, elem) || !aligned(k, elem) || !aligned(v, elem) || !aligned(o, elem) ||
+        !aligned(log_alpha, 4) || !aligned(beta, 4) || !aligned16(S))
         return KDA_ERR_INVALID_ARGUMENT;
     if (fault_injected()) return KDA_ERR_CUDA;
     const cudaError_t e = kda::launch_decode(q, k, v, log_alpha, beta, S, N, H, d_k, dtype, o,

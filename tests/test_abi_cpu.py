@@ -87,6 +87,8 @@ def test_fwd_argument_errors(kda):
     assert fwd_call(lib, q=None) == E_INV
     assert fwd_call(lib, q=ctypes.c_void_p(0x10008)) == E_INV          # misaligned
     assert fwd_call(lib, S0=ctypes.c_void_p(0x10004)) == E_INV
+    assert fwd_call(lib, beta=ctypes.c_void_p(0x10002)) == E_INV      # beta: 4-byte aligned
+    assert fwd_call(lib, beta=ctypes.c_void_p(0x10004), ws=None) == E_WS  # 4 B is enough
     assert fwd_call(lib, dt=7) == E_INV
     assert fwd_call(lib, H=0) == E_INV
     assert fwd_call(lib, T=-1) == E_INV
@@ -111,7 +113,8 @@ def test_decode_argument_errors(kda):
         return lib.kda_decode_step(a["q"], a["k"], a["v"], a["la"], a["beta"], a["S"], a["N"],
                                    a["H"], a["dk"], a["dv"], a["dt"], a["o"], a["stream"])
     assert call(S=None) == 1
-    assert call(o=ctypes.c_void_p(0x10001)) == 1
+    assert call(o=ctypes.c_void_p(0x10001)) == 1                     # odd bf16 address
+    assert call(S=ctypes.c_void_p(0x10008)) == 1                     # state needs 16 B
     assert call(dk=32, dv=32) == 2
     assert call(N=-1) == 1
     assert call(N=0, S=None) == 0  # nothing to do
