@@ -56,7 +56,8 @@ typedef enum {
     KDA_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. d_k != d_v) */
     KDA_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
     KDA_ERR_CUDA = 4,             /* a CUDA call or kernel launch failed */
-    KDA_ERR_DOMAIN = 5            /* device status: input outside the supported domain */
+    KDA_ERR_DOMAIN = 5,           /* device status: input outside the supported domain */
+    KDA_ERR_TIMEOUT = 6           /* device status: a kernel wait gave up (not expected) */
 } kda_status_t;
 
 typedef enum {
@@ -103,7 +104,9 @@ size_t kda_fwd_workspace_bytes(int N);
  * (the chunk form scales keys by exp(-G) and would overflow fp32 there); the
  * outputs of that head are then undefined.  KDA_ERR_INVALID_ARGUMENT when the
  * device-side cu_seqlens is not non-decreasing or does not end at Ttot; no
- * output is written then.
+ * output is written then.  KDA_ERR_TIMEOUT if a wait inside the tensor-core
+ * kernel exceeded its time limit (outputs undefined; the kernel still exits
+ * and releases its resources).
  */
 kda_status_t kda_fwd(const void *q, const void *k, const void *v,
                      const float *log_alpha, const float *beta, const float *S0,

@@ -39,6 +39,7 @@ const char *kda_status_string(kda_status_t s) {
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
         case KDA_ERR_DOMAIN: return "KDA_ERR_DOMAIN";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
     }
     return "KDA_ERR_UNKNOWN";
 }
@@ -85,7 +86,7 @@ kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
     if (!workspace || workspace_bytes < kda_fwd_workspace_bytes(N)) return KDA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KDA_ERR_INVALID_ARGUMENT;
 
-    const bool tc_ok = kda::prefill_tc_supported(dtype, d_k, d_v);
+    const bool tc_ok = kda::prefill_tc_supported(dtype, d_k, d_v) && Ttot <= INT32_MAX;
     if (engine == KDA_ENGINE_TENSORCORE && !tc_ok) return KDA_ERR_UNSUPPORTED;
     const bool use_tc = engine == KDA_ENGINE_TENSORCORE || (engine == KDA_ENGINE_AUTO && tc_ok);
     if (fault_injected()) return KDA_ERR_CUDA;

@@ -22,6 +22,7 @@ KDA_ERR_UNSUPPORTED = 2
 KDA_ERR_WORKSPACE = 3
 KDA_ERR_CUDA = 4
 KDA_ERR_DOMAIN = 5
+KDA_ERR_TIMEOUT = 6
 
 KDA_F32, KDA_BF16 = 0, 1
 ENGINES = {"auto": 0, "tensorcore": 1, "cudacore": 2}

@@ -56,7 +56,8 @@ def test_state_bytes_edge_cases(kda):
 
 def test_status_strings(kda):
     for code, name in [(0, "KDA_OK"), (1, "KDA_ERR_INVALID_ARGUMENT"), (2, "KDA_ERR_UNSUPPORTED"),
-                       (3, "KDA_ERR_WORKSPACE"), (4, "KDA_ERR_CUDA"), (5, "KDA_ERR_DOMAIN")]:
+                       (3, "KDA_ERR_WORKSPACE"), (4, "KDA_ERR_CUDA"), (5, "KDA_ERR_DOMAIN"),
+                       (6, "KDA_ERR_TIMEOUT")]:
         assert kda.kda_status_string(code) == name
 
 
