@@ -123,6 +123,39 @@ kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
                             void *workspace, size_t workspace_bytes, void *stream,
                             kda_engine_t engine);
 
+/* Largest N kda_fwd_noalloc accepts. */
+#define KDA_NOALLOC_MAX_SEQS 16384
+
+/*
+ * kda_fwd_noalloc -- kda_fwd for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it is a convenience of
+ * the library.  kda_fwd asks its caller for a workspace.  Callers that cannot
+ * allocate -- code running where allocation is not allowed (a host callback on
+ * a stream), a plugin inside a runtime that owns every device allocation, an
+ * embedding without an allocator -- use this variant instead: it keeps the
+ * scratch (status word and launch order) in a fixed 65,552-byte array in the
+ * library's device memory, which every GPU that loads the library holds until
+ * the process exits.  It calls no allocating routine.
+ *
+ * Arguments are those of kda_fwd without the workspace, plus `device_status`:
+ * an optional (nullable, 4-byte aligned) device int32 that receives the
+ * call's device status word (see kda_fwd) on `stream`.  The engine is chosen
+ * as in kda_fwd.  N > KDA_NOALLOC_MAX_SEQS returns KDA_ERR_WORKSPACE before
+ * anything is enqueued.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  Every call shares the one array: calls that follow one
+ * another are independent (each clears what must start at zero), but calls
+ * that overlap on the GPU -- for example on two streams at once -- race.
+ */
+kda_status_t kda_fwd_noalloc(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta, const float *S0,
+                             const int32_t *cu_seqlens, int B, int T, int H, int d_k, int d_v,
+                             int N, kda_dtype_t dtype, void *o, float *S_T,
+                             int32_t *device_status, void *stream);
+
 /*
  * kda_decode_step -- one token for each of N sessions (the fused recurrent
  * form "完全拆解" recommends for decode, in its per-token order: decay,

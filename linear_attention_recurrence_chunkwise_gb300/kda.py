@@ -28,8 +28,10 @@ KDA_F32, KDA_BF16 = 0, 1
 ENGINES = {"auto": 0, "tensorcore": 1, "cudacore": 2}
 
 # every symbol include/kda.h declares
-EXPORTED = ["kda_fwd_workspace_bytes", "kda_fwd", "kda_fwd_engine", "kda_decode_step",
-            "kda_read_device_status", "kda_state_bytes", "kda_status_string"]
+EXPORTED = ["kda_fwd_workspace_bytes", "kda_fwd", "kda_fwd_engine", "kda_fwd_noalloc",
+            "kda_decode_step", "kda_read_device_status", "kda_state_bytes",
+            "kda_status_string"]
+KDA_NOALLOC_MAX_SEQS = 16384
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +61,8 @@ def load() -> ctypes.CDLL:
         lib.kda_fwd.argtypes = fwd_args
         lib.kda_fwd_engine.restype = ci
         lib.kda_fwd_engine.argtypes = fwd_args + [ci]
+        lib.kda_fwd_noalloc.restype = ci
+        lib.kda_fwd_noalloc.argtypes = fwd_args[:16] + [vp, vp]
         lib.kda_decode_step.restype = ci
         lib.kda_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, ci, ci, ci, ci, ci, vp, vp]
         lib.kda_read_device_status.restype = ci
@@ -167,6 +171,48 @@ def kda_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, o=None, S_T=N
                             ENGINES[engine])
     if rc != KDA_OK:
         raise KdaError(rc, "kda_fwd")
+    return o, S_T
+
+
+def kda_fwd_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, o=None,
+                    S_T=None, device_status=None, stream=None):
+    """kda_fwd for callers that cannot allocate device memory.
+
+    The library keeps the scratch kda_fwd would take as a workspace in a fixed
+    array of its own; only inputs and outputs are passed (o and S_T are
+    allocated with torch here when not given, which callers that cannot
+    allocate avoid by passing them).  `device_status` is an optional device
+    int32 tensor that receives the call's status word.  Returns (o, S_T).
+    """
+    dev = q.device
+    dt = q.dtype
+    _check(q, "q", dt), _check(k, "k", dt, dev), _check(v, "v", dt, dev)
+    _check(log_alpha, "log_alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    _check(S0, "S0", torch.float32, dev)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    _check(device_status, "device_status", torch.int32, dev)
+    H, d_k = q.shape[-2], q.shape[-1]
+    d_v = v.shape[-1]
+    if cu_seqlens is not None:
+        B, T, N = 1, q.shape[0], cu_seqlens.numel() - 1
+    elif q.dim() == 4:
+        B, T = q.shape[0], q.shape[1]
+        N = B
+    else:
+        B, T, N = 1, q.shape[0], 1
+    if o is None:
+        o = torch.empty(v.shape, dtype=dt, device=dev)
+    if S_T is None:
+        S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=dev)
+    _check(o, "o", dt, dev)
+    _check(S_T, "S_T", torch.float32, dev)
+    rc = load().kda_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                _ptr(S0), _ptr(cu_seqlens), B, T, H, d_k, d_v, N,
+                                _dtype_code(dt), _ptr(o), _ptr(S_T), _ptr(device_status),
+                                _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_fwd_noalloc")
     return o, S_T
 
 
