@@ -1,9 +1,9 @@
 // Tensor-core chunkwise KDA forward for sm_103a (bf16 q/k/v, d_k = d_v = 128).
 //
 // One CTA per (sequence, head) walks the sequence in 64-token chunks.  The
-// algorithm is the chunk form of the recurrence (see the CUDA-core engine for
-// the derivation; "Kimi Delta Attention 完全拆解", chunkwise section; "Kimi K3
-// 的 KDA" section 5):
+// algorithm is the chunk form of the recurrence (the CUDA-core engine gives the
+// derivation; "Kimi Delta Attention 完全拆解", chunkwise section; "Kimi K3 的 KDA"
+// section 5):
 //
 //   G = in-chunk inclusive cumsum of log_alpha, Gamma = exp(G), gamma = Gamma_last
 //   Kh = K . Gamma,  Qh = Q . Gamma,  Kb = K / Gamma                       (a1, a2)
@@ -17,15 +17,22 @@
 // tokens are N or K.  So the products are U^T = U~^T - S^T W^T, O^T = S^T Qh^T
 // + U^T M^T, (S^T)' = S^T + U^T Kb, W^T = Kh^T T'^T, U~^T = V^T T'^T, and R
 // stacks Kh and Qh as the 128 rows of one A operand.  The fp32 state lives in
-// tensor memory for the whole sequence (the S-update MMA accumulates into it);
-// a bf16 copy in shared memory is the MMA operand.
+// tensor memory for the whole sequence (the S-update MMA accumulates into it),
+// next to a bf16 copy that is the A operand of the carry-in MMAs, read straight
+// from tensor memory.  The 64 x 64 triangular solve runs on the warp-level
+// tensor cores (TF32, kda_solve.cuh).  Gates are handled in log2 units
+// (G2 = G log2 e) so the exponentials are single ex2 instructions.
 //
-// Warp roles (288 threads):
-//   warp 0      TMA producer: q, k, v tiles (64 tokens x 64 channels, 128-byte
-//               swizzle) into a two-stage ring; allocates tensor memory.
-//   warps 1-4   chunk-local work for chunk n+1 (a1-a5): gates, scaled operands,
-//               R, masks, the triangular solve, W and U~.
-//   warps 5-8   the serial carry for chunk n (a6) and the output store.
+// Warp roles (384 threads, 3 warps per SM sub-partition, so up to 168
+// registers per thread):
+//   warps 0-7   chunk-local work of chunk n+1 (a1-a5): gates, scaled operands,
+//               R, masks, the triangular solve, W and U~.  Warp 0 allocates
+//               tensor memory; one thread loads each chunk's log_alpha tile
+//               (TMA) as soon as the previous tile has been read.
+//   warps 8-11  the serial carry of chunk n (a6) and the output, staged in
+//               shared memory and written with a TMA store.  Their MMA-issuing
+//               thread also refills the q/k/v stage a chunk has just released
+//               (TMA, 64 tokens x 64 channels per box, 128-byte swizzle).
 // The chunk-local work of the next chunk overlaps the carry of the current one.
 //
 // Every wait is bounded in time; on a timeout the kernel records
@@ -37,6 +44,7 @@
 
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
+#include "kda_solve.cuh"
 
 namespace kda {
 namespace {
@@ -45,18 +53,21 @@ using namespace sm100;
 
 constexpr int D = 128;
 constexpr int C = kChunk;
-constexpr int kPrepWarp0 = 1;
-constexpr int kEpiWarp0 = 5;
-constexpr int kThreads = 32 * 9;
+constexpr int kPrepWarp0 = 0, kPrepWarps = 8, kPrepThreads = 32 * kPrepWarps;
+constexpr int kCarryWarp0 = 8, kCarryWarps = 4, kCarryThreads = 32 * kCarryWarps;
+constexpr int kThreads = 32 * (kPrepWarps + kCarryWarps);
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns (fp32 accumulators, 128 lanes each)
 constexpr uint32_t kColRW = 0;    // R, then W^T              (64 columns)
 constexpr uint32_t kColU = 64;    // U~^T / U^T, two buffers (2 x 64)
 constexpr uint32_t kColO = 192;   // O^T, two buffers         (2 x 64)
+constexpr uint32_t kColSb = 320;  // S^T, bf16 pairs          (64): MMA A operand
 constexpr uint32_t kColS = 384;   // S^T master copy, fp32    (128)
-constexpr int LDA = 68;           // fp32 row stride of the solve matrix
-constexpr uint32_t kBarPrep = 1, kBarEpi = 2;  // named barrier ids
-constexpr uint32_t kTileBytes = 64 * 64 * 2;   // one TMA box
+constexpr int LDA = kSolveLd;     // fp32 row stride of the solve matrix
+constexpr uint32_t kBarPrep = 1, kBarCarry = 2;  // named barrier ids
+constexpr uint32_t kTileBytes = 64 * 64 * 2;     // one TMA box
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLog2DecayLimit = kLogDecayLimit * kLog2e;
 
 struct __align__(1024) TcStage {
     uint8_t kq[32768];  // per 64-channel slab: Kh rows 0-63 | Qh rows 0-63; Kh area -> -W
@@ -71,10 +82,10 @@ struct __align__(1024) TcStage {
 struct __align__(1024) TcSmem {
     TcStage st[2];
     uint8_t tp[8192];   // T' bf16 [r][j]; fp32 scratch while solving
-    uint8_t ut[16384];  // U^T bf16 [v][j]
-    uint8_t sb[32768];  // S^T bf16 [v][c], two slabs
-    float as[C * LDA];  // solve matrix / block inverse (fp32)
-    uint64_t full[2], ready[2], empty[2], uempty[2];
+    uint8_t ut[16384];  // U^T bf16 [v][j]; then the staged output tile [r][v]
+    uint8_t gt[32768];  // log_alpha tile: 4 boxes of 32 channels x 64 tokens (fp32, swizzled)
+    float as[C * LDA];  // solve matrix / inverse blocks (fp32)
+    uint64_t full[2], ready[2], uempty[2], gfull;
     uint64_t bar_r, bar_w, bar_u, bar_s, bar_fin;
     uint32_t tmem_base;
     int abort;
@@ -111,114 +122,66 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
     }
 }
 
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+__device__ __forceinline__ uint4 pack8(const float *f) {
     return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
                       pack_bf16(f[6], f[7]));
 }
 
-// Store 16 fp32 values (one row segment of 16 consecutive bf16 columns) into a
-// 128-byte-swizzled tile at (row, col16 .. col16 + 15).
-__device__ __forceinline__ void store_row16(uint8_t *tile, int row, int col16,
-                                            const float (&f)[16]) {
-    float a[8], b[8];
+// Store n (multiple of 8) fp32 values as consecutive bf16 columns
+// col .. col + n - 1 of one row of a 128-byte-swizzled tile.
+template <int n>
+__device__ __forceinline__ void store_row(uint8_t *tile, int row, int col, const float *f) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        a[j] = f[j];
-        b[j] = f[8 + j];
-    }
-    *reinterpret_cast<uint4 *>(tile + sw128_offset(row, col16)) = pack8(a);
-    *reinterpret_cast<uint4 *>(tile + sw128_offset(row, col16 + 8)) = pack8(b);
+    for (int j = 0; j < n; j += 8)
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(row, col + j)) = pack8(f + j);
 }
 
-// T' = (I + A)^{-1} diag(beta) for the 64 x 64 strictly lower A in sm.as,
-// by 16 x 16 blocks: invert the diagonal blocks by forward substitution, then
-// the off-diagonal blocks diagonal by diagonal, T_ij = -T_ii sum_{k=j}^{i-1}
-// A_ik T_kj.  T_ij (i > j) is kept in the unused upper block (j, i) of sm.as,
-// so T_kj for k >= j always sits at row 16 j + ., column block k.
+// Gates of one prep thread from the landed log_alpha tile: tokens 4 tg .. 4 tg + 3
+// of channels c0 .. c0 + 7.  The tile is four TMA boxes of 32 fp32 channels x 64
+// tokens with the 128-byte swizzle (16-byte chunk index XOR row % 8).
+__device__ __forceinline__ void read_gates(const uint8_t *gt, int tg, int c0, float (&g)[4][8]) {
+    const uint8_t *box = gt + (c0 >> 5) * 8192;
+    const int ch = (c0 & 31) >> 2;  // first of two 16-byte chunks in the 128-byte row
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = 4 * tg + i;
+        const uint8_t *row = box + (t >> 3) * 1024 + (t & 7) * 128;
+        const float4 a = *reinterpret_cast<const float4 *>(row + ((ch ^ (t & 7)) << 4));
+        const float4 b = *reinterpret_cast<const float4 *>(row + (((ch + 1) ^ (t & 7)) << 4));
+        g[i][0] = a.x; g[i][1] = a.y; g[i][2] = a.z; g[i][3] = a.w;
+        g[i][4] = b.x; g[i][5] = b.y; g[i][6] = b.z; g[i][7] = b.w;
+    }
+}
+
+// T' = (I + A)^{-1} diag(beta) in bf16 ([r][j], 128-byte swizzle, into sm.tp)
+// for the 64 x 64 strictly lower A in sm.as.  The inverse runs on the
+// warp-level tensor cores (kda_solve.cuh) with sm.tp as its scratch.
 __device__ __forceinline__ void solve_ut(TcSmem &sm, const float *bet, int pt) {
-    float *A = sm.as;
-    float *Y = reinterpret_cast<float *>(sm.tp);
-    if (pt < 64) {
-        const int b = pt >> 4, j = pt & 15;
-        float x[16];
+    inverse_unit_lower64(sm.as, reinterpret_cast<float *>(sm.tp), pt, kBarPrep);
+    const int row = pt >> 2, j0 = 16 * (pt & 3);
+    float f[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = r == j ? 1.f : 0.f;
-#pragma unroll
-        for (int i = 0; i < 15; ++i)
-#pragma unroll
-            for (int r = i + 1; r < 16; ++r)
-                x[r] = fmaf(-A[(16 * b + r) * LDA + 16 * b + i], x[i], x[r]);
-        named_bar_sync(kBarPrep, 128);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) A[(16 * b + r) * LDA + 16 * b + j] = x[r];
-    } else {
-        named_bar_sync(kBarPrep, 128);
-    }
-    named_bar_sync(kBarPrep, 128);
+    for (int e = 0; e < 16; ++e) f[e] = inv_entry(sm.as, row, j0 + e) * bet[j0 + e];
+    store_row<16>(sm.tp, row, j0, f);
+}
 
-    const int r = pt >> 3, c = 2 * (pt & 7);
+// Pack 16 fp32 values (as bits) into 8 bf16 pairs (even index in the low half).
+__device__ __forceinline__ void pack16(const uint32_t (&u)[16], uint32_t (&w)[8]) {
 #pragma unroll
-    for (int d = 1; d < 4; ++d) {
-        // Y_ij = -sum_{k=j}^{i-1} A_ik T_kj  for every block (i, j = i - d)
-        for (int bi = d; bi < 4; ++bi) {
-            const int bj = bi - d;
-            float y0 = 0.f, y1 = 0.f;
-            for (int k = bj; k < bi; ++k) {
-#pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    const float a = A[(16 * bi + r) * LDA + 16 * k + kk];
-                    const float2 t =
-                        *reinterpret_cast<const float2 *>(&A[(16 * bj + kk) * LDA + 16 * k + c]);
-                    y0 = fmaf(a, t.x, y0);
-                    y1 = fmaf(a, t.y, y1);
-                }
-            }
-            *reinterpret_cast<float2 *>(&Y[(bi - d) * 256 + r * 16 + c]) = make_float2(-y0, -y1);
-        }
-        named_bar_sync(kBarPrep, 128);
-        // T_ij = T_ii Y_ij, stored in the upper block (j, i)
-        for (int bi = d; bi < 4; ++bi) {
-            const int bj = bi - d;
-            float t0 = 0.f, t1 = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-                const float a = A[(16 * bi + r) * LDA + 16 * bi + kk];
-                const float2 y = *reinterpret_cast<const float2 *>(&Y[(bi - d) * 256 + kk * 16 + c]);
-                t0 = fmaf(a, y.x, t0);
-                t1 = fmaf(a, y.y, t1);
-            }
-            *reinterpret_cast<float2 *>(&A[(16 * bj + r) * LDA + 16 * bi + c]) =
-                make_float2(t0, t1);
-        }
-        named_bar_sync(kBarPrep, 128);
-    }
-
-    // T'[row][j] = T[row][j] beta_j in bf16, 128-byte swizzled [r][j]
-    const int row = pt >> 1, half = pt & 1;
-    const int bi = row >> 4;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int j0 = 32 * half + 8 * q;
-        const int bj = j0 >> 4;
-        float f[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int j = j0 + e;
-            float t = 0.f;
-            if (bj <= bi && j <= row) t = A[(16 * bj + (row & 15)) * LDA + 16 * bi + (j & 15)];
-            f[e] = t * bet[j];
-        }
-        *reinterpret_cast<uint4 *>(sm.tp + sw128_offset(row, j0)) = pack8(f);
-    }
+    for (int j = 0; j < 8; ++j) w[j] = pack_bf16(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1]));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v) {
-    extern __shared__ uint8_t smem_raw[];
-    TcSmem &sm = *reinterpret_cast<TcSmem *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o,
+                      const __grid_constant__ CUtensorMap tm_g) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // Align by offsetting the shared-memory pointer itself (not through an
+    // integer round trip), so the compiler keeps every access in the shared
+    // address space.
+    TcSmem &sm = *reinterpret_cast<TcSmem *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (*p.status == KDA_ERR_INVALID_ARGUMENT) return;  // set by the schedule kernel
 
@@ -244,7 +207,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.ready[s]), 1);
-            mbar_init(smem_u32(&sm.empty[s]), 2);
             mbar_init(smem_u32(&sm.uempty[s]), 1);
         }
         mbar_init(smem_u32(&sm.bar_r), 1);
@@ -252,9 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&sm.bar_u), 1);
         mbar_init(smem_u32(&sm.bar_s), 1);
         mbar_init(smem_u32(&sm.bar_fin), 2);
+        mbar_init(smem_u32(&sm.gfull), 1);
         fence_mbar_init();
     }
-    if (warp == 0) {
+    if (warp == kPrepWarp0) {
         tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
         tmem_relinquish();
     }
@@ -265,105 +228,117 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const int L = 32 * (warp & 3) + lane;  // this thread's TMEM lane
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            prefetch_tensormap(&tm_q);
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            int issued = 0;
-            for (int n = 0; n < nchunks; ++n) {
-                const int s = n & 1;
-                if (n >= 2) wait_phase(sm.empty[s], ((n >> 1) - 1) & 1, abort);
-                const uint32_t fb = smem_u32(&sm.full[s]);
-                mbar_arrive_expect_tx(fb, 6 * kTileBytes);
-                const int t0 = static_cast<int>(start + (int64_t)n * C);
-                TcStage &S = sm.st[s];
-                tma_load_3d(smem_u32(S.kq), &tm_k, fb, 0, h, t0);
-                tma_load_3d(smem_u32(S.kq + 8192), &tm_q, fb, 0, h, t0);
-                tma_load_3d(smem_u32(S.kq + 16384), &tm_k, fb, 64, h, t0);
-                tma_load_3d(smem_u32(S.kq + 24576), &tm_q, fb, 64, h, t0);
-                tma_load_3d(smem_u32(S.v), &tm_v, fb, 0, h, t0);
-                tma_load_3d(smem_u32(S.v + 8192), &tm_v, fb, 64, h, t0);
-                issued = n + 1;
-                if (n + 2 < nchunks) {
-                    const int t2 = t0 + 2 * C;
-                    tma_prefetch_3d(&tm_k, 0, h, t2);
-                    tma_prefetch_3d(&tm_k, 64, h, t2);
-                    tma_prefetch_3d(&tm_q, 0, h, t2);
-                    tma_prefetch_3d(&tm_q, 64, h, t2);
-                    tma_prefetch_3d(&tm_v, 0, h, t2);
-                    tma_prefetch_3d(&tm_v, 64, h, t2);
-                }
-            }
-            // never leave with a copy in flight
-            for (int n = issued > 2 ? issued - 2 : 0; n < issued; ++n)
-                wait_drain(sm.full[n & 1], (n >> 1) & 1);
+    // TMA of the q, k, v tiles of chunk n into stage n % 2 (and an L2 prefetch of
+    // the chunk after), and of the log_alpha tile of chunk n into the gate buffer.
+    auto load_stage = [&](int n) {
+        const int s = n & 1;
+        const uint32_t fb = smem_u32(&sm.full[s]);
+        mbar_arrive_expect_tx(fb, 6 * kTileBytes);
+        const int t0 = static_cast<int>(start + (int64_t)n * C);
+        TcStage &S = sm.st[s];
+        tma_load_3d(smem_u32(S.kq), &tm_k, fb, 0, h, t0);
+        tma_load_3d(smem_u32(S.kq + 8192), &tm_q, fb, 0, h, t0);
+        tma_load_3d(smem_u32(S.kq + 16384), &tm_k, fb, 64, h, t0);
+        tma_load_3d(smem_u32(S.kq + 24576), &tm_q, fb, 64, h, t0);
+        tma_load_3d(smem_u32(S.v), &tm_v, fb, 0, h, t0);
+        tma_load_3d(smem_u32(S.v + 8192), &tm_v, fb, 64, h, t0);
+        if (n + 1 < nchunks) {
+            const int t1 = t0 + C;
+            tma_prefetch_3d(&tm_k, 0, h, t1);
+            tma_prefetch_3d(&tm_k, 64, h, t1);
+            tma_prefetch_3d(&tm_q, 0, h, t1);
+            tma_prefetch_3d(&tm_q, 64, h, t1);
+            tma_prefetch_3d(&tm_v, 0, h, t1);
+            tma_prefetch_3d(&tm_v, 64, h, t1);
         }
-    } else if (warp < kEpiWarp0) {
+    };
+    auto load_gates = [&](int n) {
+        const uint32_t gb = smem_u32(&sm.gfull);
+        mbar_arrive_expect_tx(gb, 4 * 8192);
+        const int t0 = static_cast<int>(start + (int64_t)n * C);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) tma_load_3d(smem_u32(sm.gt + b * 8192), &tm_g, gb, 32 * b, h, t0);
+    };
+    if (tid == 32 * kCarryWarp0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_g);
+        load_gates(0);
+        load_stage(0);
+        if (nchunks > 1) load_stage(1);
+    }
+
+    if (warp < kCarryWarp0) {
         // ------------------------------------------------ chunk-local work (a1-a5)
-        const int pt = tid - 32 * kPrepWarp0;
-        const int cg = pt >> 3, tg = pt & 7;  // 8 channels x 8 tokens per thread
+        const int pt = tid - 32 * kPrepWarp0;     // 0..255
+        const int pw = pt >> 5;                   // prep warp 0..7
+        const int half = pw >> 2;                 // which 32 of 64 TMEM columns
+        const int cg = pt >> 4, tg = pt & 15;     // 8 channels x 4 tokens per thread
         const int c0 = 8 * cg;
         const int slab = c0 >> 6, col = c0 & 63;
         bool domain_ok = true;
+
+        float bn = 0.f;  // beta of the next chunk, loaded one chunk ahead
+        if (pt < C && pt < len) bn = p.beta[(size_t)(start + pt) * p.H + h];
+
         for (int n = 0; n < nchunks; ++n) {
             const int s = n & 1;
             TcStage &S = sm.st[s];
             const int64_t t0 = start + (int64_t)n * C;
             const int valid = min(C, len - n * C);
 
-            // a1: in-chunk cumulative log-decay, G[t][c] = sum_{t' <= t} log_alpha
-            float g[8][8];
+            // a1: in-chunk cumulative log2-decay G2[t][c] = log2(e) sum_{t' <= t} log_alpha
+            float g[4][8];
+            wait_phase_warp(sm.gfull, n & 1, abort);
+            read_gates(sm.gt, tg, c0, g);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = 8 * tg + i;
-                if (t < valid) {
-                    const float4 *src = reinterpret_cast<const float4 *>(
-                        p.log_alpha + ((size_t)(t0 + t) * p.H + h) * D + c0);
-                    const float4 a = src[0], b = src[1];
-                    g[i][0] = a.x; g[i][1] = a.y; g[i][2] = a.z; g[i][3] = a.w;
-                    g[i][4] = b.x; g[i][5] = b.y; g[i][6] = b.z; g[i][7] = b.w;
-                } else {
+            for (int i = 0; i < 4; ++i) {
+                const bool live = 4 * tg + i < valid;  // the tile runs past the sequence end
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) g[i][e] = 0.f;
-                }
+                for (int e = 0; e < 8; ++e) g[i][e] = live ? g[i][e] * kLog2e : 0.f;
             }
-            const float bet = (pt < C && pt < valid) ? p.beta[(size_t)(t0 + pt) * p.H + h] : 0.f;
+            const float bet = bn;
 #pragma unroll
-            for (int i = 1; i < 8; ++i)
+            for (int i = 1; i < 4; ++i)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) g[i][e] += g[i - 1][e];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float tot = g[7][e];
+                const float tot = g[3][e];
                 float inc = tot;
 #pragma unroll
-                for (int o = 1; o < 8; o <<= 1) {
-                    const float up = __shfl_up_sync(0xffffffffu, inc, o, 8);
+                for (int o = 1; o < 16; o <<= 1) {
+                    const float up = __shfl_up_sync(0xffffffffu, inc, o, 16);
                     if (tg >= o) inc += up;
                 }
                 const float pre = inc - tot;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 4; ++i) {
                     g[i][e] += pre;
-                    if (fabsf(g[i][e]) > kLogDecayLimit) domain_ok = false;
+                    if (fabsf(g[i][e]) > kLog2DecayLimit) domain_ok = false;
                 }
+            }
+            if (n + 1 < nchunks) {  // beta of the next chunk
+                const int64_t t1 = t0 + C;
+                const int valid1 = min(C, len - (n + 1) * C);
+                bn = (pt < C && pt < valid1) ? p.beta[(size_t)(t1 + pt) * p.H + h] : 0.f;
             }
 
             wait_phase_warp(sm.full[s], (n >> 1) & 1, abort);
-            if (tg == 7)
+            if (tg == 15)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) S.gam[c0 + e] = expf(g[7][e]);
+                for (int e = 0; e < 8; ++e) S.gam[c0 + e] = exp2f(g[3][e]);
             if (pt < C) S.bet[pt] = bet;
 
             // a2: scaled operands, written over the landed tiles (same swizzle)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = 8 * tg + i;
+            for (int i = 0; i < 4; ++i) {
+                const float *gr = g[i];
+                const int t = 4 * tg + i;
                 const uint32_t off = slab * 16384 + sw128_offset(t, col);
                 const uint32_t offv = slab * 8192 + sw128_offset(t, col);
-                float kf[8], qf[8], kh[8], qh[8], kb[8];
+                float kf[8], qf[8], kb[8];
                 if (t < valid) {
                     unpack8(*reinterpret_cast<const uint4 *>(S.kq + off), kf);
                     unpack8(*reinterpret_cast<const uint4 *>(S.kq + off + 8192), qf);
@@ -374,18 +349,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float gf = __expf(g[i][e]);
-                    const float gi = __expf(-g[i][e]);
-                    kh[e] = kf[e] * gf;
-                    qh[e] = qf[e] * gf;
+                    const float gf = ex2_approx(gr[e]);
+                    const float gi = ex2_approx(-gr[e]);
                     kb[e] = kf[e] * gi;
+                    kf[e] *= gf;
+                    qf[e] *= gf;
                 }
-                *reinterpret_cast<uint4 *>(S.kq + off) = pack8(kh);
-                *reinterpret_cast<uint4 *>(S.kq + off + 8192) = pack8(qh);
+                *reinterpret_cast<uint4 *>(S.kq + off) = pack8(kf);
+                *reinterpret_cast<uint4 *>(S.kq + off + 8192) = pack8(qf);
                 *reinterpret_cast<uint4 *>(S.kb + offv) = pack8(kb);
             }
             fence_proxy_async_smem();
-            named_bar_sync(kBarPrep, 128);
+            named_bar_sync(kBarPrep, kPrepThreads);
+            // every prep thread has read this chunk's gates: fetch the next tile
+            if (pt == 0 && n + 1 < nchunks) load_gates(n + 1);
 
             // a3 + a5: R = [Kh; Qh] Kb^T (M = 128, N = 64, K = 128)
             if (pt == 0) {
@@ -403,44 +380,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             wait_phase_warp(sm.bar_r, n & 1, abort);
             tc_fence_after();
-            if (L < 64) {  // A[r][j] = beta_r R[r][j], j < r
-                const int r = L;
-                const float br = S.bet[r];
 #pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t x[16];
-                    tmem_ld16(tmem + lane_addr + kColRW + 16 * cb, x);
+            for (int piece = 0; piece < 2; ++piece) {
+                const int j0 = 32 * half + 16 * piece;
+                uint32_t x[16];
+                tmem_ld16(tmem + lane_addr + kColRW + j0, x);
+                if (L < 64) {  // A[r][j] = beta_r R[r][j], j < r
+                    const int r = L;
+                    const float br = S.bet[r];
 #pragma unroll
                     for (int j4 = 0; j4 < 4; ++j4) {
+                        const int j = j0 + 4 * j4;
                         float4 w;
-                        const int j = 16 * cb + 4 * j4;
                         w.x = j + 0 < r ? br * __uint_as_float(x[4 * j4 + 0]) : 0.f;
                         w.y = j + 1 < r ? br * __uint_as_float(x[4 * j4 + 1]) : 0.f;
                         w.z = j + 2 < r ? br * __uint_as_float(x[4 * j4 + 2]) : 0.f;
                         w.w = j + 3 < r ? br * __uint_as_float(x[4 * j4 + 3]) : 0.f;
                         *reinterpret_cast<float4 *>(&sm.as[r * LDA + j]) = w;
                     }
-                }
-            } else {  // M[r][j] = R[64 + r][j], j <= r
-                const int r = L - 64;
-#pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t x[16];
-                    tmem_ld16(tmem + lane_addr + kColRW + 16 * cb, x);
+                } else {  // M[r][j] = R[64 + r][j], j <= r
+                    const int r = L - 64;
                     float f[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        f[j] = 16 * cb + j <= r ? __uint_as_float(x[j]) : 0.f;
-                    store_row16(S.m, r, 16 * cb, f);
+                        f[j] = j0 + j <= r ? __uint_as_float(x[j]) : 0.f;
+                    store_row<16>(S.m, r, j0, f);
                 }
             }
             tc_fence_before();
-            named_bar_sync(kBarPrep, 128);
+            named_bar_sync(kBarPrep, kPrepThreads);
 
             // a4: T' = (I + A)^-1 diag(beta)
             solve_ut(sm, S.bet, pt);
             fence_proxy_async_smem();
-            named_bar_sync(kBarPrep, 128);
+            named_bar_sync(kBarPrep, kPrepThreads);
 
             // a4: W^T = Kh^T T'^T, U~^T = V^T T'^T (M = 128, N = 64, K = 64)
             if (pt == 0) {
@@ -459,54 +432,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             wait_phase_warp(sm.bar_w, n & 1, abort);
             tc_fence_after();
-            {  // -W as the MN-major operand [c][r], over the Kh area
-                const int c = L;
-                uint8_t *dst = S.kq + (c >> 6) * 16384;
 #pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t x[16];
-                    tmem_ld16(tmem + lane_addr + kColRW + 16 * cb, x);
-                    float f[16];
+            for (int piece = 0; piece < 2; ++piece) {  // -W as the MN-major operand [c][r]
+                const int c = L, j0 = 32 * half + 16 * piece;
+                uint32_t x[16];
+                tmem_ld16(tmem + lane_addr + kColRW + j0, x);
+                float f[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) f[j] = -__uint_as_float(x[j]);
-                    store_row16(dst, c & 63, 16 * cb, f);
-                }
+                for (int j = 0; j < 16; ++j) f[j] = -__uint_as_float(x[j]);
+                store_row<16>(S.kq + (c >> 6) * 16384, c & 63, j0, f);
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_bar_sync(kBarPrep, 128);
+            named_bar_sync(kBarPrep, kPrepThreads);
             if (pt == 0) mbar_arrive(smem_u32(&sm.ready[s]));
         }
         if (!domain_ok) sm.domain = 1;
     } else {
         // -------------------------------------------------- serial carry (a6)
-        const int et = tid - 32 * kEpiWarp0;
+        const int et = tid - 32 * kCarryWarp0;
         const bool issuer = et == 0;
         const int v = L;
         {  // initial state: row v of S0 ([v][c] memory) -> TMEM fp32 and bf16 operand
             const float *src = p.S0 ? p.S0 + state_off + (size_t)v * D : nullptr;
 #pragma unroll
             for (int cb = 0; cb < 8; ++cb) {
-                float f[16];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float4 x = src ? reinterpret_cast<const float4 *>(src + 16 * cb)[q]
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-                    f[4 * q] = x.x; f[4 * q + 1] = x.y; f[4 * q + 2] = x.z; f[4 * q + 3] = x.w;
-                }
                 uint32_t u[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(f[j]);
+                for (int q = 0; q < 4; ++q) {
+                    const float4 x = src ? reinterpret_cast<const float4 *>(src + 16 * cb)[q]
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                    u[4 * q] = __float_as_uint(x.x); u[4 * q + 1] = __float_as_uint(x.y);
+                    u[4 * q + 2] = __float_as_uint(x.z); u[4 * q + 3] = __float_as_uint(x.w);
+                }
                 tmem_st16(tmem + lane_addr + kColS + 16 * cb, u);
-                store_row16(sm.sb + (cb >> 2) * 16384, v, 16 * (cb & 3), f);
+                uint32_t w[8];
+                pack16(u, w);
+                tmem_st8(tmem + lane_addr + kColSb + 8 * cb, w);
             }
             tmem_wait_st();
-            fence_proxy_async_smem();
             tc_fence_before();
-            named_bar_sync(kBarEpi, 128);
+            named_bar_sync(kBarCarry, kCarryThreads);
         }
 
-        auto issue_carry_in = [&](int n) {  // U^T += S^T (-W)^T ; O^T = S^T Qh^T
+        auto issue_carry_in = [&](int n) {  // U^T += S^T (-W)^T ; O^T = S^T Qh^T (S^T from TMEM)
             const int s = n & 1;
             TcStage &S = sm.st[s];
             wait_phase(sm.ready[s], (n >> 1) & 1, abort);
@@ -515,36 +484,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t id_o = idesc_bf16(128, 64, false, false);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const uint64_t a =
-                    desc_sw128(smem_u32(sm.sb) + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+                const uint32_t a = tmem + kColSb + 8 * k;
                 const uint64_t bw =
                     desc_sw128(smem_u32(S.kq) + (k >> 2) * 16384 + (k & 3) * 2048, 8192, 1024);
                 const uint64_t bq = desc_sw128(
                     smem_u32(S.kq) + 8192 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-                mma_bf16(tmem + kColU + 64 * s, a, bw, id_u, 1);
-                mma_bf16(tmem + kColO + 64 * s, a, bq, id_o, k > 0);
+                mma_bf16_tmem_a(tmem + kColU + 64 * s, a, bw, id_u, 1);
+                mma_bf16_tmem_a(tmem + kColO + 64 * s, a, bq, id_o, k > 0);
             }
             mma_commit(smem_u32(&sm.bar_u));
         };
 
-        auto store_output = [&](int n) {  // O^T (lane v, column r) -> o[t0 + r][h][v]
+        // O^T of chunk n (lane v, column r) -> staged tile [r][v] in sm.ut (two
+        // 64-channel slabs, 128-byte swizzle) -> global: one TMA store per slab
+        // for a full chunk; a masked copy for the last, partial chunk.
+        auto store_output = [&](int n) {
             const int s = n & 1;
             const int64_t t0 = start + (int64_t)n * C;
             const int valid = min(C, len - n * C);
-            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+            uint8_t *stage = sm.ut + (v >> 6) * 8192;
+            const int vc = v & 63;
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t x[16];
                 tmem_ld16(tmem + lane_addr + kColO + 64 * s + 16 * cb, x);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int r = 16 * cb + j;
-                    if (r < valid)
-                        o[((size_t)(t0 + r) * p.H + h) * D + v] =
-                            __float2bfloat16_rn(__uint_as_float(x[j]));
-                }
+                for (int j = 0; j < 16; ++j)
+                    *reinterpret_cast<__nv_bfloat16 *>(stage + sw128_offset(16 * cb + j, vc)) =
+                        __float2bfloat16_rn(__uint_as_float(x[j]));
             }
             tc_fence_before();
+            fence_proxy_async_smem();
+            named_bar_sync(kBarCarry, kCarryThreads);
+            if (valid == C) {
+                if (issuer) {
+                    tma_store_3d(&tm_o, smem_u32(sm.ut), 0, h, static_cast<int>(t0));
+                    tma_store_3d(&tm_o, smem_u32(sm.ut + 8192), 64, h, static_cast<int>(t0));
+                    bulk_commit_group();
+                }
+            } else {
+                __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+                for (int idx = et; idx < valid * 16; idx += kCarryThreads) {
+                    const int r = idx >> 4, ch = idx & 15;  // 16 pieces of 8 channels per row
+                    const uint4 val = *reinterpret_cast<const uint4 *>(
+                        sm.ut + (ch >> 3) * 8192 + sw128_offset(r, (ch & 7) * 8));
+                    *reinterpret_cast<uint4 *>(o + ((size_t)(t0 + r) * p.H + h) * D + 8 * ch) =
+                        val;
+                }
+            }
         };
 
         if (issuer) issue_carry_in(0);
@@ -552,8 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = n & 1;
             TcStage &S = sm.st[s];
             __syncwarp();  // the issuer lane rejoins before the warp-wide TMEM loads
-            if (n >= 1) store_output(n - 1);
             wait_phase_warp(sm.bar_u, n & 1, abort);
+            if (issuer) bulk_wait_group_read0();  // the previous output tile has left sm.ut
+            named_bar_sync(kBarCarry, kCarryThreads);
             tc_fence_after();
             // U^T (lane v, column j) -> bf16 operand [v][j]
 #pragma unroll
@@ -563,11 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float f[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(x[j]);
-                store_row16(sm.ut, v, 16 * cb, f);
+                store_row<16>(sm.ut, v, 16 * cb, f);
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_bar_sync(kBarEpi, 128);
+            named_bar_sync(kBarCarry, kCarryThreads);
             if (issuer) {
                 mbar_arrive(smem_u32(&sm.uempty[s]));
                 tc_fence_after();
@@ -582,35 +570,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16(tmem + kColS, a, bk, id_s, 1);
                 }
                 mma_commit(smem_u32(&sm.bar_s));
-                mma_commit(smem_u32(&sm.empty[s]));
             }
+            __syncwarp();
             wait_phase_warp(sm.bar_s, n & 1, abort);
             tc_fence_after();
-            // S^T <- Diag(gamma) applied along c to (S^T + U^T Kb): TMEM fp32 and bf16 copy
+            // S^T <- (S^T + U^T Kb) scaled by gamma along c: TMEM fp32 and bf16 copy
 #pragma unroll
             for (int cb = 0; cb < 8; ++cb) {
                 uint32_t x[16];
                 tmem_ld16(tmem + lane_addr + kColS + 16 * cb, x);
-                float f[16];
+                const float4 *gm = reinterpret_cast<const float4 *>(S.gam + 16 * cb);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    f[j] = __uint_as_float(x[j]) * S.gam[16 * cb + j];
-                    x[j] = __float_as_uint(f[j]);
+                for (int q = 0; q < 4; ++q) {
+                    const float4 gq = gm[q];
+                    x[4 * q + 0] = __float_as_uint(__uint_as_float(x[4 * q + 0]) * gq.x);
+                    x[4 * q + 1] = __float_as_uint(__uint_as_float(x[4 * q + 1]) * gq.y);
+                    x[4 * q + 2] = __float_as_uint(__uint_as_float(x[4 * q + 2]) * gq.z);
+                    x[4 * q + 3] = __float_as_uint(__uint_as_float(x[4 * q + 3]) * gq.w);
                 }
                 tmem_st16(tmem + lane_addr + kColS + 16 * cb, x);
-                store_row16(sm.sb + (cb >> 2) * 16384, v, 16 * (cb & 3), f);
+                uint32_t w[8];
+                pack16(x, w);
+                tmem_st8(tmem + lane_addr + kColSb + 8 * cb, w);
             }
             tmem_wait_st();
-            fence_proxy_async_smem();
             tc_fence_before();
-            named_bar_sync(kBarEpi, 128);
+            named_bar_sync(kBarCarry, kCarryThreads);
             if (issuer) {
-                mbar_arrive(smem_u32(&sm.empty[s]));
+                // stage s is no longer read by anyone: refill it with chunk n + 2
+                if (n + 2 < nchunks) load_stage(n + 2);
                 if (n + 1 < nchunks) issue_carry_in(n + 1);
             }
+            __syncwarp();
+            store_output(n);  // overlaps the MMAs of chunk n + 1
         }
+        if (issuer) bulk_wait_group0();
         __syncwarp();
-        store_output(nchunks - 1);
         if (p.S_T) {
             float *dst = p.S_T + state_off + (size_t)v * D;
 #pragma unroll
@@ -628,13 +623,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------------- teardown
-    if (tid == 32 * kPrepWarp0 || tid == 32 * kEpiWarp0) mma_commit(smem_u32(&sm.bar_fin));
+    if (tid == 32 * kPrepWarp0 || tid == 32 * kCarryWarp0) mma_commit(smem_u32(&sm.bar_fin));
+    if (tid == 32 * kCarryWarp0)  // never leave with a copy in flight
+        for (int n = nchunks > 2 ? nchunks - 2 : 0; n < nchunks; ++n)
+            wait_drain(sm.full[n & 1], (n >> 1) & 1);
+    if (tid == 32 * kPrepWarp0) wait_drain(sm.gfull, (nchunks - 1) & 1);
     __syncthreads();
     if (tid == 0) {
         if (sm.abort) raise_status(p.status, KDA_ERR_TIMEOUT);
         else if (sm.domain) raise_status(p.status, KDA_ERR_DOMAIN);
     }
-    if (warp == 0) {
+    if (warp == kPrepWarp0) {
         wait_drain(sm.bar_fin, 0);
         __syncwarp();
         tc_fence_after();
@@ -669,6 +668,21 @@ bool make_token_map(CUtensorMap *map, const void *base, int H, int64_t Ttot) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [Ttot][H][128] fp32 viewed as a 3-D tensor, tile = 32 channels x 1 head x 64
+// tokens (128-byte rows, 128-byte swizzle).
+bool make_gate_map(CUtensorMap *map, const float *base, int H, int64_t Ttot) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)Ttot};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
+    cuuint32_t box[3] = {32, 1, 64};
+    cuuint32_t elem[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides,
+               box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool prefill_tc_supported(kda_dtype_t dt, int dk, int dv) {
@@ -679,15 +693,17 @@ cudaError_t launch_prefill_tc(const FwdParams &p, cudaStream_t s) {
     if ((size_t)p.N * p.H == 0) return cudaSuccess;
     if (p.Ttot == 0) return launch_prefill_simt(p, KDA_BF16, s);  // nothing to contract
     if (p.Ttot > INT32_MAX) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo, mg;
     if (!make_token_map(&mq, p.q, p.H, p.Ttot) || !make_token_map(&mk, p.k, p.H, p.Ttot) ||
-        !make_token_map(&mv, p.v, p.H, p.Ttot))
+        !make_token_map(&mv, p.v, p.H, p.Ttot) || !make_token_map(&mo, p.o, p.H, p.Ttot) ||
+        !make_gate_map(&mg, p.log_alpha, p.H, p.Ttot))
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(TcSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<<<(unsigned)((size_t)p.N * p.H), kThreads, smem, s>>>(p, mq, mk, mv);
+    prefill_tc_kernel<<<(unsigned)((size_t)p.N * p.H), kThreads, smem, s>>>(p, mq, mk, mv, mo,
+                                                                             mg);
     return cudaGetLastError();
 }
 
