@@ -25,14 +25,19 @@
 //
 // Warp roles (384 threads, 3 warps per SM sub-partition, so up to 168
 // registers per thread):
-//   warps 0-7   chunk-local work of chunk n+1 (a1-a5): gates, scaled operands,
-//               R, masks, the triangular solve, W and U~.  Warp 0 allocates
-//               tensor memory; one thread loads each chunk's log_alpha tile
-//               (TMA) as soon as the previous tile has been read.
-//   warps 8-11  the serial carry of chunk n (a6) and the output, staged in
-//               shared memory and written with a TMA store.  Their MMA-issuing
-//               thread also refills the q/k/v stage a chunk has just released
-//               (TMA, 64 tokens x 64 channels per box, 128-byte swizzle).
+//   warps 0-7   chunk-local work of chunk n+1 (a1-a5): scaled operands, R,
+//               masks, the triangular solve (which writes T' in bf16 straight
+//               from its registers), and the W / U~ MMAs, whose completion
+//               hands the chunk to the carry.  The gate scan of the chunk after
+//               runs while R is on the tensor cores.  Warp 0 allocates tensor
+//               memory; one thread loads each chunk's log_alpha tile (TMA) as
+//               soon as the previous tile has been read.
+//   warps 8-11  the serial carry of chunk n (a6): -W out of tensor memory into
+//               the operand tile, the U, O and S MMAs, the gamma scaling of the
+//               state, and the output, staged in shared memory and written with
+//               a TMA store.  Their MMA-issuing thread also refills the q/k/v
+//               stage a chunk has just released (TMA, 64 tokens x 64 channels
+//               per box, 128-byte swizzle).
 // The chunk-local work of the next chunk overlaps the carry of the current one.
 //
 // Every wait is bounded in time; on a timeout the kernel records
@@ -58,9 +63,10 @@ constexpr int kCarryWarp0 = 8, kCarryWarps = 4, kCarryThreads = 32 * kCarryWarps
 constexpr int kThreads = 32 * (kPrepWarps + kCarryWarps);
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns (fp32 accumulators, 128 lanes each)
-constexpr uint32_t kColRW = 0;    // R, then W^T              (64 columns)
-constexpr uint32_t kColU = 64;    // U~^T / U^T, two buffers (2 x 64)
-constexpr uint32_t kColO = 192;   // O^T, two buffers         (2 x 64)
+constexpr uint32_t kColR = 0;     // R = [Kh; Qh] Kb^T        (64 columns)
+constexpr uint32_t kColW = 64;    // W^T                      (64)
+constexpr uint32_t kColU = 128;   // U~^T / U^T, two buffers (2 x 64)
+constexpr uint32_t kColO = 256;   // O^T                      (64)
 constexpr uint32_t kColSb = 320;  // S^T, bf16 pairs          (64): MMA A operand
 constexpr uint32_t kColS = 384;   // S^T master copy, fp32    (128)
 constexpr int LDA = kSolveLd;     // fp32 row stride of the solve matrix
@@ -85,8 +91,9 @@ struct __align__(1024) TcSmem {
     uint8_t ut[16384];  // U^T bf16 [v][j]; then the staged output tile [r][v]
     uint8_t gt[32768];  // log_alpha tile: 4 boxes of 32 channels x 64 tokens (fp32, swizzled)
     float as[C * LDA];  // solve matrix / inverse blocks (fp32)
-    uint64_t full[2], ready[2], uempty[2], gfull;
-    uint64_t bar_r, bar_w, bar_u, bar_s, bar_fin;
+    float ys[3 * 16 * kSolveYLd];  // solve scratch
+    uint64_t full[2], ready[2], uempty[2], gfull, wfree;
+    uint64_t bar_r, bar_u, bar_s, bar_fin;
     uint32_t tmem_base;
     int abort;
     int domain;
@@ -136,33 +143,33 @@ __device__ __forceinline__ void store_row(uint8_t *tile, int row, int col, const
         *reinterpret_cast<uint4 *>(tile + sw128_offset(row, col + j)) = pack8(f + j);
 }
 
-// Gates of one prep thread from the landed log_alpha tile: tokens 4 tg .. 4 tg + 3
-// of channels c0 .. c0 + 7.  The tile is four TMA boxes of 32 fp32 channels x 64
-// tokens with the 128-byte swizzle (16-byte chunk index XOR row % 8).
-__device__ __forceinline__ void read_gates(const uint8_t *gt, int tg, int c0, float (&g)[4][8]) {
+// Gates of one prep thread from the landed log_alpha tile: tokens 2 l, 2 l + 1
+// (l = lane) of channels c0 .. c0 + 15.  The tile is four TMA boxes of 32 fp32
+// channels x 64 tokens with the 128-byte swizzle (16-byte chunk XOR row % 8).
+__device__ __forceinline__ void read_gates(const uint8_t *gt, int lane, int c0,
+                                           float (&g)[2][16]) {
     const uint8_t *box = gt + (c0 >> 5) * 8192;
-    const int ch = (c0 & 31) >> 2;  // first of two 16-byte chunks in the 128-byte row
+    const int ch = (c0 & 31) >> 2;  // first of four 16-byte chunks in the 128-byte row
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = 4 * tg + i;
+    for (int i = 0; i < 2; ++i) {
+        const int t = 2 * lane + i;
         const uint8_t *row = box + (t >> 3) * 1024 + (t & 7) * 128;
-        const float4 a = *reinterpret_cast<const float4 *>(row + ((ch ^ (t & 7)) << 4));
-        const float4 b = *reinterpret_cast<const float4 *>(row + (((ch + 1) ^ (t & 7)) << 4));
-        g[i][0] = a.x; g[i][1] = a.y; g[i][2] = a.z; g[i][3] = a.w;
-        g[i][4] = b.x; g[i][5] = b.y; g[i][6] = b.z; g[i][7] = b.w;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 a = *reinterpret_cast<const float4 *>(row + (((ch + k) ^ (t & 7)) << 4));
+            g[i][4 * k + 0] = a.x;
+            g[i][4 * k + 1] = a.y;
+            g[i][4 * k + 2] = a.z;
+            g[i][4 * k + 3] = a.w;
+        }
     }
 }
 
 // T' = (I + A)^{-1} diag(beta) in bf16 ([r][j], 128-byte swizzle, into sm.tp)
-// for the 64 x 64 strictly lower A in sm.as.  The inverse runs on the
-// warp-level tensor cores (kda_solve.cuh) with sm.tp as its scratch.
+// for the 64 x 64 strictly lower A in sm.as, on the warp-level tensor cores
+// (kda_solve.cuh), written straight from the registers that produce it.
 __device__ __forceinline__ void solve_ut(TcSmem &sm, const float *bet, int pt) {
-    inverse_unit_lower64(sm.as, reinterpret_cast<float *>(sm.tp), pt, kBarPrep);
-    const int row = pt >> 2, j0 = 16 * (pt & 3);
-    float f[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) f[e] = inv_entry(sm.as, row, j0 + e) * bet[j0 + e];
-    store_row<16>(sm.tp, row, j0, f);
+    inverse_unit_lower64(sm.as, sm.ys, pt, kBarPrep, TprimeOut{sm.tp, bet});
 }
 
 // Pack 16 fp32 values (as bits) into 8 bf16 pairs (even index in the low half).
@@ -210,11 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&sm.uempty[s]), 1);
         }
         mbar_init(smem_u32(&sm.bar_r), 1);
-        mbar_init(smem_u32(&sm.bar_w), 1);
         mbar_init(smem_u32(&sm.bar_u), 1);
         mbar_init(smem_u32(&sm.bar_s), 1);
         mbar_init(smem_u32(&sm.bar_fin), 2);
         mbar_init(smem_u32(&sm.gfull), 1);
+        mbar_init(smem_u32(&sm.wfree), 1);
         fence_mbar_init();
     }
     if (warp == kPrepWarp0) {
@@ -274,11 +281,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pt = tid - 32 * kPrepWarp0;     // 0..255
         const int pw = pt >> 5;                   // prep warp 0..7
         const int half = pw >> 2;                 // which 32 of 64 TMEM columns
-        const int cg = pt >> 4, tg = pt & 15;     // 8 channels x 4 tokens per thread
-        const int c0 = 8 * cg;
+        // gates and scaled operands: warp pw owns channels 16 pw .. 16 pw + 15, lane l
+        // tokens 2 l and 2 l + 1, so the prefix sum over tokens is one warp scan
+        const int c0 = 16 * pw;
         const int slab = c0 >> 6, col = c0 & 63;
         bool domain_ok = true;
 
+        // a1 for chunk m: log2-decay cumsum G2[t][c] = log2(e) sum_{t' <= t} log_alpha
+        // of this thread's two tokens and 16 channels, from the landed gate tile.
+        auto gate_scan = [&](int m, float (&g)[2][16]) {
+            const int validm = min(C, len - m * C);
+            wait_phase_warp(sm.gfull, m & 1, abort);
+            read_gates(sm.gt, lane, c0, g);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const bool live = 2 * lane + i < validm;  // the tile runs past the sequence end
+#pragma unroll
+                for (int e = 0; e < 16; ++e) g[i][e] = live ? g[i][e] * kLog2e : 0.f;
+            }
+            float inc[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) inc[e] = g[0][e] + g[1][e];  // this lane's total
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {  // inclusive scan across the warp
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float up = __shfl_up_sync(0xffffffffu, inc[e], o);
+                    if (lane >= o) inc[e] += up;
+                }
+            }
+            float lo = 0.f, hi = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float x1 = g[1][e];
+                g[1][e] = inc[e];       // G2 at token 2 l + 1
+                g[0][e] = inc[e] - x1;  // G2 at token 2 l
+                lo = fminf(lo, fminf(g[0][e], g[1][e]));
+                hi = fmaxf(hi, fmaxf(g[0][e], g[1][e]));
+            }
+            if (-lo > kLog2DecayLimit || hi > kLog2DecayLimit) domain_ok = false;
+        };
+
+        float gnx[2][16];  // G2 of the next chunk, scanned one chunk ahead
+        gate_scan(0, gnx);
+        named_bar_sync(kBarPrep, kPrepThreads);  // every thread has read tile 0
+        if (pt == 0 && nchunks > 1) load_gates(1);
         float bn = 0.f;  // beta of the next chunk, loaded one chunk ahead
         if (pt < C && pt < len) bn = p.beta[(size_t)(start + pt) * p.H + h];
 
@@ -287,57 +334,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             TcStage &S = sm.st[s];
             const int64_t t0 = start + (int64_t)n * C;
             const int valid = min(C, len - n * C);
-
-            // a1: in-chunk cumulative log2-decay G2[t][c] = log2(e) sum_{t' <= t} log_alpha
-            float g[4][8];
-            wait_phase_warp(sm.gfull, n & 1, abort);
-            read_gates(sm.gt, tg, c0, g);
+            float g[2][16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool live = 4 * tg + i < valid;  // the tile runs past the sequence end
+            for (int i = 0; i < 2; ++i)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) g[i][e] = live ? g[i][e] * kLog2e : 0.f;
-            }
+                for (int e = 0; e < 16; ++e) g[i][e] = gnx[i][e];
             const float bet = bn;
-#pragma unroll
-            for (int i = 1; i < 4; ++i)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) g[i][e] += g[i - 1][e];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float tot = g[3][e];
-                float inc = tot;
-#pragma unroll
-                for (int o = 1; o < 16; o <<= 1) {
-                    const float up = __shfl_up_sync(0xffffffffu, inc, o, 16);
-                    if (tg >= o) inc += up;
-                }
-                const float pre = inc - tot;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    g[i][e] += pre;
-                    if (fabsf(g[i][e]) > kLog2DecayLimit) domain_ok = false;
-                }
-            }
-            if (n + 1 < nchunks) {  // beta of the next chunk
-                const int64_t t1 = t0 + C;
+            if (n + 1 < nchunks) {
                 const int valid1 = min(C, len - (n + 1) * C);
-                bn = (pt < C && pt < valid1) ? p.beta[(size_t)(t1 + pt) * p.H + h] : 0.f;
+                bn = (pt < C && pt < valid1) ? p.beta[(size_t)(t0 + C + pt) * p.H + h] : 0.f;
             }
 
             wait_phase_warp(sm.full[s], (n >> 1) & 1, abort);
-            if (tg == 15)
+            if (lane == 31)  // token 63 closes the chunk
 #pragma unroll
-                for (int e = 0; e < 8; ++e) S.gam[c0 + e] = exp2f(g[3][e]);
+                for (int e = 0; e < 16; ++e) S.gam[c0 + e] = exp2f(g[1][e]);
             if (pt < C) S.bet[pt] = bet;
 
             // a2: scaled operands, written over the landed tiles (same swizzle)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float *gr = g[i];
-                const int t = 4 * tg + i;
-                const uint32_t off = slab * 16384 + sw128_offset(t, col);
-                const uint32_t offv = slab * 8192 + sw128_offset(t, col);
+            for (int ik = 0; ik < 4; ++ik) {
+                const int i = ik >> 1, k = ik & 1;
+                const float *gr = g[i] + 8 * k;
+                const int t = 2 * lane + i;
+                const uint32_t off = slab * 16384 + sw128_offset(t, col + 8 * k);
+                const uint32_t offv = slab * 8192 + sw128_offset(t, col + 8 * k);
                 float kf[8], qf[8], kb[8];
                 if (t < valid) {
                     unpack8(*reinterpret_cast<const uint4 *>(S.kq + off), kf);
@@ -361,8 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             named_bar_sync(kBarPrep, kPrepThreads);
-            // every prep thread has read this chunk's gates: fetch the next tile
-            if (pt == 0 && n + 1 < nchunks) load_gates(n + 1);
 
             // a3 + a5: R = [Kh; Qh] Kb^T (M = 128, N = 64, K = 128)
             if (pt == 0) {
@@ -374,17 +393,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         desc_sw128(smem_u32(S.kq) + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
                     const uint64_t b =
                         desc_sw128(smem_u32(S.kb) + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
-                    mma_bf16(tmem + kColRW, a, b, id, k > 0);
+                    mma_bf16(tmem + kColR, a, b, id, k > 0);
                 }
                 mma_commit(smem_u32(&sm.bar_r));
             }
+            // while R is computed: the gate scan of the next chunk
+            if (n + 1 < nchunks) gate_scan(n + 1, gnx);
             wait_phase_warp(sm.bar_r, n & 1, abort);
             tc_fence_after();
 #pragma unroll
             for (int piece = 0; piece < 2; ++piece) {
                 const int j0 = 32 * half + 16 * piece;
                 uint32_t x[16];
-                tmem_ld16(tmem + lane_addr + kColRW + j0, x);
+                tmem_ld16(tmem + lane_addr + kColR + j0, x);
                 if (L < 64) {  // A[r][j] = beta_r R[r][j], j < r
                     const int r = L;
                     const float br = S.bet[r];
@@ -409,14 +430,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             named_bar_sync(kBarPrep, kPrepThreads);
+            // every thread has read the next chunk's gate tile: fetch the one after
+            if (pt == 0 && n + 2 < nchunks) load_gates(n + 2);
 
             // a4: T' = (I + A)^-1 diag(beta)
             solve_ut(sm, S.bet, pt);
             fence_proxy_async_smem();
             named_bar_sync(kBarPrep, kPrepThreads);
 
-            // a4: W^T = Kh^T T'^T, U~^T = V^T T'^T (M = 128, N = 64, K = 64)
+            // a4: W^T = Kh^T T'^T, U~^T = V^T T'^T (M = 128, N = 64, K = 64); their
+            // completion hands the chunk to the carry warps (ready[s]).
             if (pt == 0) {
+                if (n >= 1) wait_phase(sm.wfree, (n - 1) & 1, abort);
                 if (n >= 2) wait_phase(sm.uempty[s], ((n >> 1) - 1) & 1, abort);
                 tc_fence_after();
                 const uint32_t id = idesc_bf16(128, 64, true, false);
@@ -425,27 +450,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t aw = desc_sw128(smem_u32(S.kq) + k * 2048, 16384, 1024);
                     const uint64_t av = desc_sw128(smem_u32(S.v) + k * 2048, 8192, 1024);
                     const uint64_t b = desc_sw128(smem_u32(sm.tp) + k * 32, 16, 1024);
-                    mma_bf16(tmem + kColRW, aw, b, id, k > 0);
+                    mma_bf16(tmem + kColW, aw, b, id, k > 0);
                     mma_bf16(tmem + kColU + 64 * s, av, b, id, k > 0);
                 }
-                mma_commit(smem_u32(&sm.bar_w));
+                mma_commit(smem_u32(&sm.ready[s]));
             }
-            wait_phase_warp(sm.bar_w, n & 1, abort);
-            tc_fence_after();
-#pragma unroll
-            for (int piece = 0; piece < 2; ++piece) {  // -W as the MN-major operand [c][r]
-                const int c = L, j0 = 32 * half + 16 * piece;
-                uint32_t x[16];
-                tmem_ld16(tmem + lane_addr + kColRW + j0, x);
-                float f[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = -__uint_as_float(x[j]);
-                store_row<16>(S.kq + (c >> 6) * 16384, c & 63, j0, f);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar_sync(kBarPrep, kPrepThreads);
-            if (pt == 0) mbar_arrive(smem_u32(&sm.ready[s]));
         }
         if (!domain_ok) sm.domain = 1;
     } else {
@@ -475,42 +484,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_sync(kBarCarry, kCarryThreads);
         }
 
-        auto issue_carry_in = [&](int n) {  // U^T += S^T (-W)^T ; O^T = S^T Qh^T (S^T from TMEM)
-            const int s = n & 1;
-            TcStage &S = sm.st[s];
-            wait_phase(sm.ready[s], (n >> 1) & 1, abort);
-            tc_fence_after();
-            const uint32_t id_u = idesc_bf16(128, 64, false, true);
-            const uint32_t id_o = idesc_bf16(128, 64, false, false);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t a = tmem + kColSb + 8 * k;
-                const uint64_t bw =
-                    desc_sw128(smem_u32(S.kq) + (k >> 2) * 16384 + (k & 3) * 2048, 8192, 1024);
-                const uint64_t bq = desc_sw128(
-                    smem_u32(S.kq) + 8192 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-                mma_bf16_tmem_a(tmem + kColU + 64 * s, a, bw, id_u, 1);
-                mma_bf16_tmem_a(tmem + kColO + 64 * s, a, bq, id_o, k > 0);
-            }
-            mma_commit(smem_u32(&sm.bar_u));
-        };
-
         // O^T of chunk n (lane v, column r) -> staged tile [r][v] in sm.ut (two
         // 64-channel slabs, 128-byte swizzle) -> global: one TMA store per slab
         // for a full chunk; a masked copy for the last, partial chunk.
         auto store_output = [&](int n) {
-            const int s = n & 1;
             const int64_t t0 = start + (int64_t)n * C;
             const int valid = min(C, len - n * C);
             uint8_t *stage = sm.ut + (v >> 6) * 8192;
             const int vc = v & 63;
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t x[16];
-                tmem_ld16(tmem + lane_addr + kColO + 64 * s + 16 * cb, x);
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t x[32];
+                tmem_ld32(tmem + lane_addr + kColO + 32 * cb, x);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    *reinterpret_cast<__nv_bfloat16 *>(stage + sw128_offset(16 * cb + j, vc)) =
+                for (int j = 0; j < 32; ++j)
+                    *reinterpret_cast<__nv_bfloat16 *>(stage + sw128_offset(32 * cb + j, vc)) =
                         __float2bfloat16_rn(__uint_as_float(x[j]));
             }
             tc_fence_before();
@@ -534,24 +522,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
 
-        if (issuer) issue_carry_in(0);
         for (int n = 0; n < nchunks; ++n) {
             const int s = n & 1;
             TcStage &S = sm.st[s];
-            __syncwarp();  // the issuer lane rejoins before the warp-wide TMEM loads
+            // W^T and U~^T of chunk n are complete: -W as the MN-major operand
+            // [c][r] over the Kh area (lane c holds row c of W^T)
+            __syncwarp();
+            wait_phase_warp(sm.ready[s], (n >> 1) & 1, abort);
+            tc_fence_after();
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t x[32];
+                tmem_ld32(tmem + lane_addr + kColW + 32 * cb, x);
+                float f[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) f[j] = -__uint_as_float(x[j]);
+                store_row<32>(S.kq + (v >> 6) * 16384, v & 63, 32 * cb, f);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar_sync(kBarCarry, kCarryThreads);
+            if (issuer) {  // U^T += S^T (-W)^T, S^T read from tensor memory
+                mbar_arrive(smem_u32(&sm.wfree));
+                tc_fence_after();
+                const uint32_t id_u = idesc_bf16(128, 64, false, true);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t bw =
+                        desc_sw128(smem_u32(S.kq) + (k >> 2) * 16384 + (k & 3) * 2048, 8192, 1024);
+                    mma_bf16_tmem_a(tmem + kColU + 64 * s, tmem + kColSb + 8 * k, bw, id_u, 1);
+                }
+                mma_commit(smem_u32(&sm.bar_u));
+            }
+            __syncwarp();
+            if (n >= 1) store_output(n - 1);  // frees the O accumulator
+            if (issuer) {  // O^T = S^T Qh^T
+                tc_fence_after();
+                const uint32_t id_o = idesc_bf16(128, 64, false, false);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t bq = desc_sw128(
+                        smem_u32(S.kq) + 8192 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+                    mma_bf16_tmem_a(tmem + kColO, tmem + kColSb + 8 * k, bq, id_o, k > 0);
+                }
+            }
+            __syncwarp();
             wait_phase_warp(sm.bar_u, n & 1, abort);
             if (issuer) bulk_wait_group_read0();  // the previous output tile has left sm.ut
             named_bar_sync(kBarCarry, kCarryThreads);
             tc_fence_after();
             // U^T (lane v, column j) -> bf16 operand [v][j]
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t x[16];
-                tmem_ld16(tmem + lane_addr + kColU + 64 * s + 16 * cb, x);
-                float f[16];
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t x[32];
+                tmem_ld32(tmem + lane_addr + kColU + 64 * s + 32 * cb, x);
+                float f[32];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(x[j]);
-                store_row<16>(sm.ut, v, 16 * cb, f);
+                for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(x[j]);
+                store_row<32>(sm.ut, v, 32 * cb, f);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -566,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t a = desc_sw128(smem_u32(sm.ut) + k * 32, 16, 1024);
                     const uint64_t bm = desc_sw128(smem_u32(S.m) + k * 32, 16, 1024);
                     const uint64_t bk = desc_sw128(smem_u32(S.kb) + k * 2048, 8192, 1024);
-                    mma_bf16(tmem + kColO + 64 * s, a, bm, id_o, 1);
+                    mma_bf16(tmem + kColO, a, bm, id_o, 1);
                     mma_bf16(tmem + kColS, a, bk, id_s, 1);
                 }
                 mma_commit(smem_u32(&sm.bar_s));
@@ -576,34 +604,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // S^T <- (S^T + U^T Kb) scaled by gamma along c: TMEM fp32 and bf16 copy
 #pragma unroll
-            for (int cb = 0; cb < 8; ++cb) {
-                uint32_t x[16];
-                tmem_ld16(tmem + lane_addr + kColS + 16 * cb, x);
-                const float4 *gm = reinterpret_cast<const float4 *>(S.gam + 16 * cb);
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t x[32];
+                tmem_ld32(tmem + lane_addr + kColS + 32 * cb, x);
+                const float4 *gm = reinterpret_cast<const float4 *>(S.gam + 32 * cb);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 8; ++q) {
                     const float4 gq = gm[q];
                     x[4 * q + 0] = __float_as_uint(__uint_as_float(x[4 * q + 0]) * gq.x);
                     x[4 * q + 1] = __float_as_uint(__uint_as_float(x[4 * q + 1]) * gq.y);
                     x[4 * q + 2] = __float_as_uint(__uint_as_float(x[4 * q + 2]) * gq.z);
                     x[4 * q + 3] = __float_as_uint(__uint_as_float(x[4 * q + 3]) * gq.w);
                 }
-                tmem_st16(tmem + lane_addr + kColS + 16 * cb, x);
-                uint32_t w[8];
-                pack16(x, w);
-                tmem_st8(tmem + lane_addr + kColSb + 8 * cb, w);
+                tmem_st32(tmem + lane_addr + kColS + 32 * cb, x);
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    w[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+                tmem_st16(tmem + lane_addr + kColSb + 16 * cb, w);
             }
             tmem_wait_st();
             tc_fence_before();
             named_bar_sync(kBarCarry, kCarryThreads);
-            if (issuer) {
-                // stage s is no longer read by anyone: refill it with chunk n + 2
-                if (n + 2 < nchunks) load_stage(n + 2);
-                if (n + 1 < nchunks) issue_carry_in(n + 1);
-            }
-            __syncwarp();
-            store_output(n);  // overlaps the MMAs of chunk n + 1
+            // stage s is no longer read by anyone: refill it with chunk n + 2
+            if (issuer && n + 2 < nchunks) load_stage(n + 2);
         }
+        __syncwarp();
+        store_output(nchunks - 1);
         if (issuer) bulk_wait_group0();
         __syncwarp();
         if (p.S_T) {

@@ -12,6 +12,7 @@
 // solve costs a few hundred shared-memory cycles instead of thousands.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 #include "kda_sm100.cuh"
@@ -79,10 +80,26 @@ __device__ __forceinline__ const float *t_block(const float *as, int bi, int bj)
     return as + (16 * bj) * kSolveLd + 16 * bi;
 }
 
-// T = (I + A)^-1 in place in `as` (see the file comment).  `ys` is scratch for
-// three 16 x kSolveYLd blocks.  Called by 256 threads (8 warps) that all reach
-// the named barrier `bar` (id) between the stages.
-__device__ __forceinline__ void inverse_unit_lower64(float *as, float *ys, int pt, uint32_t bar) {
+// Byte offset of bf16 element (row, col) of a 64 x 64 tile with 128-byte rows
+// and the 128-byte swizzle (16-byte chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t tp_offset(int row, int col) {
+    return (row >> 3) * 1024 + (row & 7) * 128 + ((((col >> 3) ^ row) & 7) << 4) + (col & 7) * 2;
+}
+
+// Optional second output of the inverse: T' = T diag(beta) in bf16, written
+// straight from the registers that produce T into a swizzled tile (the B
+// operand of the W and U~ products).
+struct TprimeOut {
+    uint8_t *tile;      // 64 x 64 bf16, 128-byte swizzle; nullptr: no second output
+    const float *beta;  // column scale, 64 values
+};
+
+// T = (I + A)^-1 in place in `as` (see the file comment), and T' when
+// `out.tile` is set.  `ys` is scratch for three 16 x kSolveYLd blocks.  Called
+// by 256 threads (8 warps) that all reach the named barrier `bar` (id)
+// between the stages.
+__device__ __forceinline__ void inverse_unit_lower64(float *as, float *ys, int pt, uint32_t bar,
+                                                     TprimeOut out = {nullptr, nullptr}) {
     const int warp = pt >> 5, lane = pt & 31;
     // diagonal 16 x 16 blocks: lane = column c of block b, forward substitution
     if (pt < 64) {
@@ -107,6 +124,23 @@ __device__ __forceinline__ void inverse_unit_lower64(float *as, float *ys, int p
         __syncwarp();
 #pragma unroll
         for (int r = 0; r < 16; ++r) Ab[r * kSolveLd + c] = x[r];
+        if (out.tile) {
+            const float bc = out.beta[16 * b + c];
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                *reinterpret_cast<__nv_bfloat16 *>(out.tile + tp_offset(16 * b + r, 16 * b + c)) =
+                    __float2bfloat16_rn(x[r] * bc);
+        }
+    } else if (out.tile && pt < 64 + 96) {
+        // zero the six blocks above the diagonal of T' (16-byte pieces)
+        const int q = pt - 64, blk = q >> 4, piece = q & 15;  // 6 blocks x 16 rows
+        const int bi = blk < 3 ? 0 : blk < 5 ? 1 : 2;
+        const int bj = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
+        const int row = 16 * bi + piece;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            *reinterpret_cast<uint4 *>(out.tile + tp_offset(row, 16 * bj + 8 * h)) =
+                make_uint4(0, 0, 0, 0);
     }
     sm100::named_bar_sync(bar, 256);
     // off-diagonal blocks, one block per warp, diagonal d = 1, 2, 3
@@ -124,6 +158,18 @@ __device__ __forceinline__ void inverse_unit_lower64(float *as, float *ys, int p
             float tt[2][4] = {};
             mma_block16(tt, t_block(as, bi, bi), kSolveLd, Y, kSolveYLd, lane);
             store_block16(as + (16 * bj) * kSolveLd + 16 * bi, kSolveLd, tt, -1.f, lane);
+            if (out.tile) {  // T' block (bi, bj) = -tt scaled by beta along columns
+                const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int col = 16 * bj + 8 * nt + 2 * t;
+                    const float b0 = out.beta[col], b1 = out.beta[col + 1];
+                    *reinterpret_cast<uint32_t *>(out.tile + tp_offset(16 * bi + g, col)) =
+                        sm100::pack_bf16(-tt[nt][0] * b0, -tt[nt][1] * b1);
+                    *reinterpret_cast<uint32_t *>(out.tile + tp_offset(16 * bi + g + 8, col)) =
+                        sm100::pack_bf16(-tt[nt][2] * b0, -tt[nt][3] * b1);
+                }
+            }
         }
         sm100::named_bar_sync(bar, 256);
     }
