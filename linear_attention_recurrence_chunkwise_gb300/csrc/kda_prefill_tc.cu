@@ -26,18 +26,21 @@
 // Warp roles (384 threads, 3 warps per SM sub-partition, so up to 168
 // registers per thread):
 //   warps 0-7   chunk-local work of chunk n+1 (a1-a5): scaled operands, R,
-//               masks, the triangular solve (which writes T' in bf16 straight
-//               from its registers), and the W / U~ MMAs, whose completion
-//               hands the chunk to the carry.  The gate scan of the chunk after
-//               runs while R is on the tensor cores.  Warp 0 allocates tensor
-//               memory; one thread loads each chunk's log_alpha tile (TMA) as
-//               soon as the previous tile has been read.
-//   warps 8-11  the serial carry of chunk n (a6): -W out of tensor memory into
-//               the operand tile, the U, O and S MMAs, the gamma scaling of the
-//               state, and the output, staged in shared memory and written with
-//               a TMA store.  Their MMA-issuing thread also refills the q/k/v
-//               stage a chunk has just released (TMA, 64 tokens x 64 channels
-//               per box, 128-byte swizzle).
+//               masks and the triangular solve, which writes T' in bf16 straight
+//               from its registers and so hands the chunk to the carry warps.
+//               The gate scan of the chunk after runs while R is on the tensor
+//               cores.  Warp 0 allocates tensor memory; one thread loads each
+//               chunk's log_alpha tile (TMA) as soon as the previous tile has
+//               been read.
+//   warps 8-11  the serial carry of chunk n (a6): the W / U~ MMAs, -W out of
+//               tensor memory into the operand tile, the U, O and S MMAs, the
+//               gamma scaling of the state, and the output, staged in shared
+//               memory and written with a TMA store.  Their MMA-issuing thread
+//               also refills the q/k/v stage a chunk has just released (TMA, 64
+//               tokens x 64 channels per box, 128-byte swizzle).  Issuing an MMA
+//               keeps a thread busy for about as long as the MMA runs, so the
+//               W / U~ products are issued here, where the carry would otherwise
+//               wait for the chunk-local warps.
 // The chunk-local work of the next chunk overlaps the carry of the current one.
 //
 // Every wait is bounded in time; on a timeout the kernel records
@@ -70,7 +73,7 @@ constexpr uint32_t kColO = 256;   // O^T                      (64)
 constexpr uint32_t kColSb = 320;  // S^T, bf16 pairs          (64): MMA A operand
 constexpr uint32_t kColS = 384;   // S^T master copy, fp32    (128)
 constexpr int LDA = kSolveLd;     // fp32 row stride of the solve matrix
-constexpr uint32_t kBarPrep = 1, kBarCarry = 2;  // named barrier ids
+constexpr uint32_t kBarPrep = 1, kBarCarry = 2, kBarSolve = 3;  // named barrier ids
 constexpr uint32_t kTileBytes = 64 * 64 * 2;     // one TMA box
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLog2DecayLimit = kLogDecayLimit * kLog2e;
@@ -91,8 +94,7 @@ struct __align__(1024) TcSmem {
     uint8_t ut[16384];  // U^T bf16 [v][j]; then the staged output tile [r][v]
     uint8_t gt[32768];  // log_alpha tile: 4 boxes of 32 channels x 64 tokens (fp32, swizzled)
     float as[C * LDA];  // solve matrix / inverse blocks (fp32)
-    float ys[3 * 16 * kSolveYLd];  // solve scratch
-    uint64_t full[2], ready[2], uempty[2], gfull, wfree;
+    uint64_t full[2], ready[2], gfull, tpfull;
     uint64_t bar_r, bar_u, bar_s, bar_fin;
     uint32_t tmem_base;
     int abort;
@@ -146,13 +148,13 @@ __device__ __forceinline__ void store_row(uint8_t *tile, int row, int col, const
 // Gates of one prep thread from the landed log_alpha tile: tokens 2 l, 2 l + 1
 // (l = lane) of channels c0 .. c0 + 15.  The tile is four TMA boxes of 32 fp32
 // channels x 64 tokens with the 128-byte swizzle (16-byte chunk XOR row % 8).
-__device__ __forceinline__ void read_gates(const uint8_t *gt, int lane, int c0,
+__device__ __forceinline__ void read_gates(const uint8_t *gt, int lane, int fl, int c0,
                                            float (&g)[2][16]) {
     const uint8_t *box = gt + (c0 >> 5) * 8192;
     const int ch = (c0 & 31) >> 2;  // first of four 16-byte chunks in the 128-byte row
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        const int t = 2 * lane + i;
+        const int t = 2 * lane + (i ^ fl);
         const uint8_t *row = box + (t >> 3) * 1024 + (t & 7) * 128;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -169,7 +171,7 @@ __device__ __forceinline__ void read_gates(const uint8_t *gt, int lane, int c0,
 // for the 64 x 64 strictly lower A in sm.as, on the warp-level tensor cores
 // (kda_solve.cuh), written straight from the registers that produce it.
 __device__ __forceinline__ void solve_ut(TcSmem &sm, const float *bet, int pt) {
-    inverse_unit_lower64(sm.as, sm.ys, pt, kBarPrep, TprimeOut{sm.tp, bet});
+    solve_tprime64(sm.as, bet, sm.tp, pt, kBarSolve);
 }
 
 // Pack 16 fp32 values (as bits) into 8 bf16 pairs (even index in the low half).
@@ -214,14 +216,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.ready[s]), 1);
-            mbar_init(smem_u32(&sm.uempty[s]), 1);
         }
         mbar_init(smem_u32(&sm.bar_r), 1);
         mbar_init(smem_u32(&sm.bar_u), 1);
         mbar_init(smem_u32(&sm.bar_s), 1);
         mbar_init(smem_u32(&sm.bar_fin), 2);
         mbar_init(smem_u32(&sm.gfull), 1);
-        mbar_init(smem_u32(&sm.wfree), 1);
+        mbar_init(smem_u32(&sm.tpfull), 1);
         fence_mbar_init();
     }
     if (warp == kPrepWarp0) {
@@ -282,7 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pw = pt >> 5;                   // prep warp 0..7
         const int half = pw >> 2;                 // which 32 of 64 TMEM columns
         // gates and scaled operands: warp pw owns channels 16 pw .. 16 pw + 15, lane l
-        // tokens 2 l and 2 l + 1, so the prefix sum over tokens is one warp scan
+        // tokens 2 l and 2 l + 1, so the prefix sum over tokens is one warp scan.
+        // Register slot i holds token 2 l + (i ^ fl): lanes 4-7 of each group of 8
+        // take the odd token first, so the 8 lanes of a shared-memory phase touch
+        // 8 different rows mod 8 -- 8 different 16-byte columns of the swizzled
+        // tiles, free of bank conflicts.
+        const int fl = (lane >> 2) & 1;
         const int c0 = 16 * pw;
         const int slab = c0 >> 6, col = c0 & 63;
         bool domain_ok = true;
@@ -292,10 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto gate_scan = [&](int m, float (&g)[2][16]) {
             const int validm = min(C, len - m * C);
             wait_phase_warp(sm.gfull, m & 1, abort);
-            read_gates(sm.gt, lane, c0, g);
+            read_gates(sm.gt, lane, fl, c0, g);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const bool live = 2 * lane + i < validm;  // the tile runs past the sequence end
+                const bool live = 2 * lane + (i ^ fl) < validm;  // the tile runs past the sequence end
 #pragma unroll
                 for (int e = 0; e < 16; ++e) g[i][e] = live ? g[i][e] * kLog2e : 0.f;
             }
@@ -313,9 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             float lo = 0.f, hi = 0.f;
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-                const float x1 = g[1][e];
-                g[1][e] = inc[e];       // G2 at token 2 l + 1
-                g[0][e] = inc[e] - x1;  // G2 at token 2 l
+                const float x1 = fl ? g[0][e] : g[1][e];  // log-decay of token 2 l + 1
+                const float ge = inc[e] - x1;              // G2 at token 2 l
+                g[0][e] = fl ? inc[e] : ge;
+                g[1][e] = fl ? ge : inc[e];
                 lo = fminf(lo, fminf(g[0][e], g[1][e]));
                 hi = fmaxf(hi, fmaxf(g[0][e], g[1][e]));
             }
@@ -346,9 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             wait_phase_warp(sm.full[s], (n >> 1) & 1, abort);
-            if (lane == 31)  // token 63 closes the chunk
+            if (lane == 31)  // token 63 closes the chunk (lane 31 keeps it in slot 0)
 #pragma unroll
-                for (int e = 0; e < 16; ++e) S.gam[c0 + e] = exp2f(g[1][e]);
+                for (int e = 0; e < 16; ++e) S.gam[c0 + e] = exp2f(g[0][e]);
             if (pt < C) S.bet[pt] = bet;
 
             // a2: scaled operands, written over the landed tiles (same swizzle)
@@ -356,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ik = 0; ik < 4; ++ik) {
                 const int i = ik >> 1, k = ik & 1;
                 const float *gr = g[i] + 8 * k;
-                const int t = 2 * lane + i;
+                const int t = 2 * lane + (i ^ fl);
                 const uint32_t off = slab * 16384 + sw128_offset(t, col + 8 * k);
                 const uint32_t offv = slab * 8192 + sw128_offset(t, col + 8 * k);
                 float kf[8], qf[8], kb[8];
@@ -428,33 +435,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     store_row<16>(S.m, r, j0, f);
                 }
             }
+            // the previous chunk's W and U~ products (issued by the carry
+            // warps) have finished reading sm.tp
+            if (pt == 0 && n >= 1) wait_phase(sm.ready[s ^ 1], ((n - 1) >> 1) & 1, abort);
             tc_fence_before();
             named_bar_sync(kBarPrep, kPrepThreads);
             // every thread has read the next chunk's gate tile: fetch the one after
-            if (pt == 0 && n + 2 < nchunks) load_gates(n + 2);
+            // (from warp 7, which has no part in the first steps of the solve)
+            if (pt == 224 && n + 2 < nchunks) load_gates(n + 2);
 
-            // a4: T' = (I + A)^-1 diag(beta)
+            // a4: T' = (I + A)^-1 diag(beta); the carry warps take it from here
             solve_ut(sm, S.bet, pt);
             fence_proxy_async_smem();
             named_bar_sync(kBarPrep, kPrepThreads);
-
-            // a4: W^T = Kh^T T'^T, U~^T = V^T T'^T (M = 128, N = 64, K = 64); their
-            // completion hands the chunk to the carry warps (ready[s]).
-            if (pt == 0) {
-                if (n >= 1) wait_phase(sm.wfree, (n - 1) & 1, abort);
-                if (n >= 2) wait_phase(sm.uempty[s], ((n >> 1) - 1) & 1, abort);
-                tc_fence_after();
-                const uint32_t id = idesc_bf16(128, 64, true, false);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint64_t aw = desc_sw128(smem_u32(S.kq) + k * 2048, 16384, 1024);
-                    const uint64_t av = desc_sw128(smem_u32(S.v) + k * 2048, 8192, 1024);
-                    const uint64_t b = desc_sw128(smem_u32(sm.tp) + k * 32, 16, 1024);
-                    mma_bf16(tmem + kColW, aw, b, id, k > 0);
-                    mma_bf16(tmem + kColU + 64 * s, av, b, id, k > 0);
-                }
-                mma_commit(smem_u32(&sm.ready[s]));
-            }
+            if (pt == 0) mbar_arrive(smem_u32(&sm.tpfull));
         }
         if (!domain_ok) sm.domain = 1;
     } else {
@@ -525,6 +519,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = 0; n < nchunks; ++n) {
             const int s = n & 1;
             TcStage &S = sm.st[s];
+            // a4: W^T = Kh^T T'^T, U~^T = V^T T'^T (M = 128, N = 64, K = 64) once
+            // the chunk-local warps have T'
+            if (issuer) {
+                wait_phase(sm.tpfull, n & 1, abort);
+                tc_fence_after();
+                const uint32_t id = idesc_bf16(128, 64, true, false);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t aw = desc_sw128(smem_u32(S.kq) + k * 2048, 16384, 1024);
+                    const uint64_t av = desc_sw128(smem_u32(S.v) + k * 2048, 8192, 1024);
+                    const uint64_t b = desc_sw128(smem_u32(sm.tp) + k * 32, 16, 1024);
+                    mma_bf16(tmem + kColW, aw, b, id, k > 0);
+                    mma_bf16(tmem + kColU + 64 * s, av, b, id, k > 0);
+                }
+                mma_commit(smem_u32(&sm.ready[s]));
+            }
             // W^T and U~^T of chunk n are complete: -W as the MN-major operand
             // [c][r] over the Kh area (lane c holds row c of W^T)
             __syncwarp();
@@ -543,7 +553,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             named_bar_sync(kBarCarry, kCarryThreads);
             if (issuer) {  // U^T += S^T (-W)^T, S^T read from tensor memory
-                mbar_arrive(smem_u32(&sm.wfree));
                 tc_fence_after();
                 const uint32_t id_u = idesc_bf16(128, 64, false, true);
 #pragma unroll
@@ -585,7 +594,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             named_bar_sync(kBarCarry, kCarryThreads);
             if (issuer) {
-                mbar_arrive(smem_u32(&sm.uempty[s]));
                 tc_fence_after();
                 const uint32_t id_o = idesc_bf16(128, 64, false, false);
                 const uint32_t id_s = idesc_bf16(128, 128, false, true);

@@ -1,15 +1,20 @@
-// Inverse of a 64 x 64 unit lower-triangular matrix, (I + A)^-1 with A
-// strictly lower, on the warp-level tensor cores (mma.sync, TF32 inputs, fp32
-// accumulate) -- the UT/WY solve of a 64-token chunk.
+// T' = (I + A)^-1 diag(beta) for a 64 x 64 strictly lower-triangular A -- the
+// UT/WY solve of a 64-token chunk -- on the warp-level tensor cores (mma.sync,
+// TF32 inputs, fp32 accumulate), written in bf16 as the 128-byte-swizzled
+// operand tile of the W and U~ products.
 //
-// Layout: fp32 row-major with row stride kSolveLd.  On entry `as` holds A
-// (zero on and above the diagonal).  The diagonal 16 x 16 blocks are inverted
-// by forward substitution (one lane per column); the off-diagonal blocks then
-// follow diagonal by diagonal, T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, as
-// 16 x 16 x 16 mma.sync products.  On exit T_ii sits in the diagonal block and
-// T_ij (i > j) in the otherwise unused upper block (j, i); inv_entry() reads T.
-// Every block product reads its operands from shared memory once, so the
-// solve costs a few hundred shared-memory cycles instead of thousands.
+// With T = (I + A)^-1 cut into 16 x 16 blocks T_IJ (I >= J):
+//   1. the diagonal blocks T_II, by forward substitution (one lane per column);
+//   2. T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (one warp each), which
+//      completes the two 32 x 32 diagonal halves of T;
+//   3. the lower-left 32 x 32 half, T_IJ = -sum_K T_IK X_KJ with
+//      X_KJ = sum_L A_KL T_LJ (I, K in {2, 3}; J, L in {0, 1}), one warp per
+//      output block.
+// Each warp keeps the intermediate X in mma.sync accumulator registers and
+// feeds it straight into the next product as its B operand (see mma_xt and
+// mma_tx), so a chain of block products never goes through shared memory.
+// Three dependent steps with two barriers in between, instead of one step per
+// block diagonal.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -19,8 +24,7 @@
 
 namespace kda {
 
-constexpr int kSolveLd = 68;     // fp32 row stride of the matrix
-constexpr int kSolveYLd = 20;    // fp32 row stride of a 16 x 16 scratch block
+constexpr int kSolveLd = 68;  // fp32 row stride of the matrix
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
@@ -38,46 +42,67 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// acc[nt] += X (16 x 16 block at xs, row stride ldx) * Y (16 x 16 block at ys,
-// row stride ldy), the two 8-column halves of the product in acc[0], acc[1]
-// (mma.sync accumulator fragments).
-__device__ __forceinline__ void mma_block16(float (&acc)[2][4], const float *xs, int ldx,
-                                            const float *ys, int ldy, int lane) {
+// p += (A_KL T_LJ)^T as two m16n8 accumulator fragments (p[nt] = columns
+// 8 nt .. 8 nt + 7 of the transpose).  tl -> 16 x 16 block T_LJ, ak -> A_KL,
+// both fp32 with row stride kSolveLd.  The transpose is what lets mma_tx use
+// the result as a B operand without leaving registers.
+__device__ __forceinline__ void mma_xt(float (&p)[2][4], const float *tl, const float *ak,
+                                       int lane) {
     const int g = lane >> 2, t = lane & 3;
+    constexpr int ld = kSolveLd;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        uint32_t a[4];
-        a[0] = to_tf32(xs[g * ldx + 8 * ks + t]);
-        a[1] = to_tf32(xs[(g + 8) * ldx + 8 * ks + t]);
-        a[2] = to_tf32(xs[g * ldx + 8 * ks + t + 4]);
-        a[3] = to_tf32(xs[(g + 8) * ldx + 8 * ks + t + 4]);
+        uint32_t a[4];  // A operand = T_LJ^T: element (m, k) = T_LJ[k][m]
+        a[0] = to_tf32(tl[(8 * ks + t) * ld + g]);
+        a[1] = to_tf32(tl[(8 * ks + t) * ld + g + 8]);
+        a[2] = to_tf32(tl[(8 * ks + t + 4) * ld + g]);
+        a[3] = to_tf32(tl[(8 * ks + t + 4) * ld + g + 8]);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 2; ++nt) {  // B operand = A_KL^T: (k, n) = A_KL[n][k]
             uint32_t b[2];
-            b[0] = to_tf32(ys[(8 * ks + t) * ldy + 8 * nt + g]);
-            b[1] = to_tf32(ys[(8 * ks + t + 4) * ldy + 8 * nt + g]);
-            mma_tf32_16x8x8(acc[nt], a, b);
+            b[0] = to_tf32(ak[(8 * nt + g) * ld + 8 * ks + t]);
+            b[1] = to_tf32(ak[(8 * nt + g) * ld + 8 * ks + t + 4]);
+            mma_tf32_16x8x8(p[nt], a, b);
         }
     }
 }
 
-// Store scale * acc (16 x 16 accumulator fragments) into a row-major block.
-__device__ __forceinline__ void store_block16(float *dst, int ld, const float (&acc)[2][4],
-                                              float scale, int lane) {
+// z += T_IK X_KJ with X_KJ^T held in the accumulator fragments p (from
+// mma_xt).  An accumulator fragment gives lane (g, t) the entries
+// X[8 ks + 2t][n] and X[8 ks + 2t + 1][n] for n = g and g + 8, which is a B
+// fragment once the eight k of each step are taken in the order 2t, 2t + 1
+// instead of t, t + 4; the A fragment of T_IK is loaded in that same order, so
+// the sum over k is unchanged.
+__device__ __forceinline__ void mma_tx(float (&z)[2][4], const float *tk, const float (&p)[2][4],
+                                       int lane) {
     const int g = lane >> 2, t = lane & 3;
+    constexpr int ld = kSolveLd;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        *reinterpret_cast<float2 *>(dst + g * ld + 8 * nt + 2 * t) =
-            make_float2(scale * acc[nt][0], scale * acc[nt][1]);
-        *reinterpret_cast<float2 *>(dst + (g + 8) * ld + 8 * nt + 2 * t) =
-            make_float2(scale * acc[nt][2], scale * acc[nt][3]);
+    for (int ks = 0; ks < 2; ++ks) {
+        const float2 r0 = *reinterpret_cast<const float2 *>(tk + g * ld + 8 * ks + 2 * t);
+        const float2 r1 = *reinterpret_cast<const float2 *>(tk + (g + 8) * ld + 8 * ks + 2 * t);
+        uint32_t a[4];
+        a[0] = to_tf32(r0.x);
+        a[1] = to_tf32(r1.x);
+        a[2] = to_tf32(r0.y);
+        a[3] = to_tf32(r1.y);
+#pragma unroll
+        for (int nz = 0; nz < 2; ++nz) {
+            uint32_t b[2];
+            b[0] = to_tf32(p[ks][2 * nz]);
+            b[1] = to_tf32(p[ks][2 * nz + 1]);
+            mma_tf32_16x8x8(z[nz], a, b);
+        }
     }
 }
 
-// Block (bi, bj) of T lives at row 16 bj, column 16 bi for bi >= bj (the
-// diagonal blocks in place, the lower blocks mirrored into the upper half).
-__device__ __forceinline__ const float *t_block(const float *as, int bi, int bj) {
+// Block (I, J) of T, I >= J: the diagonal blocks sit in place, a lower block
+// T_IJ in the upper-triangle slot (J, I), which A leaves free.
+__device__ __forceinline__ float *t_block(float *as, int bi, int bj) {
     return as + (16 * bj) * kSolveLd + 16 * bi;
+}
+__device__ __forceinline__ const float *a_block(const float *as, int bi, int bj) {
+    return as + (16 * bi) * kSolveLd + 16 * bj;
 }
 
 // Byte offset of bf16 element (row, col) of a 64 x 64 tile with 128-byte rows
@@ -86,100 +111,117 @@ __device__ __forceinline__ uint32_t tp_offset(int row, int col) {
     return (row >> 3) * 1024 + (row & 7) * 128 + ((((col >> 3) ^ row) & 7) << 4) + (col & 7) * 2;
 }
 
-// Optional second output of the inverse: T' = T diag(beta) in bf16, written
-// straight from the registers that produce T into a swizzled tile (the B
-// operand of the W and U~ products).
-struct TprimeOut {
-    uint8_t *tile;      // 64 x 64 bf16, 128-byte swizzle; nullptr: no second output
-    const float *beta;  // column scale, 64 values
-};
-
-// T = (I + A)^-1 in place in `as` (see the file comment), and T' when
-// `out.tile` is set.  `ys` is scratch for three 16 x kSolveYLd blocks.  Called
-// by 256 threads (8 warps) that all reach the named barrier `bar` (id)
-// between the stages.
-__device__ __forceinline__ void inverse_unit_lower64(float *as, float *ys, int pt, uint32_t bar,
-                                                     TprimeOut out = {nullptr, nullptr}) {
-    const int warp = pt >> 5, lane = pt & 31;
-    // diagonal 16 x 16 blocks: lane = column c of block b, forward substitution
-    if (pt < 64) {
-        const int b = pt >> 4, c = pt & 15;
-        float *Ab = as + (16 * b) * kSolveLd + 16 * b;
-        float x[16];
+// T'_IJ = -z diag(beta) (z from mma_tx) into the bf16 tile.
+__device__ __forceinline__ void store_tprime(uint8_t *tp, const float *beta, int bi, int bj,
+                                             const float (&z)[2][4], int lane) {
+    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = 0.f;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = r == c ? 1.f : 0.f;
-#pragma unroll
-            for (int i = 0; i < r; i += 4) {  // A is zero on and above the diagonal
-                const float4 a = *reinterpret_cast<const float4 *>(Ab + r * kSolveLd + i);
-                acc = fmaf(-a.x, x[i], acc);
-                acc = fmaf(-a.y, x[i + 1], acc);
-                acc = fmaf(-a.z, x[i + 2], acc);
-                acc = fmaf(-a.w, x[i + 3], acc);
-            }
-            x[r] = acc;
-        }
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Ab[r * kSolveLd + c] = x[r];
-        if (out.tile) {
-            const float bc = out.beta[16 * b + c];
-#pragma unroll
-            for (int r = 0; r < 16; ++r)
-                *reinterpret_cast<__nv_bfloat16 *>(out.tile + tp_offset(16 * b + r, 16 * b + c)) =
-                    __float2bfloat16_rn(x[r] * bc);
-        }
-    } else if (out.tile && pt < 64 + 96) {
-        // zero the six blocks above the diagonal of T' (16-byte pieces)
-        const int q = pt - 64, blk = q >> 4, piece = q & 15;  // 6 blocks x 16 rows
-        const int bi = blk < 3 ? 0 : blk < 5 ? 1 : 2;
-        const int bj = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
-        const int row = 16 * bi + piece;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-            *reinterpret_cast<uint4 *>(out.tile + tp_offset(row, 16 * bj + 8 * h)) =
-                make_uint4(0, 0, 0, 0);
-    }
-    sm100::named_bar_sync(bar, 256);
-    // off-diagonal blocks, one block per warp, diagonal d = 1, 2, 3
-#pragma unroll
-    for (int d = 1; d < 4; ++d) {
-        if (warp < 4 - d) {
-            const int bi = warp + d, bj = warp;
-            float *Y = ys + warp * 16 * kSolveYLd;
-            float acc[2][4] = {};
-            for (int k = bj; k < bi; ++k)  // Y = sum_k A_ik T_kj
-                mma_block16(acc, as + (16 * bi) * kSolveLd + 16 * k, kSolveLd,
-                            t_block(as, k, bj), kSolveLd, lane);
-            store_block16(Y, kSolveYLd, acc, 1.f, lane);
-            __syncwarp();
-            float tt[2][4] = {};
-            mma_block16(tt, t_block(as, bi, bi), kSolveLd, Y, kSolveYLd, lane);
-            store_block16(as + (16 * bj) * kSolveLd + 16 * bi, kSolveLd, tt, -1.f, lane);
-            if (out.tile) {  // T' block (bi, bj) = -tt scaled by beta along columns
-                const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int col = 16 * bj + 8 * nt + 2 * t;
-                    const float b0 = out.beta[col], b1 = out.beta[col + 1];
-                    *reinterpret_cast<uint32_t *>(out.tile + tp_offset(16 * bi + g, col)) =
-                        sm100::pack_bf16(-tt[nt][0] * b0, -tt[nt][1] * b1);
-                    *reinterpret_cast<uint32_t *>(out.tile + tp_offset(16 * bi + g + 8, col)) =
-                        sm100::pack_bf16(-tt[nt][2] * b0, -tt[nt][3] * b1);
-                }
-            }
-        }
-        sm100::named_bar_sync(bar, 256);
+    for (int nz = 0; nz < 2; ++nz) {
+        const int col = 16 * bj + 8 * nz + 2 * t;
+        const float b0 = beta[col], b1 = beta[col + 1];
+        *reinterpret_cast<uint32_t *>(tp + tp_offset(16 * bi + g, col)) =
+            sm100::pack_bf16(-z[nz][0] * b0, -z[nz][1] * b1);
+        *reinterpret_cast<uint32_t *>(tp + tp_offset(16 * bi + g + 8, col)) =
+            sm100::pack_bf16(-z[nz][2] * b0, -z[nz][3] * b1);
     }
 }
 
-// Entry (r, j) of T after inverse_unit_lower64.
-__device__ __forceinline__ float inv_entry(const float *as, int r, int j) {
-    if (j > r) return 0.f;
-    const int bi = r >> 4, bj = j >> 4;
-    return t_block(as, bi, bj)[(r & 15) * kSolveLd + (j & 15)];
+// On entry `as` (fp32, row stride kSolveLd) holds A, zero on and above the
+// diagonal, and beta[64] the token weights.  On exit `tp` holds T' (bf16,
+// [r][j], 128-byte swizzle) and `as` is scratch.  Called by the 256 threads
+// (pt = 0 .. 255) of eight warps: warps 0-3 compute and synchronise among
+// themselves on the named barrier `bar` (128 threads); warps 4-7 only zero
+// the upper blocks of T' and return.  The caller makes the tile visible to
+// the tensor cores (fence.proxy.async) and synchronises all 256 threads.
+__device__ __forceinline__ void solve_tprime64(float *as, const float *beta, uint8_t *tp, int pt,
+                                               uint32_t bar) {
+    constexpr int ld = kSolveLd;
+    const int warp = pt >> 5, lane = pt & 31;
+    if (warp >= 4) {
+        // zero the six blocks above the diagonal of T' (16-byte pieces)
+        const int q = pt - 128;
+        if (q < 96) {
+            const int blk = q >> 4, piece = q & 15;  // 6 blocks x 16 rows
+            const int bi = blk < 3 ? 0 : blk < 5 ? 1 : 2;
+            const int bj = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
+            const int row = 16 * bi + piece;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                *reinterpret_cast<uint4 *>(tp + tp_offset(row, 16 * bj + 8 * h)) =
+                    make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+    // 1. diagonal blocks: lane = column c of block b, substitution down the
+    //    rows, each row's sum taken over i = 0, 1, ... in order
+    if (pt < 64) {
+        const int b = pt >> 4, c = pt & 15;
+        float *Ab = as + (16 * b) * ld + 16 * b;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = r == c ? 1.f : 0.f;
+#pragma unroll
+        for (int i4 = 0; i4 < 16; i4 += 4) {
+            float4 a[16];  // A[r][i4 .. i4 + 3] for the rows still to update
+#pragma unroll
+            for (int r = i4 + 1; r < 16; ++r)
+                a[r] = *reinterpret_cast<const float4 *>(Ab + r * ld + i4);
+#pragma unroll
+            for (int i = i4; i < i4 + 4; ++i) {
+#pragma unroll
+                for (int r = i + 1; r < 16; ++r) {
+                    const float4 v = a[r];
+                    const float air = i - i4 == 0 ? v.x : i - i4 == 1 ? v.y : i - i4 == 2 ? v.z : v.w;
+                    x[r] = fmaf(-air, x[i], x[r]);
+                }
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Ab[r * ld + c] = x[r];
+        const float bc = beta[16 * b + c];
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            *reinterpret_cast<__nv_bfloat16 *>(tp + tp_offset(16 * b + r, 16 * b + c)) =
+                __float2bfloat16_rn(x[r] * bc);
+    }
+    sm100::named_bar_sync(bar, 128);
+    // 2. T_10 (warp 0) and T_32 (warp 1)
+    if (warp < 2) {
+        const int bi = 2 * warp + 1, bj = 2 * warp;
+        float p[2][4] = {}, z[2][4] = {};
+        mma_xt(p, t_block(as, bj, bj), a_block(as, bi, bj), lane);
+        mma_tx(z, t_block(as, bi, bi), p, lane);
+        const int g = lane >> 2, t = lane & 3;
+        float *dst = t_block(as, bi, bj);
+#pragma unroll
+        for (int nz = 0; nz < 2; ++nz) {
+            *reinterpret_cast<float2 *>(dst + g * ld + 8 * nz + 2 * t) =
+                make_float2(-z[nz][0], -z[nz][1]);
+            *reinterpret_cast<float2 *>(dst + (g + 8) * ld + 8 * nz + 2 * t) =
+                make_float2(-z[nz][2], -z[nz][3]);
+        }
+        store_tprime(tp, beta, bi, bj, z, lane);
+    }
+    sm100::named_bar_sync(bar, 128);
+    // 3. T_IJ, (I, J) = (2, 0), (2, 1), (3, 0), (3, 1) for warps 0 .. 3
+    {
+        const int bj = warp & 1, bi = 2 + (warp >> 1);
+        float p2[2][4] = {}, z[2][4] = {};
+        // X_2J = sum_{L = J}^{1} A_2L T_LJ
+        if (bj == 0) mma_xt(p2, t_block(as, 0, 0), a_block(as, 2, 0), lane);
+        mma_xt(p2, t_block(as, 1, bj), a_block(as, 2, 1), lane);
+        if (bi == 2) {
+            mma_tx(z, t_block(as, 2, 2), p2, lane);
+        } else {
+            float p3[2][4] = {};  // X_3J
+            if (bj == 0) mma_xt(p3, t_block(as, 0, 0), a_block(as, 3, 0), lane);
+            mma_xt(p3, t_block(as, 1, bj), a_block(as, 3, 1), lane);
+            mma_tx(z, t_block(as, 3, 2), p2, lane);
+            mma_tx(z, t_block(as, 3, 3), p3, lane);
+        }
+        store_tprime(tp, beta, bi, bj, z, lane);
+    }
 }
 
 }  // namespace kda
