@@ -35,10 +35,11 @@ sys.path.insert(0, ROOT)
 from linear_attention_recurrence_chunkwise_gb300 import inputs as I  # noqa: E402
 
 METRIC = "KDA prefill tokens/s and decode state GB/s (H=96,d=128) vs roofline"
-KERNEL_SOURCES = {
-    "prefill_tc": "linear_attention_recurrence_chunkwise_gb300/csrc/kda_prefill_tc.cu",
-    "prefill_simt": "linear_attention_recurrence_chunkwise_gb300/csrc/kda_prefill_simt.cu",
-    "decode": "linear_attention_recurrence_chunkwise_gb300/csrc/kda_decode.cu",
+_CSRC = "linear_attention_recurrence_chunkwise_gb300/csrc/"
+KERNEL_SOURCES = {  # every source file a kernel is compiled from
+    "prefill_tc": (_CSRC + "kda_prefill_tc.cu", _CSRC + "kda_solve.cuh", _CSRC + "kda_sm100.cuh"),
+    "prefill_simt": (_CSRC + "kda_prefill_simt.cu",),
+    "decode": (_CSRC + "kda_decode.cu",),
 }
 
 
@@ -55,9 +56,12 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
-def source_hash(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_hash(rels):
+    h = hashlib.sha256()
+    for rel in rels:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(kernel_key, workload):
