@@ -95,7 +95,7 @@ struct __align__(1024) TcSmem {
     uint8_t gt[32768];  // log_alpha tile: 4 boxes of 32 channels x 64 tokens (fp32, swizzled)
     float as[C * LDA];  // solve matrix / inverse blocks (fp32)
     uint64_t full[2], ready[2], gfull, tpfull;
-    uint64_t bar_r, bar_u, bar_s, bar_fin;
+    uint64_t bar_r, bar_u, bar_o, bar_s, bar_fin, tailfree[2];
     uint32_t tmem_base;
     int abort;
     int domain;
@@ -220,6 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&sm.bar_r), 1);
         mbar_init(smem_u32(&sm.bar_u), 1);
         mbar_init(smem_u32(&sm.bar_s), 1);
+        mbar_init(smem_u32(&sm.bar_o), 1);
+        mbar_init(smem_u32(&sm.tailfree[0]), 1);
+        mbar_init(smem_u32(&sm.tailfree[1]), 1);
         mbar_init(smem_u32(&sm.bar_fin), 2);
         mbar_init(smem_u32(&sm.gfull), 1);
         mbar_init(smem_u32(&sm.tpfull), 1);
@@ -353,6 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             wait_phase_warp(sm.full[s], (n >> 1) & 1, abort);
+            // Kb, M and gamma of chunk n - 2 (same slot) are no longer read by the carry
+            if (n >= 2) wait_phase_warp(sm.tailfree[s], ((n >> 1) - 1) & 1, abort);
             if (lane == 31)  // token 63 closes the chunk (lane 31 keeps it in slot 0)
 #pragma unroll
                 for (int e = 0; e < 16; ++e) S.gam[c0 + e] = exp2f(g[0][e]);
@@ -376,12 +381,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(S.v + offv) = make_uint4(0, 0, 0, 0);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float gf = ex2_approx(gr[e]);
-                    const float gi = ex2_approx(-gr[e]);
-                    kb[e] = kf[e] * gi;
-                    kf[e] *= gf;
-                    qf[e] *= gf;
+                for (int e = 0; e < 8; e += 2) {
+                    const float gf0 = ex2_approx(gr[e]), gf1 = ex2_approx(gr[e + 1]);
+                    const float gi0 = ex2_approx(-gr[e]), gi1 = ex2_approx(-gr[e + 1]);
+                    kb[e] = kf[e];
+                    kb[e + 1] = kf[e + 1];
+                    mul2(kb[e], kb[e + 1], gi0, gi1);
+                    mul2(kf[e], kf[e + 1], gf0, gf1);
+                    mul2(qf[e], qf[e + 1], gf0, gf1);
                 }
                 *reinterpret_cast<uint4 *>(S.kq + off) = pack8(kf);
                 *reinterpret_cast<uint4 *>(S.kq + off + 8192) = pack8(qf);
@@ -574,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         smem_u32(S.kq) + 8192 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
                     mma_bf16_tmem_a(tmem + kColO, tmem + kColSb + 8 * k, bq, id_o, k > 0);
                 }
+                mma_commit(smem_u32(&sm.bar_o));
             }
             __syncwarp();
             wait_phase_warp(sm.bar_u, n & 1, abort);
@@ -606,6 +614,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16(tmem + kColS, a, bk, id_s, 1);
                 }
                 mma_commit(smem_u32(&sm.bar_s));
+                // the U and O products (the last readers of the q / k / v tiles of
+                // this slot) are done: refill it with chunk n + 2 while the carry
+                // finishes chunk n
+                wait_phase(sm.bar_o, n & 1, abort);
+                if (n + 2 < nchunks) load_stage(n + 2);
             }
             __syncwarp();
             wait_phase_warp(sm.bar_s, n & 1, abort);
@@ -619,10 +632,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const float4 gq = gm[q];
-                    x[4 * q + 0] = __float_as_uint(__uint_as_float(x[4 * q + 0]) * gq.x);
-                    x[4 * q + 1] = __float_as_uint(__uint_as_float(x[4 * q + 1]) * gq.y);
-                    x[4 * q + 2] = __float_as_uint(__uint_as_float(x[4 * q + 2]) * gq.z);
-                    x[4 * q + 3] = __float_as_uint(__uint_as_float(x[4 * q + 3]) * gq.w);
+                    float a0 = __uint_as_float(x[4 * q + 0]), a1 = __uint_as_float(x[4 * q + 1]);
+                    float a2 = __uint_as_float(x[4 * q + 2]), a3 = __uint_as_float(x[4 * q + 3]);
+                    mul2(a0, a1, gq.x, gq.y);
+                    mul2(a2, a3, gq.z, gq.w);
+                    x[4 * q + 0] = __float_as_uint(a0);
+                    x[4 * q + 1] = __float_as_uint(a1);
+                    x[4 * q + 2] = __float_as_uint(a2);
+                    x[4 * q + 3] = __float_as_uint(a3);
                 }
                 tmem_st32(tmem + lane_addr + kColS + 32 * cb, x);
                 uint32_t w[16];
@@ -634,8 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             named_bar_sync(kBarCarry, kCarryThreads);
-            // stage s is no longer read by anyone: refill it with chunk n + 2
-            if (issuer && n + 2 < nchunks) load_stage(n + 2);
+            // Kb, M and gamma of this slot are no longer read: the chunk-local
+            // warps may write chunk n + 2's
+            if (issuer) mbar_arrive(smem_u32(&sm.tailfree[s]));
         }
         __syncwarp();
         store_output(nchunks - 1);

@@ -298,6 +298,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// (a0, a1) * (b0, b1) elementwise as one packed fp32 instruction (mul.f32x2,
+// round to nearest: the same results as two scalar multiplies).
+__device__ __forceinline__ void mul2(float &a0, float &a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 y, {%2, %3};\n\t"
+        "mul.rn.f32x2 z, x, y;\n\t"
+        "mov.b64 {%0, %1}, z;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
