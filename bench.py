@@ -128,13 +128,19 @@ class ClockSampler:
 
 
 def dist_setup(n_gpus):
+    """One process per GPU under torchrun (RANK / LOCAL_RANK / WORLD_SIZE from the
+    environment): NCCL on GPUs; gloo where no GPU is present (the host-side
+    multi-rank path, exercised by the CPU tests)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
@@ -147,10 +153,12 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The largest x over all ranks (the job's time is its slowest rank's)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
