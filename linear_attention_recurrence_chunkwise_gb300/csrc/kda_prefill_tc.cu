@@ -25,13 +25,13 @@
 //
 // Warp roles (384 threads, 3 warps per SM sub-partition, so up to 168
 // registers per thread):
-//   warps 0-7   chunk-local work of chunk n+1 (a1-a5): scaled operands, R,
-//               masks and the triangular solve, which writes T' in bf16 straight
-//               from its registers and so hands the chunk to the carry warps.
-//               The gate scan of the chunk after runs while R is on the tensor
-//               cores.  Warp 0 allocates tensor memory; one thread loads each
-//               chunk's log_alpha tile (TMA) as soon as the previous tile has
-//               been read.
+//   warps 0-7   chunk-local work of chunk n+1 (a1-a5): scaled operands, R and
+//               its masks (all eight warps); the triangular solve (warps 0-3),
+//               which writes T' in bf16 straight from its registers and so hands
+//               the chunk to the carry warps, while warps 4-7 scan the gates of
+//               the chunk after and park them in tensor memory.  Warp 0
+//               allocates tensor memory; one thread loads each chunk's
+//               log_alpha tile (TMA) as soon as the previous tile has been read.
 //   warps 8-11  the serial carry of chunk n (a6): the W / U~ MMAs, -W out of
 //               tensor memory into the operand tile, the U, O and S MMAs, the
 //               gamma scaling of the state, and the output, staged in shared
@@ -68,12 +68,13 @@ constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns (fp32 accumulators, 128 lanes each)
 constexpr uint32_t kColR = 0;     // R = [Kh; Qh] Kb^T        (64 columns)
 constexpr uint32_t kColW = 64;    // W^T                      (64)
-constexpr uint32_t kColU = 128;   // U~^T / U^T, two buffers (2 x 64)
+constexpr uint32_t kColU = 128;   // U~^T / U^T                (64)
+constexpr uint32_t kColG = 192;   // G2 of the next chunk, parked between scan and scaling (64)
 constexpr uint32_t kColO = 256;   // O^T                      (64)
 constexpr uint32_t kColSb = 320;  // S^T, bf16 pairs          (64): MMA A operand
 constexpr uint32_t kColS = 384;   // S^T master copy, fp32    (128)
 constexpr int LDA = kSolveLd;     // fp32 row stride of the solve matrix
-constexpr uint32_t kBarPrep = 1, kBarCarry = 2, kBarSolve = 3;  // named barrier ids
+constexpr uint32_t kBarPrep = 1, kBarCarry = 2, kBarSolve = 3, kBarScan = 4;  // named barrier ids
 constexpr uint32_t kTileBytes = 64 * 64 * 2;     // one TMA box
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLog2DecayLimit = kLogDecayLimit * kLog2e;
@@ -171,7 +172,7 @@ __device__ __forceinline__ void read_gates(const uint8_t *gt, int lane, int fl, 
 // for the 64 x 64 strictly lower A in sm.as, on the warp-level tensor cores
 // (kda_solve.cuh), written straight from the registers that produce it.
 __device__ __forceinline__ void solve_ut(TcSmem &sm, const float *bet, int pt) {
-    solve_tprime64(sm.as, bet, sm.tp, pt, kBarSolve);
+    solve_tprime64(sm.as, bet, sm.tp, pt, kBarSolve);  // warps 0-3
 }
 
 // Pack 16 fp32 values (as bits) into 8 bf16 pairs (even index in the low half).
@@ -285,23 +286,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pt = tid - 32 * kPrepWarp0;     // 0..255
         const int pw = pt >> 5;                   // prep warp 0..7
         const int half = pw >> 2;                 // which 32 of 64 TMEM columns
-        // gates and scaled operands: warp pw owns channels 16 pw .. 16 pw + 15, lane l
-        // tokens 2 l and 2 l + 1, so the prefix sum over tokens is one warp scan.
-        // Register slot i holds token 2 l + (i ^ fl): lanes 4-7 of each group of 8
-        // take the odd token first, so the 8 lanes of a shared-memory phase touch
-        // 8 different rows mod 8 -- 8 different 16-byte columns of the swizzled
-        // tiles, free of bank conflicts.
+        // Scaled operands: warp pw owns channels 16 pw .. 16 pw + 15; lane l holds
+        // tokens 2 l and 2 l + 1 of them.  Register slot i holds token
+        // 2 l + (i ^ fl): lanes 4-7 of each group of 8 take the odd token first, so
+        // the 8 lanes of a shared-memory phase touch 8 different rows mod 8 -- 8
+        // different 16-byte columns of the swizzled tiles, free of bank conflicts.
         const int fl = (lane >> 2) & 1;
         const int c0 = 16 * pw;
         const int slab = c0 >> 6, col = c0 & 63;
+        // Warps 4-7 scan the gates of the next chunk while warps 0-3 solve the
+        // current one.  The scan uses the same layout (so the prefix sum over
+        // tokens is one warp scan) for channel groups q and q + 4 (q = the warp's
+        // TMEM quadrant, pw & 3) and parks G2 in tensor memory: quadrant q,
+        // columns kColG (group q) and kColG + 32 (group q + 4).  Warp pw reads its
+        // own group back from column kColG + 32 (pw >> 2).
+        const bool scanner = pw >= 4;
+        const int bt = pt - 128;
+        const uint32_t gpark = tmem + lane_addr + kColG;
         bool domain_ok = true;
 
         // a1 for chunk m: log2-decay cumsum G2[t][c] = log2(e) sum_{t' <= t} log_alpha
-        // of this thread's two tokens and 16 channels, from the landed gate tile.
-        auto gate_scan = [&](int m, float (&g)[2][16]) {
+        // of this thread's two tokens and the 16 channels from cg, from the landed
+        // gate tile.
+        auto gate_scan = [&](int m, int cg, float (&g)[2][16]) {
             const int validm = min(C, len - m * C);
-            wait_phase_warp(sm.gfull, m & 1, abort);
-            read_gates(sm.gt, lane, fl, c0, g);
+            read_gates(sm.gt, lane, fl, cg, g);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const bool live = 2 * lane + (i ^ fl) < validm;  // the tile runs past the sequence end
@@ -331,11 +340,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (-lo > kLog2DecayLimit || hi > kLog2DecayLimit) domain_ok = false;
         };
+        // Warps 4-7: gates of chunk m scanned and parked; once every scanning
+        // thread has read the gate tile, it takes chunk m + 1.
+        auto scan_ahead = [&](int m) {
+            wait_phase_warp(sm.gfull, m & 1, abort);
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2) {  // channel groups q, then q + 4
+                float gm[2][16];
+                gate_scan(m, 16 * ((pw & 3) + 4 * h2), gm);
+                tmem_st32(gpark + 32 * h2, reinterpret_cast<const uint32_t(&)[32]>(gm));
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar_sync(kBarScan, 128);
+            if (bt == 96 && m + 1 < nchunks) load_gates(m + 1);
+        };
 
-        float gnx[2][16];  // G2 of the next chunk, scanned one chunk ahead
-        gate_scan(0, gnx);
-        named_bar_sync(kBarPrep, kPrepThreads);  // every thread has read tile 0
-        if (pt == 0 && nchunks > 1) load_gates(1);
+        if (scanner) scan_ahead(0);
         float bn = 0.f;  // beta of the next chunk, loaded one chunk ahead
         if (pt < C && pt < len) bn = p.beta[(size_t)(start + pt) * p.H + h];
 
@@ -344,11 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             TcStage &S = sm.st[s];
             const int64_t t0 = start + (int64_t)n * C;
             const int valid = min(C, len - n * C);
+            // G2 of chunk n, parked by warps 4-7 one step earlier
+            named_bar_sync(kBarPrep, kPrepThreads);
+            tc_fence_after();
             float g[2][16];
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int e = 0; e < 16; ++e) g[i][e] = gnx[i][e];
+            tmem_ld32(gpark + 32 * half, reinterpret_cast<uint32_t(&)[32]>(g));
             const float bet = bn;
             if (n + 1 < nchunks) {
                 const int valid1 = min(C, len - (n + 1) * C);
@@ -411,8 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(smem_u32(&sm.bar_r));
             }
-            // while R is computed: the gate scan of the next chunk
-            if (n + 1 < nchunks) gate_scan(n + 1, gnx);
             wait_phase_warp(sm.bar_r, n & 1, abort);
             tc_fence_after();
 #pragma unroll
@@ -447,15 +466,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (pt == 0 && n >= 1) wait_phase(sm.ready[s ^ 1], ((n - 1) >> 1) & 1, abort);
             tc_fence_before();
             named_bar_sync(kBarPrep, kPrepThreads);
-            // every thread has read the next chunk's gate tile: fetch the one after
-            // (from warp 7, which has no part in the first steps of the solve)
-            if (pt == 224 && n + 2 < nchunks) load_gates(n + 2);
 
-            // a4: T' = (I + A)^-1 diag(beta); the carry warps take it from here
-            solve_ut(sm, S.bet, pt);
-            fence_proxy_async_smem();
-            named_bar_sync(kBarPrep, kPrepThreads);
-            if (pt == 0) mbar_arrive(smem_u32(&sm.tpfull));
+            if (!scanner) {
+                // a4: T' = (I + A)^-1 diag(beta); the carry warps take it from here
+                solve_ut(sm, S.bet, pt);
+                fence_proxy_async_smem();
+                named_bar_sync(kBarSolve, 128);
+                if (pt == 0) mbar_arrive(smem_u32(&sm.tpfull));
+            } else if (n + 1 < nchunks) {
+                scan_ahead(n + 1);
+            }
         }
         if (!domain_ok) sm.domain = 1;
     } else {
@@ -538,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t av = desc_sw128(smem_u32(S.v) + k * 2048, 8192, 1024);
                     const uint64_t b = desc_sw128(smem_u32(sm.tp) + k * 32, 16, 1024);
                     mma_bf16(tmem + kColW, aw, b, id, k > 0);
-                    mma_bf16(tmem + kColU + 64 * s, av, b, id, k > 0);
+                    mma_bf16(tmem + kColU, av, b, id, k > 0);
                 }
                 mma_commit(smem_u32(&sm.ready[s]));
             }
@@ -566,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 8; ++k) {
                     const uint64_t bw =
                         desc_sw128(smem_u32(S.kq) + (k >> 2) * 16384 + (k & 3) * 2048, 8192, 1024);
-                    mma_bf16_tmem_a(tmem + kColU + 64 * s, tmem + kColSb + 8 * k, bw, id_u, 1);
+                    mma_bf16_tmem_a(tmem + kColU, tmem + kColSb + 8 * k, bw, id_u, 1);
                 }
                 mma_commit(smem_u32(&sm.bar_u));
             }
@@ -592,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t x[32];
-                tmem_ld32(tmem + lane_addr + kColU + 64 * s + 32 * cb, x);
+                tmem_ld32(tmem + lane_addr + kColU + 32 * cb, x);
                 float f[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(x[j]);

@@ -128,29 +128,25 @@ __device__ __forceinline__ void store_tprime(uint8_t *tp, const float *beta, int
 
 // On entry `as` (fp32, row stride kSolveLd) holds A, zero on and above the
 // diagonal, and beta[64] the token weights.  On exit `tp` holds T' (bf16,
-// [r][j], 128-byte swizzle) and `as` is scratch.  Called by the 256 threads
-// (pt = 0 .. 255) of eight warps: warps 0-3 compute and synchronise among
-// themselves on the named barrier `bar` (128 threads); warps 4-7 only zero
-// the upper blocks of T' and return.  The caller makes the tile visible to
-// the tensor cores (fence.proxy.async) and synchronises all 256 threads.
+// [r][j], 128-byte swizzle) and `as` is scratch.  Called by the 128 threads
+// (pt = 0 .. 127) of four warps, which synchronise among themselves on the
+// named barrier `bar`.  The caller makes the tile visible to the tensor cores
+// (fence.proxy.async) and synchronises the four warps.
 __device__ __forceinline__ void solve_tprime64(float *as, const float *beta, uint8_t *tp, int pt,
                                                uint32_t bar) {
     constexpr int ld = kSolveLd;
     const int warp = pt >> 5, lane = pt & 31;
-    if (warp >= 4) {
-        // zero the six blocks above the diagonal of T' (16-byte pieces)
-        const int q = pt - 128;
-        if (q < 96) {
-            const int blk = q >> 4, piece = q & 15;  // 6 blocks x 16 rows
-            const int bi = blk < 3 ? 0 : blk < 5 ? 1 : 2;
-            const int bj = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
-            const int row = 16 * bi + piece;
+    // zero the six blocks above the diagonal of T' (96 pieces: 16 rows x 16
+    // bytes of each block), from the threads that have no column in step 1
+    for (int q = pt - 64; q >= 0 && q < 96; q += 64) {
+        const int blk = q >> 4, piece = q & 15;
+        const int bi = blk < 3 ? 0 : blk < 5 ? 1 : 2;
+        const int bj = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
+        const int row = 16 * bi + piece;
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-                *reinterpret_cast<uint4 *>(tp + tp_offset(row, 16 * bj + 8 * h)) =
-                    make_uint4(0, 0, 0, 0);
-        }
-        return;
+        for (int h = 0; h < 2; ++h)
+            *reinterpret_cast<uint4 *>(tp + tp_offset(row, 16 * bj + 8 * h)) =
+                make_uint4(0, 0, 0, 0);
     }
     // 1. diagonal blocks: lane = column c of block b, substitution down the
     //    rows, each row's sum taken over i = 0, 1, ... in order
