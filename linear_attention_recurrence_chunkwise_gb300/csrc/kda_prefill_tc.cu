@@ -68,7 +68,7 @@ constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns (fp32 accumulators, 128 lanes each)
 constexpr uint32_t kColR = 0;     // R = [Kh; Qh] Kb^T        (64 columns)
 constexpr uint32_t kColW = 64;    // W^T                      (64)
-constexpr uint32_t kColU = 128;   // U~^T / U^T                (64)
+constexpr uint32_t kColU = 128;   // U~^T / U^T; later U^T in bf16 pairs (64)
 constexpr uint32_t kColG = 192;   // G2 of the next chunk, parked between scan and scaling (64)
 constexpr uint32_t kColO = 256;   // O^T                      (64)
 constexpr uint32_t kColSb = 320;  // S^T, bf16 pairs          (64): MMA A operand
@@ -434,31 +434,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             wait_phase_warp(sm.bar_r, n & 1, abort);
             tc_fence_after();
-#pragma unroll
-            for (int piece = 0; piece < 2; ++piece) {
-                const int j0 = 32 * half + 16 * piece;
-                uint32_t x[16];
-                tmem_ld16(tmem + lane_addr + kColR + j0, x);
+            {
+                const int j0 = 32 * half;
+                uint32_t x[32];
+                tmem_ld32(tmem + lane_addr + kColR + j0, x);
                 if (L < 64) {  // A[r][j] = beta_r R[r][j], j < r
                     const int r = L;
                     const float br = S.bet[r];
 #pragma unroll
-                    for (int j4 = 0; j4 < 4; ++j4) {
+                    for (int j4 = 0; j4 < 8; ++j4) {
                         const int j = j0 + 4 * j4;
-                        float4 w;
-                        w.x = j + 0 < r ? br * __uint_as_float(x[4 * j4 + 0]) : 0.f;
-                        w.y = j + 1 < r ? br * __uint_as_float(x[4 * j4 + 1]) : 0.f;
-                        w.z = j + 2 < r ? br * __uint_as_float(x[4 * j4 + 2]) : 0.f;
-                        w.w = j + 3 < r ? br * __uint_as_float(x[4 * j4 + 3]) : 0.f;
+                        float4 w = make_float4(__uint_as_float(x[4 * j4 + 0]), __uint_as_float(x[4 * j4 + 1]),
+                                               __uint_as_float(x[4 * j4 + 2]), __uint_as_float(x[4 * j4 + 3]));
+                        mul2(w.x, w.y, br, br);
+                        mul2(w.z, w.w, br, br);
+                        w.x = j + 0 < r ? w.x : 0.f;
+                        w.y = j + 1 < r ? w.y : 0.f;
+                        w.z = j + 2 < r ? w.z : 0.f;
+                        w.w = j + 3 < r ? w.w : 0.f;
                         *reinterpret_cast<float4 *>(&sm.as[r * LDA + j]) = w;
                     }
                 } else {  // M[r][j] = R[64 + r][j], j <= r
                     const int r = L - 64;
-                    float f[16];
+                    float f[32];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
+                    for (int j = 0; j < 32; ++j)
                         f[j] = j0 + j <= r ? __uint_as_float(x[j]) : 0.f;
-                    store_row<16>(S.m, r, j0, f);
+                    store_row<32>(S.m, r, j0, f);
                 }
             }
             // the previous chunk's W and U~ products (issued by the carry
@@ -608,17 +610,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (issuer) bulk_wait_group_read0();  // the previous output tile has left sm.ut
             named_bar_sync(kBarCarry, kCarryThreads);
             tc_fence_after();
-            // U^T (lane v, column j) -> bf16 operand [v][j]
+            // U^T (lane v, column j) -> bf16 pairs in tensor memory, over U^T itself:
+            // the A operand of the two products that follow
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t x[32];
                 tmem_ld32(tmem + lane_addr + kColU + 32 * cb, x);
-                float f[32];
+                uint32_t w[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(x[j]);
-                store_row<32>(sm.ut, v, 32 * cb, f);
+                for (int j = 0; j < 16; ++j)
+                    w[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+                tmem_st16(tmem + lane_addr + kColU + 16 * cb, w);
             }
-            fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             named_bar_sync(kBarCarry, kCarryThreads);
             if (issuer) {
@@ -627,11 +631,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t id_s = idesc_bf16(128, 128, false, true);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const uint64_t a = desc_sw128(smem_u32(sm.ut) + k * 32, 16, 1024);
+                    const uint32_t a = tmem + kColU + 8 * k;
                     const uint64_t bm = desc_sw128(smem_u32(S.m) + k * 32, 16, 1024);
                     const uint64_t bk = desc_sw128(smem_u32(S.kb) + k * 2048, 8192, 1024);
-                    mma_bf16(tmem + kColO, a, bm, id_o, 1);
-                    mma_bf16(tmem + kColS, a, bk, id_s, 1);
+                    mma_bf16_tmem_a(tmem + kColO, a, bm, id_o, 1);
+                    mma_bf16_tmem_a(tmem + kColS, a, bk, id_s, 1);
                 }
                 mma_commit(smem_u32(&sm.bar_s));
                 // the U and O products (the last readers of the q / k / v tiles of
