@@ -192,6 +192,46 @@ def test_bad_device_offsets_write_nothing(kda):
 
 # --------------------------------------------------------------- decode, small
 
+def _padded(shape, dtype, pad, fill):
+    """A contiguous view of `shape` inside a buffer with `pad` canary elements
+    on each side (pad keeps the view 16-byte aligned)."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * pad,), fill, dtype=dtype, device=DEV)
+    return buf, buf[pad:pad + n].view(shape)
+
+
+def _canaries_intact(buf, pad, fill):
+    head, tail = buf[:pad], buf[-pad:]
+    return bool((head == fill).all()) and bool((tail == fill).all())
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_no_writes_outside_outputs(kda, engine):
+    """Ragged varlen tails, a single-token sequence and an empty one: o and S_T
+    live inside canary-filled buffers, which must come back untouched, and the
+    results must still match the oracle."""
+    lengths = [1, 0, 65, 130, 7, 200]
+    prob = I.prefill_problem(1, 0, 2, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=31,
+                             device=DEV, lengths=lengths)
+    pad, fill = 1024, -768.0  # exact in bf16 and fp32
+    obuf, o = _padded(tuple(prob.v.shape), prob.v.dtype, pad, fill)
+    sbuf, ST = _padded(tuple(prob.S0.shape), torch.float32, pad, fill)
+    kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0, prob.cu_seqlens,
+                o=o, S_T=ST, engine=engine)
+    torch.cuda.synchronize()
+    assert _canaries_intact(obuf, pad, fill) and _canaries_intact(sbuf, pad, fill)
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1])
+    assert rel_err(o, o_ref) < 2e-2
+    assert rel_err(ST, S_ref) < 1e-2
+    # decode on the returned states, in place, with a canary-padded output
+    x = I.decode_token(len(lengths), 2, 128, 128, "bf16", (-0.1, -0.0005), seed=3, step=0,
+                       device=DEV)
+    dbuf, od = _padded((len(lengths), 2, 128), torch.bfloat16, pad, fill)
+    kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], ST, o=od)
+    torch.cuda.synchronize()
+    assert _canaries_intact(dbuf, pad, fill) and _canaries_intact(sbuf, pad, fill)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 def test_decode_small(kda, dtype, d):
