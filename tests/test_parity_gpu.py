@@ -192,6 +192,25 @@ def test_bad_device_offsets_write_nothing(kda):
 
 # --------------------------------------------------------------- decode, small
 
+@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("N", [8192, 8500])
+def test_many_short_sequences(kda, engine, N):
+    """N packed sequences of 0-130 tokens: 8192 is the largest count that gets
+    the longest-first launch order, 8500 runs in the given order.  Every
+    sequence of one head follows the oracle."""
+    pattern = [0, 1, 2, 7, 63, 64, 65, 130]
+    lengths = [pattern[(i * 5 + i // 8) % len(pattern)] for i in range(N)]
+    prob = I.prefill_problem(1, 0, 2, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=N,
+                             device=DEV, lengths=lengths)
+    ws = torch.zeros(kda.kda_fwd_workspace_bytes(N), dtype=torch.uint8, device=DEV)
+    o, ST = run_fwd(kda, prob, engine, workspace=ws)
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK
+    o_ref, S_ref = oracle_on_heads(prob, [1])
+    idx = torch.tensor([1], device=DEV)
+    assert rel_err(o.index_select(1, idx), o_ref) < 2e-2
+    assert rel_err(ST.index_select(1, idx), S_ref) < 1e-2
+
+
 def _padded(shape, dtype, pad, fill):
     """A contiguous view of `shape` inside a buffer with `pad` canary elements
     on each side (pad keeps the view 16-byte aligned)."""
