@@ -10,8 +10,10 @@
 // S_t, memory_output) with the read folded into the same pass over the state.
 //
 // Memory layout of S is [N, H, d_v, d_k]: row v holds the d_k key channels of
-// value channel v contiguously.  One 128-thread block owns one (session, head);
-// each warp walks rows v four at a time, 8 lanes per row, every lane holding
+// value channel v contiguously.  The grid holds as many 128-thread blocks as fit
+// on the GPU at once, each walking (session, head) pairs with a stride of the
+// grid size (no partly filled last wave); for one pair the block
+// walks rows v four at a time per warp, 8 lanes per row, every lane holding
 // d/8 key channels (c = 32 i + 4 l + e), so one warp load instruction moves
 // four fully used 128-byte segments.  The two k-axis reductions (r_v and the
 // query read) are 3-step shuffles among the 8 lanes of a row.
@@ -34,18 +36,18 @@ template <int D, typename Tin>
 __global__ void __launch_bounds__(128) decode_step_kernel(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
     const float *__restrict__ log_alpha, const float *__restrict__ beta,
-    float *__restrict__ S, Tin *__restrict__ o) {
+    float *__restrict__ S, Tin *__restrict__ o, int NH) {
     constexpr int kLanesPerRow = 8;
     constexpr int kPerLane = D / kLanesPerRow;  // key channels per lane
     constexpr int kVec = kPerLane / 4;          // float4 per lane per row
     constexpr int kRowsPerWarp = D / 4;
 
-    const int p = blockIdx.x;  // (session, head) pair
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int sub = lane >> 3;  // row within the group of four
     const int l8 = lane & 7;
 
+  for (int p = blockIdx.x; p < NH; p += gridDim.x) {  // (session, head) pairs
     const size_t vec = (size_t)p * D;
     float kk[kPerLane], qq[kPerLane], aa[kPerLane];
     float kq = 0.f;
@@ -103,14 +105,33 @@ __global__ void __launch_bounds__(128) decode_step_kernel(
         }
         if (l8 == 0) o[vec + row] = from_f<Tin>(fmaf(u, kq, rq));
     }
+  }
 }
 
 template <int D, typename Tin>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *la,
                          const float *beta, float *S, int NH, void *o, cudaStream_t s) {
-    decode_step_kernel<D, Tin><<<NH, 128, 0, s>>>(
+    // resident blocks on the whole GPU, looked up once per device (every thread
+    // that races here computes the same value)
+    constexpr int kMaxDevices = 64;
+    static int resident[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (resident[dev] == 0) {
+        int sms = 0, per = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_step_kernel<D, Tin>,
+                                                              128, 0);
+        if (e != cudaSuccess) return e;
+        resident[dev] = sms * (per > 0 ? per : 1);
+    }
+    const int grid = NH < resident[dev] ? NH : resident[dev];
+    decode_step_kernel<D, Tin><<<grid, 128, 0, s>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k),
-        static_cast<const Tin *>(v), la, beta, S, static_cast<Tin *>(o));
+        static_cast<const Tin *>(v), la, beta, S, static_cast<Tin *>(o), NH);
     return cudaGetLastError();
 }
 
