@@ -57,7 +57,9 @@ typedef enum {
     KDA_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
     KDA_ERR_CUDA = 4,             /* a CUDA call or kernel launch failed */
     KDA_ERR_DOMAIN = 5,           /* device status: input outside the supported domain */
-    KDA_ERR_TIMEOUT = 6           /* device status: a kernel wait gave up (not expected) */
+    KDA_ERR_TIMEOUT = 6,          /* device status: a kernel wait gave up (not expected) */
+    KDA_ERR_BOUNDS = 7            /* device status, bounds-checked build only: an index
+                                     outside its tensor was found and the access skipped */
 } kda_status_t;
 
 typedef enum {

@@ -39,6 +39,7 @@ const char *kda_status_string(kda_status_t s) {
         case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
         case KDA_ERR_DOMAIN: return "KDA_ERR_DOMAIN";
+        case KDA_ERR_BOUNDS: return "KDA_ERR_BOUNDS";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
     }
     return "KDA_ERR_UNKNOWN";

@@ -44,6 +44,24 @@ __device__ __forceinline__ void raise_status(int32_t *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// The bounds-checked build (KDA_BOUNDS_CHECK=1, the stand-in for a memory
+// sanitizer) checks each computed global index against its tensor's extent
+// before the access; a failure records KDA_ERR_BOUNDS and the access is
+// skipped.  In the normal build the check compiles away.
+#ifndef KDA_BOUNDS_CHECK
+#define KDA_BOUNDS_CHECK 0
+#endif
+__device__ __forceinline__ bool in_bounds(int32_t *status, size_t idx, size_t n) {
+#if KDA_BOUNDS_CHECK
+    if (idx < n) return true;
+    raise_status(status, KDA_ERR_BOUNDS);
+    return false;
+#else
+    (void)status, (void)idx, (void)n;
+    return true;
+#endif
+}
+
 cudaError_t launch_schedule(const FwdParams &p, cudaStream_t s);
 cudaError_t launch_prefill_simt(const FwdParams &p, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_prefill_tc(const FwdParams &p, cudaStream_t s);

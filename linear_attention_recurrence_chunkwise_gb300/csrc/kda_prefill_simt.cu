@@ -86,11 +86,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(FwdParams p) 
     const Tin *v = static_cast<const Tin *>(p.v);
     Tin *o = static_cast<Tin *>(p.o);
     const size_t state_off = ((size_t)n * p.H + h) * D * D;
+    const size_t n_state = (size_t)p.N * p.H * D * D;  // extents, for the bounds checks
+    const size_t n_tok = (size_t)p.Ttot * p.H * D, n_beta = (size_t)p.Ttot * p.H;
 
     // initial state: memory [v][c] -> logical S[c][v]
     for (int idx = tid; idx < D * D; idx += kThreads) {
         const int vv = idx / D, c = idx % D;
-        sm.S[c * LD + vv] = p.S0 ? p.S0[state_off + idx] : 0.f;
+        sm.S[c * LD + vv] =
+            p.S0 && in_bounds(p.status, state_off + idx, n_state) ? p.S0[state_off + idx] : 0.f;
     }
 
     const int nchunks = (len + C - 1) / C;
@@ -103,14 +106,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(FwdParams p) 
         // ---- phase 1a: load the chunk (identity tokens past the end)
         for (int idx = tid; idx < C * D; idx += kThreads) {
             const int r = idx / D, c = idx % D;
-            const bool ok = r < valid;
             const size_t gi = ((size_t)(t0 + r) * p.H + h) * D + c;
+            const bool ok = r < valid && in_bounds(p.status, gi, n_tok);
             sm.Qh[r * LD + c] = ok ? to_f(q[gi]) : 0.f;
             sm.Kh[r * LD + c] = ok ? to_f(k[gi]) : 0.f;
             sm.Vb[r * LD + c] = ok ? to_f(v[gi]) : 0.f;
             sm.Kb[r * LD + c] = ok ? p.log_alpha[gi] : 0.f;
         }
-        if (tid < C) sm.bet[tid] = tid < valid ? p.beta[(size_t)(t0 + tid) * p.H + h] : 0.f;
+        if (tid < C) {
+            const size_t bi = (size_t)(t0 + tid) * p.H + h;
+            sm.bet[tid] = tid < valid && in_bounds(p.status, bi, n_beta) ? p.beta[bi] : 0.f;
+        }
         __syncthreads();
 
         // ---- phase 1b: cumulative log-decay per key channel, scaled operands
@@ -242,7 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(FwdParams p) 
             if (r < valid) {
                 const size_t go = ((size_t)(t0 + r) * p.H + h) * D;
 #pragma unroll
-                for (int j = 0; j < NJ; ++j) o[go + tx + 16 * j] = from_f<Tin>(acc_o[i][j]);
+                for (int j = 0; j < NJ; ++j)
+                    if (in_bounds(p.status, go + tx + 16 * j, n_tok))
+                        o[go + tx + 16 * j] = from_f<Tin>(acc_o[i][j]);
             }
         }
 
@@ -282,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(FwdParams p) 
     if (p.S_T) {
         for (int idx = tid; idx < D * D; idx += kThreads) {
             const int vv = idx / D, c = idx % D;
-            p.S_T[state_off + idx] = sm.S[c * LD + vv];
+            if (in_bounds(p.status, state_off + idx, n_state))
+                p.S_T[state_off + idx] = sm.S[c * LD + vv];
         }
     }
 }

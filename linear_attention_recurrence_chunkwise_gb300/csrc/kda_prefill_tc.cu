@@ -203,10 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     seq_range(p, nseq, start, len);
     const int nchunks = (len + C - 1) / C;
     const size_t state_off = ((size_t)nseq * p.H + h) * D * D;
+    const size_t n_state = (size_t)p.N * p.H * D * D;  // extents, for the bounds checks
+    const size_t n_tok = (size_t)p.Ttot * p.H * D, n_beta = (size_t)p.Ttot * p.H;
     if (nchunks == 0) {  // empty sequence: the state passes through
         if (p.S_T)
             for (int i = tid; i < D * D; i += kThreads)
-                p.S_T[state_off + i] = p.S0 ? p.S0[state_off + i] : 0.f;
+                if (in_bounds(p.status, state_off + i, n_state))
+                    p.S_T[state_off + i] = p.S0 ? p.S0[state_off + i] : 0.f;
         return;
     }
 
@@ -358,7 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (scanner) scan_ahead(0);
         float bn = 0.f;  // beta of the next chunk, loaded one chunk ahead
-        if (pt < C && pt < len) bn = p.beta[(size_t)(start + pt) * p.H + h];
+        if (pt < C && pt < len && in_bounds(p.status, (size_t)(start + pt) * p.H + h, n_beta))
+            bn = p.beta[(size_t)(start + pt) * p.H + h];
 
         for (int n = 0; n < nchunks; ++n) {
             const int s = n & 1;
@@ -373,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float bet = bn;
             if (n + 1 < nchunks) {
                 const int valid1 = min(C, len - (n + 1) * C);
-                bn = (pt < C && pt < valid1) ? p.beta[(size_t)(t0 + C + pt) * p.H + h] : 0.f;
+                const size_t bi = (size_t)(t0 + C + pt) * p.H + h;
+                bn = (pt < C && pt < valid1 && in_bounds(p.status, bi, n_beta)) ? p.beta[bi] : 0.f;
             }
 
             wait_phase_warp(sm.full[s], (n >> 1) & 1, abort);
@@ -486,7 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool issuer = et == 0;
         const int v = L;
         {  // initial state: row v of S0 ([v][c] memory) -> TMEM fp32 and bf16 operand
-            const float *src = p.S0 ? p.S0 + state_off + (size_t)v * D : nullptr;
+            const float *src =
+                p.S0 && in_bounds(p.status, state_off + (size_t)v * D + D - 1, n_state)
+                    ? p.S0 + state_off + (size_t)v * D
+                    : nullptr;
 #pragma unroll
             for (int cb = 0; cb < 8; ++cb) {
                 uint32_t u[16];
@@ -539,8 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int r = idx >> 4, ch = idx & 15;  // 16 pieces of 8 channels per row
                     const uint4 val = *reinterpret_cast<const uint4 *>(
                         sm.ut + (ch >> 3) * 8192 + sw128_offset(r, (ch & 7) * 8));
-                    *reinterpret_cast<uint4 *>(o + ((size_t)(t0 + r) * p.H + h) * D + 8 * ch) =
-                        val;
+                    const size_t oi = ((size_t)(t0 + r) * p.H + h) * D + 8 * ch;
+                    if (in_bounds(p.status, oi + 7, n_tok))
+                        *reinterpret_cast<uint4 *>(o + oi) = val;
                 }
             }
         };
@@ -683,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         store_output(nchunks - 1);
         if (issuer) bulk_wait_group0();
         __syncwarp();
-        if (p.S_T) {
+        if (p.S_T && in_bounds(p.status, state_off + (size_t)v * D + D - 1, n_state)) {
             float *dst = p.S_T + state_off + (size_t)v * D;
 #pragma unroll
             for (int cb = 0; cb < 8; ++cb) {

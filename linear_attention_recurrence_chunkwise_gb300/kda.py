@@ -23,6 +23,7 @@ KDA_ERR_WORKSPACE = 3
 KDA_ERR_CUDA = 4
 KDA_ERR_DOMAIN = 5
 KDA_ERR_TIMEOUT = 6
+KDA_ERR_BOUNDS = 7
 
 KDA_F32, KDA_BF16 = 0, 1
 ENGINES = {"auto": 0, "tensorcore": 1, "cudacore": 2}
@@ -52,27 +53,34 @@ def load() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"libkda.so not built at {LIB_PATH}; run "
                                "linear_attention_recurrence_chunkwise_gb300.build.build()")
-        lib = ctypes.CDLL(LIB_PATH)
-        vp, sz, ci, fp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p
-        lib.kda_fwd_workspace_bytes.restype = sz
-        lib.kda_fwd_workspace_bytes.argtypes = [ci]
-        fwd_args = [vp, vp, vp, fp, fp, fp, vp, ci, ci, ci, ci, ci, ci, ci, vp, fp, vp, sz, vp]
-        lib.kda_fwd.restype = ci
-        lib.kda_fwd.argtypes = fwd_args
-        lib.kda_fwd_engine.restype = ci
-        lib.kda_fwd_engine.argtypes = fwd_args + [ci]
-        lib.kda_fwd_noalloc.restype = ci
-        lib.kda_fwd_noalloc.argtypes = fwd_args[:16] + [vp, vp]
-        lib.kda_decode_step.restype = ci
-        lib.kda_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, ci, ci, ci, ci, ci, vp, vp]
-        lib.kda_read_device_status.restype = ci
-        lib.kda_read_device_status.argtypes = [vp, sz, vp]
-        lib.kda_state_bytes.restype = sz
-        lib.kda_state_bytes.argtypes = [ci] * 6
-        lib.kda_status_string.restype = ctypes.c_char_p
-        lib.kda_status_string.argtypes = [ci]
-        _lib = lib
-        return lib
+        _lib = load_library(LIB_PATH)
+        return _lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """Open a build of libkda at `path` (for instance the bounds-checked
+    libkda_bounds.so) with the entry points' signatures; pass it as `lib=` to
+    the functions below."""
+    lib = ctypes.CDLL(path)
+    vp, sz, ci, fp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p
+    lib.kda_fwd_workspace_bytes.restype = sz
+    lib.kda_fwd_workspace_bytes.argtypes = [ci]
+    fwd_args = [vp, vp, vp, fp, fp, fp, vp, ci, ci, ci, ci, ci, ci, ci, vp, fp, vp, sz, vp]
+    lib.kda_fwd.restype = ci
+    lib.kda_fwd.argtypes = fwd_args
+    lib.kda_fwd_engine.restype = ci
+    lib.kda_fwd_engine.argtypes = fwd_args + [ci]
+    lib.kda_fwd_noalloc.restype = ci
+    lib.kda_fwd_noalloc.argtypes = fwd_args[:16] + [vp, vp]
+    lib.kda_decode_step.restype = ci
+    lib.kda_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, ci, ci, ci, ci, ci, vp, vp]
+    lib.kda_read_device_status.restype = ci
+    lib.kda_read_device_status.argtypes = [vp, sz, vp]
+    lib.kda_state_bytes.restype = sz
+    lib.kda_state_bytes.argtypes = [ci] * 6
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_status_string.argtypes = [ci]
+    return lib
 
 
 def kda_status_string(status: int) -> str:
@@ -121,13 +129,15 @@ def _check(t, name, dtype=None, device=None):
 
 
 def kda_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, o=None, S_T=None,
-            workspace=None, return_state: bool = True, engine: str = "auto", stream=None):
+            workspace=None, return_state: bool = True, engine: str = "auto", stream=None,
+            lib=None):
     """Chunkwise KDA forward (prefill).
 
     q, k, log_alpha [B, T, H, d_k] or packed [Ttot, H, d_k]; v [.., H, d_v];
     beta [.., H]; S0 [N, H, d_v, d_k] fp32 or None; cu_seqlens int32 [N+1]
     (device) or None.  Returns (o, S_T) (S_T None when return_state is False).
     Output tensors and the workspace are allocated with torch unless given.
+    `lib` selects another build of the library (see load_library).
     """
     dev = q.device
     dt = q.dtype
@@ -160,10 +170,11 @@ def kda_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, o=None, S_T=N
     if S_T is None and return_state:
         S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=dev)
     _check(S_T, "S_T", torch.float32, dev)
+    lib = lib or load()
     if workspace is None:
-        workspace = torch.empty(kda_fwd_workspace_bytes(N), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(int(lib.kda_fwd_workspace_bytes(N)), dtype=torch.uint8,
+                                device=dev)
     _check(workspace, "workspace", None, dev)
-    lib = load()
     rc = lib.kda_fwd_engine(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                             _ptr(S0), _ptr(cu_seqlens), B, T, H, d_k, d_v, N,
                             _dtype_code(dt), _ptr(o), _ptr(S_T), _ptr(workspace),
@@ -242,9 +253,9 @@ def kda_decode_step(q, k, v, log_alpha, beta, S, *, o=None, stream=None):
     return o
 
 
-def kda_read_device_status(workspace, stream=None) -> int:
+def kda_read_device_status(workspace, stream=None, lib=None) -> int:
     """Synchronise the stream and return the status word left by kda_fwd."""
-    rc = load().kda_read_device_status(_ptr(workspace),
+    rc = (lib or load()).kda_read_device_status(_ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        _stream(stream))
     return int(rc)

@@ -57,7 +57,7 @@ def test_state_bytes_edge_cases(kda):
 def test_status_strings(kda):
     for code, name in [(0, "KDA_OK"), (1, "KDA_ERR_INVALID_ARGUMENT"), (2, "KDA_ERR_UNSUPPORTED"),
                        (3, "KDA_ERR_WORKSPACE"), (4, "KDA_ERR_CUDA"), (5, "KDA_ERR_DOMAIN"),
-                       (6, "KDA_ERR_TIMEOUT")]:
+                       (6, "KDA_ERR_TIMEOUT"), (7, "KDA_ERR_BOUNDS")]:
         assert kda.kda_status_string(code) == name
 
 
@@ -136,3 +136,14 @@ def test_binding_rejects_cpu_tensors(kda):
     x = torch.zeros(1, 64, 2, 64)
     with pytest.raises(ValueError):
         kda.kda_fwd(x, x, x, x, torch.zeros(1, 64, 2))
+
+
+def test_bounds_checked_build_exports_every_symbol():
+    """The bounds-checked variant compiles (nvcc cross-compiles without a GPU)
+    and exports the same entry points."""
+    import ctypes
+    from linear_attention_recurrence_chunkwise_gb300 import build as kbuild
+    from linear_attention_recurrence_chunkwise_gb300 import kda as mod
+    lib = ctypes.CDLL(kbuild.build(bounds_check=True))
+    for name in mod.EXPORTED:
+        assert hasattr(lib, name), name

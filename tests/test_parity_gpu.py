@@ -211,6 +211,27 @@ def test_many_short_sequences(kda, engine, N):
     assert rel_err(ST.index_select(1, idx), S_ref) < 1e-2
 
 
+@pytest.mark.parametrize("engine", ENGINES)
+def test_bounds_checked_build(kda, engine):
+    """The bounds-checked build (every computed global index checked against its
+    tensor's extent, KDA_ERR_BOUNDS on a miss) runs fixed-length, ragged and
+    empty sequences without a report and with results that match the oracle."""
+    lib = kda.load_library(kbuild.build(bounds_check=True))
+    cases = [I.prefill_problem(2, T, 2, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=T,
+                               device=DEV) for T in (1, 65, 333)]
+    cases.append(I.prefill_problem(1, 0, 2, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=5,
+                                   device=DEV, lengths=[0, 130, 1, 64, 0, 7]))
+    for prob in cases:
+        n = prob.S0.shape[0]
+        ws = torch.zeros(int(lib.kda_fwd_workspace_bytes(n)), dtype=torch.uint8, device=DEV)
+        o, ST = kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0,
+                            prob.cu_seqlens, workspace=ws, engine=engine, lib=lib)
+        assert kda.kda_read_device_status(ws, lib=lib) == kda.KDA_OK
+        o_ref, S_ref = oracle_on_heads(prob, [0, 1])
+        assert rel_err(o, o_ref) < 2e-2
+        assert rel_err(ST, S_ref) < 1e-2
+
+
 def _padded(shape, dtype, pad, fill):
     """A contiguous view of `shape` inside a buffer with `pad` canary elements
     on each side (pad keeps the view 16-byte aligned)."""
