@@ -173,6 +173,35 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
                              int N, int H, int d_k, int d_v, kda_dtype_t dtype,
                              void *o, void *stream);
 
+/*
+ * Speculative-decode verification and commit ("Kimi K3 深度拆解" section 9.2:
+ * the draft tokens' projected inputs are kept instead of a copy of the state
+ * per draft position; after verification the accepted tokens are replayed on
+ * chip and the resulting state is written back).  K draft tokens per session,
+ * 1 <= K <= KDA_MAX_DRAFT_TOKENS:
+ *
+ *   q, k       [N, K, H, d_k] dtype      v, o  [N, K, H, d_v] dtype
+ *   log_alpha  [N, K, H, d_k] fp32       beta  [N, K, H]      fp32
+ *   S          [N, H, d_v, d_k] fp32
+ *
+ * kda_verify_tokens: o receives the outputs of the K tokens run in order from
+ * S (token t sees the state after tokens 0 .. t); S is read once and not
+ * written.  kda_commit_tokens: applies tokens 0 .. n_accept[n] - 1 of session
+ * n to S in place (n_accept: device int32 [N], values clamped to [0, K];
+ * NULL applies all K); S is read and written once.  Both give the same
+ * numbers as the same tokens passed one at a time to kda_decode_step.
+ * Alignment as for kda_decode_step; n_accept 4-byte aligned.  No workspace.
+ */
+#define KDA_MAX_DRAFT_TOKENS 16
+kda_status_t kda_verify_tokens(const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta, const float *S,
+                               int N, int K, int H, int d_k, int d_v, kda_dtype_t dtype,
+                               void *o, void *stream);
+kda_status_t kda_commit_tokens(const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta, float *S,
+                               const int32_t *n_accept, int N, int K, int H, int d_k, int d_v,
+                               kda_dtype_t dtype, void *stream);
+
 /* Synchronise `stream`, read the status word kda_fwd left in `workspace` and
  * return it (KDA_OK if no condition was raised).  KDA_ERR_CUDA if the copy or
  * the synchronisation fails. */

@@ -150,6 +150,51 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+static kda_status_t check_draft_args(const void *q, const void *k, const void *v,
+                                     const float *log_alpha, const float *beta, const float *S,
+                                     int N, int K, int H, int d_k, int d_v, kda_dtype_t dtype) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (N < 0 || H <= 0 || d_k <= 0 || d_v <= 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (K < 1 || K > KDA_MAX_DRAFT_TOKENS) return KDA_ERR_INVALID_ARGUMENT;
+    if (!supported_dims(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)N * K * H > INT32_MAX) return KDA_ERR_INVALID_ARGUMENT;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !S) return KDA_ERR_INVALID_ARGUMENT;
+    const unsigned elem = dtype == KDA_BF16 ? 2u : 4u;
+    if (!aligned(q, elem) || !aligned(k, elem) || !aligned(v, elem) || !aligned(log_alpha, 4) ||
+        !aligned(beta, 4) || !aligned16(S))
+        return KDA_ERR_INVALID_ARGUMENT;
+    return KDA_OK;
+}
+
+kda_status_t kda_verify_tokens(const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta, const float *S,
+                               int N, int K, int H, int d_k, int d_v, kda_dtype_t dtype,
+                               void *o, void *stream) {
+    const kda_status_t st = check_draft_args(q, k, v, log_alpha, beta, S, N, K, H, d_k, d_v,
+                                             dtype);
+    if (st != KDA_OK || N == 0) return st;
+    if (!o || !aligned(o, dtype == KDA_BF16 ? 2u : 4u)) return KDA_ERR_INVALID_ARGUMENT;
+    if (fault_injected()) return KDA_ERR_CUDA;
+    const cudaError_t e = kda::launch_verify(q, k, v, log_alpha, beta, S, N, K, H, d_k, dtype,
+                                             o, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_commit_tokens(const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta, float *S,
+                               const int32_t *n_accept, int N, int K, int H, int d_k, int d_v,
+                               kda_dtype_t dtype, void *stream) {
+    const kda_status_t st = check_draft_args(q, k, v, log_alpha, beta, S, N, K, H, d_k, d_v,
+                                             dtype);
+    if (st != KDA_OK || N == 0) return st;
+    if (n_accept && !aligned(n_accept, 4)) return KDA_ERR_INVALID_ARGUMENT;
+    if (fault_injected()) return KDA_ERR_CUDA;
+    const cudaError_t e = kda::launch_commit(q, k, v, log_alpha, beta, S, n_accept, N, K, H,
+                                             d_k, dtype, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status_t kda_read_device_status(const void *workspace, size_t workspace_bytes,
                                     void *stream) {
     if (!workspace || workspace_bytes < 4) return KDA_ERR_WORKSPACE;

@@ -66,6 +66,12 @@ cudaError_t launch_schedule(const FwdParams &p, cudaStream_t s);
 cudaError_t launch_prefill_simt(const FwdParams &p, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_prefill_tc(const FwdParams &p, cudaStream_t s);
 bool prefill_tc_supported(kda_dtype_t dt, int dk, int dv);
+cudaError_t launch_verify(const void *q, const void *k, const void *v, const float *log_alpha,
+                          const float *beta, const float *S, int N, int K, int H, int d,
+                          kda_dtype_t dt, void *o, cudaStream_t s);
+cudaError_t launch_commit(const void *q, const void *k, const void *v, const float *log_alpha,
+                          const float *beta, float *S, const int32_t *n_accept, int N, int K,
+                          int H, int d, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_decode(const void *q, const void *k, const void *v,
                           const float *log_alpha, const float *beta, float *S, int N,
                           int H, int d, kda_dtype_t dt, void *o, cudaStream_t s);

@@ -30,9 +30,10 @@ ENGINES = {"auto": 0, "tensorcore": 1, "cudacore": 2}
 
 # every symbol include/kda.h declares
 EXPORTED = ["kda_fwd_workspace_bytes", "kda_fwd", "kda_fwd_engine", "kda_fwd_noalloc",
-            "kda_decode_step", "kda_read_device_status", "kda_state_bytes",
-            "kda_status_string"]
+            "kda_decode_step", "kda_verify_tokens", "kda_commit_tokens",
+            "kda_read_device_status", "kda_state_bytes", "kda_status_string"]
 KDA_NOALLOC_MAX_SEQS = 16384
+KDA_MAX_DRAFT_TOKENS = 16
 
 _lock = threading.Lock()
 _lib = None
@@ -74,6 +75,10 @@ def load_library(path: str) -> ctypes.CDLL:
     lib.kda_fwd_noalloc.argtypes = fwd_args[:16] + [vp, vp]
     lib.kda_decode_step.restype = ci
     lib.kda_decode_step.argtypes = [vp, vp, vp, fp, fp, fp, ci, ci, ci, ci, ci, vp, vp]
+    lib.kda_verify_tokens.restype = ci
+    lib.kda_verify_tokens.argtypes = [vp, vp, vp, fp, fp, fp, ci, ci, ci, ci, ci, ci, vp, vp]
+    lib.kda_commit_tokens.restype = ci
+    lib.kda_commit_tokens.argtypes = [vp, vp, vp, fp, fp, fp, vp, ci, ci, ci, ci, ci, ci, vp]
     lib.kda_read_device_status.restype = ci
     lib.kda_read_device_status.argtypes = [vp, sz, vp]
     lib.kda_state_bytes.restype = sz
@@ -251,6 +256,55 @@ def kda_decode_step(q, k, v, log_alpha, beta, S, *, o=None, stream=None):
     if rc != KDA_OK:
         raise KdaError(rc, "kda_decode_step")
     return o
+
+
+def _check_draft(q, k, v, log_alpha, beta, S):
+    dev, dt = q.device, q.dtype
+    _check(q, "q", dt), _check(k, "k", dt, dev), _check(v, "v", dt, dev)
+    _check(log_alpha, "log_alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    _check(S, "S", torch.float32, dev)
+    if q.dim() != 4:
+        raise ValueError("draft tokens are [N, K, H, d]")
+    N, K, H, d_k = q.shape
+    d_v = v.shape[-1]
+    if k.shape != q.shape or log_alpha.shape != q.shape or v.shape[:-1] != q.shape[:-1] \
+            or beta.shape != q.shape[:-1]:
+        raise ValueError("q, k, v, log_alpha, beta shapes disagree")
+    if S.shape != (N, H, d_v, d_k):
+        raise ValueError(f"S must be [N, H, d_v, d_k] = {(N, H, d_v, d_k)}")
+    return N, K, H, d_k, d_v
+
+
+def kda_verify_tokens(q, k, v, log_alpha, beta, S, *, o=None, stream=None):
+    """Outputs of K draft tokens per session run in order from the committed
+    state S, which is left unchanged.  q, k, log_alpha [N, K, H, d_k]; v
+    [N, K, H, d_v]; beta [N, K, H].  Returns o [N, K, H, d_v]."""
+    N, K, H, d_k, d_v = _check_draft(q, k, v, log_alpha, beta, S)
+    if o is None:
+        o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
+    _check(o, "o", q.dtype, q.device)
+    rc = load().kda_verify_tokens(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                  _ptr(S), N, K, H, d_k, d_v, _dtype_code(q.dtype), _ptr(o),
+                                  _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_verify_tokens")
+    return o
+
+
+def kda_commit_tokens(q, k, v, log_alpha, beta, S, n_accept=None, *, stream=None):
+    """Apply the first n_accept[n] of session n's K draft tokens to S in place
+    (n_accept: device int32 [N], clamped to [0, K]; None applies all K)."""
+    N, K, H, d_k, d_v = _check_draft(q, k, v, log_alpha, beta, S)
+    _check(n_accept, "n_accept", torch.int32, q.device)
+    if n_accept is not None and n_accept.shape != (N,):
+        raise ValueError("n_accept must be [N]")
+    rc = load().kda_commit_tokens(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                  _ptr(S), _ptr(n_accept), N, K, H, d_k, d_v,
+                                  _dtype_code(q.dtype), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_commit_tokens")
+    return S
 
 
 def kda_read_device_status(workspace, stream=None, lib=None) -> int:

@@ -24,6 +24,11 @@ Contents
     beta_i and the S_0 term; both are restored here, since unrolling the
     recurrence S_t = A_t S_{t-1} + beta_t k_t v_t^T produces them).
 
+``verify_tokens`` / ``commit_tokens``
+    Speculative-decode verification and commit over K cached draft tokens
+    ("Kimi K3 深度拆解" section 9.2), written out as K (or n_accept[n]) calls of
+    ``decode_step``; no arithmetic of their own.
+
 Parity status of every function is pinned by ``tests/test_oracle_pins.py``.
 """
 from __future__ import annotations
@@ -165,6 +170,37 @@ def decode_step(q, k, v, log_alpha, beta, S):
     if rc != 0:
         raise ValueError("kda_oracle_decode_step rejected its arguments")
     return o, S
+
+
+def verify_tokens(q, k, v, log_alpha, beta, S):
+    """Speculative-decode verification ("Kimi K3 深度拆解" section 9.2): the
+    outputs of K draft tokens per session run in order from S, which is not
+    changed.  q, k, log_alpha [N, K, H, dk]; v [N, K, H, dv]; beta [N, K, H];
+    S [N, H, dv, dk].  The definition written out: K decode steps on a copy of
+    S.  Returns o [N, K, H, dv]."""
+    q, k, v, g, b = (_f64(x) for x in (q, k, v, log_alpha, beta))
+    St = _f64(S)
+    N, K = q.shape[:2]
+    o = np.zeros(v.shape, dtype=np.float64)
+    for t in range(K):
+        o[:, t], St = decode_step(q[:, t], k[:, t], v[:, t], g[:, t], b[:, t], St)
+    return o
+
+
+def commit_tokens(q, k, v, log_alpha, beta, S, n_accept=None):
+    """The first n_accept[n] draft tokens of session n applied to S (all K when
+    n_accept is None): that many decode steps, session by session.  Returns
+    the new state [N, H, dv, dk]; the inputs are not modified."""
+    q, k, v, g, b = (_f64(x) for x in (q, k, v, log_alpha, beta))
+    S = _f64(S).copy()
+    N, K = q.shape[:2]
+    acc = [K] * N if n_accept is None else \
+        [min(max(int(a), 0), K) for a in np.asarray(_f64(n_accept)).reshape(-1)]
+    for n in range(N):
+        for t in range(acc[n]):
+            _, S[n:n + 1] = decode_step(q[n:n + 1, t], k[n:n + 1, t], v[n:n + 1, t],
+                                        g[n:n + 1, t], b[n:n + 1, t], S[n:n + 1])
+    return S
 
 
 def bruteforce(q, k, v, log_alpha, beta, S0=None):

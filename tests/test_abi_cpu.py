@@ -121,6 +121,35 @@ def test_decode_argument_errors(kda):
     assert call(N=0, S=None) == 0  # nothing to do
 
 
+def test_draft_token_argument_errors(kda):
+    """kda_verify_tokens / kda_commit_tokens reject bad arguments before any
+    launch (fake device addresses are never dereferenced)."""
+    lib = kda.load()
+
+    def verify(**kw):
+        a = dict(q=P[0], k=P[1], v=P[2], la=P[3], beta=P[4], S=P[5], N=4, K=3, H=2, dk=128,
+                 dv=128, dt=1, o=P[6], stream=None)
+        a.update(kw)
+        return lib.kda_verify_tokens(a["q"], a["k"], a["v"], a["la"], a["beta"], a["S"], a["N"],
+                                     a["K"], a["H"], a["dk"], a["dv"], a["dt"], a["o"],
+                                     a["stream"])
+
+    def commit(**kw):
+        a = dict(q=P[0], k=P[1], v=P[2], la=P[3], beta=P[4], S=P[5], acc=None, N=4, K=3, H=2,
+                 dk=128, dv=128, dt=1, stream=None)
+        a.update(kw)
+        return lib.kda_commit_tokens(a["q"], a["k"], a["v"], a["la"], a["beta"], a["S"],
+                                     a["acc"], a["N"], a["K"], a["H"], a["dk"], a["dv"], a["dt"],
+                                     a["stream"])
+    assert verify(K=0) == 1 and verify(K=kda.KDA_MAX_DRAFT_TOKENS + 1) == 1
+    assert verify(o=None) == 1 and verify(S=ctypes.c_void_p(0x10008)) == 1
+    assert verify(dk=32, dv=32) == 2 and verify(dt=5) == 1
+    assert verify(N=0, S=None, o=None) == 0                        # nothing to do
+    assert commit(acc=ctypes.c_void_p(0x10002)) == 1               # n_accept needs 4 B
+    assert commit(q=None) == 1 and commit(N=-1) == 1
+    assert commit(N=0, S=None) == 0
+
+
 def test_failure_injection_reports_cuda_error(kda, monkeypatch):
     """The host-only injection hook turns a valid call into KDA_ERR_CUDA
     without enqueueing anything."""

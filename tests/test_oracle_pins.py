@@ -187,3 +187,33 @@ def test_rejects_bad_arguments():
         oracle.fwd(q, k, v, g, b, S0, np.array([0, 7, 6]))      # decreasing offsets
     with pytest.raises(ValueError):
         oracle.fwd(q, k, v, g, b, S0, np.array([0, 3, 5]))      # does not cover all tokens
+
+
+def test_verify_and_commit_compose_like_a_prefill():
+    """The draft-token verify/commit helpers against the prefill recurrence on
+    the same tokens: verify's outputs are the prefill outputs of the K tokens
+    from S, commit(all) is the prefill's final state, commit(0) leaves S, and
+    committing a tokens equals a prefill over those a tokens."""
+    rng = np.random.default_rng(11)
+    N, K, H, d = 3, 5, 2, 8
+    q = rng.standard_normal((N, K, H, d)); q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = rng.standard_normal((N, K, H, d)); k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((N, K, H, d))
+    g = rng.uniform(-0.5, -0.01, (N, K, H, d))
+    b = rng.uniform(0.1, 0.9, (N, K, H))
+    S = rng.standard_normal((N, H, d, d)) * 0.1
+    o = oracle.verify_tokens(q, k, v, g, b, S)
+    o_ref, S_ref = oracle.fwd(q, k, v, g, b, S)          # [B=N, T=K, H, d] prefill form
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.commit_tokens(q, k, v, g, b, S), S_ref, rtol=1e-12,
+                               atol=1e-12)
+    np.testing.assert_array_equal(oracle.commit_tokens(q, k, v, g, b, S, [0, 0, 0]), S)
+    acc = [2, 0, 5]
+    Sc = oracle.commit_tokens(q, k, v, g, b, S, acc)
+    for n, a in enumerate(acc):
+        if a:
+            _, Sa = oracle.fwd(q[n:n + 1, :a], k[n:n + 1, :a], v[n:n + 1, :a], g[n:n + 1, :a],
+                               b[n:n + 1, :a], S[n:n + 1])
+            np.testing.assert_allclose(Sc[n:n + 1], Sa, rtol=1e-12, atol=1e-12)
+        else:
+            np.testing.assert_array_equal(Sc[n], S[n])

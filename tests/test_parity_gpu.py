@@ -232,6 +232,42 @@ def test_bounds_checked_build(kda, engine):
         assert rel_err(ST, S_ref) < 1e-2
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("K", [1, 4, 16])
+def test_verify_and_commit_draft_tokens(kda, dtype, d, K):
+    """Speculative-decode verify / commit over K cached draft tokens: outputs
+    and states against the oracle, S untouched by verify, per-session accepted
+    counts (clamped to [0, K]), and the same numbers as K single-token steps."""
+    N, H = 5, 3
+    toks = [I.decode_token(N, H, d, d, dtype, seed=K, step=t, device=DEV) for t in range(K)]
+    q, k, v, la, b = (torch.stack([x[key] for x in toks], dim=1).contiguous()
+                      for key in ("q", "k", "v", "log_alpha", "beta"))
+    S = I.decode_state(N, H, d, d, 0.02, seed=K, device=DEV)
+    S0 = S.clone()
+    o = kda.kda_verify_tokens(q, k, v, la, b, S)
+    torch.cuda.synchronize()
+    assert torch.equal(S, S0)
+    assert rel_err(o, oracle.verify_tokens(q, k, v, la, b, S0)) < tol_o(q.dtype)
+    Sd, od = S0.clone(), []
+    for t in range(K):
+        od.append(kda.kda_decode_step(q[:, t].contiguous(), k[:, t].contiguous(),
+                                      v[:, t].contiguous(), la[:, t].contiguous(),
+                                      b[:, t].contiguous(), Sd))
+    torch.cuda.synchronize()
+    assert torch.equal(o, torch.stack(od, dim=1))
+    acc = torch.tensor([0, K, 1, K // 2, K + 3], dtype=torch.int32, device=DEV)
+    kda.kda_commit_tokens(q, k, v, la, b, S, n_accept=acc)
+    torch.cuda.synchronize()
+    S_ref = oracle.commit_tokens(q, k, v, la, b, S0, acc.cpu().numpy())
+    assert rel_err(S, S_ref) < (1e-4 if dtype == "f32" else 1e-2)
+    assert torch.equal(S[0], S0[0])
+    S_all = S0.clone()
+    kda.kda_commit_tokens(q, k, v, la, b, S_all)
+    torch.cuda.synchronize()
+    assert torch.equal(S_all, Sd)
+
+
 def _padded(shape, dtype, pad, fill):
     """A contiguous view of `shape` inside a buffer with `pad` canary elements
     on each side (pad keeps the view 16-byte aligned)."""
