@@ -4,7 +4,9 @@ Default workload (the headline): chunkwise prefill, B=1, H=96, T=8192,
 d_k=d_v=128, bf16 q/k/v, fp32 log_alpha/beta, fp32 state, S0 = 0 -- metric
 tokens/s.  The same JSON line carries a ``decode`` object: one decode step for
 64 sessions x 96 heads (fp32 state [64, 96, 128, 128], 403 MB, in place) --
-metric state-GB/s = 2 * state bytes / step time.
+metric state-GB/s = 2 * state bytes / step time -- and a ``draft`` object:
+speculative decode on the same state, verify 8 draft tokens then commit them
+(kda_verify_tokens + kda_commit_tokens), metric draft tokens/s.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload prefill|decode|long|varlen]
@@ -40,6 +42,7 @@ KERNEL_SOURCES = {  # every source file a kernel is compiled from
     "prefill_tc": (_CSRC + "kda_prefill_tc.cu", _CSRC + "kda_solve.cuh", _CSRC + "kda_sm100.cuh"),
     "prefill_simt": (_CSRC + "kda_prefill_simt.cu",),
     "decode": (_CSRC + "kda_decode.cu",),
+    "multitoken": (_CSRC + "kda_multitoken.cu",),
 }
 
 
@@ -323,8 +326,11 @@ def run_ours(args, world, rank):
         line["e2e"] = e2e_prefill(kda, w, max(2, min(args.steps, 5)), stream, world)
         if args.workload == "prefill" and not args.no_decode:
             line["decode"] = decode_sub(kda, args, stream, pk)
+            line["draft"] = draft_sub(kda, args, stream, pk, line["decode"]["us_per_step"])
     else:
         line["e2e"] = e2e_decode(kda, w, max(2, min(args.steps, 20)), stream, world)
+        if not args.no_decode:
+            line["draft"] = draft_sub(kda, args, stream, pk, ms_step * 1e3)
     if rank == 0 and world == 1 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(w, args)
     return line
@@ -360,6 +366,55 @@ def decode_sub(kda, args, stream, pk):
                          "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
                          "traffic": traffic_for("decode", "decode"),
                          "algorithmic_bytes_per_launch": alg}}
+
+
+def draft_sub(kda, args, stream, pk, decode_us):
+    """Speculative decode on the decode state: verify K draft tokens (outputs,
+    state read once and kept), then commit all K (state read and written once;
+    every session accepting everything is the commit's slowest case)."""
+    p = I.PRESETS["draft"]
+    N, K, H, d = p["N"], p["K"], p["H"], p["d"]
+    S = I.decode_state(N, H, d, d, p["s0_std"], args.seed, "cuda")
+    x = I.draft_tokens(N, K, H, d, d, p["dtype"], p["la"], args.seed + 1, "cuda")
+    ins = (x["q"], x["k"], x["v"], x["log_alpha"], x["beta"])
+    o = torch.empty_like(x["v"])
+    acc = torch.full((N,), K, dtype=torch.int32, device="cuda")
+    reps = 30
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            kda.kda_verify_tokens(*ins, S, o=o, stream=stream)
+            kda.kda_commit_tokens(*ins, S, n_accept=acc, stream=stream)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for e in ev:
+            e[0].record(stream)
+            kda.kda_verify_tokens(*ins, S, o=o, stream=stream)
+            e[1].record(stream)
+            kda.kda_commit_tokens(*ins, S, n_accept=acc, stream=stream)
+            e[2].record(stream)
+    stream.synchronize()
+    ver_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    com_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    alg_v = nbytes(S, *ins, o)
+    alg_c = 2 * nbytes(S) + nbytes(x["k"], x["v"], x["log_alpha"], x["beta"], acc)
+
+    def roof(alg, ms):
+        gbs = alg / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                "frac": round(gbs / pk["hbm"], 4), "traffic": None,
+                "algorithmic_bytes_per_launch": alg, "avg_launch_us": round(ms * 1e3, 2)}
+    rv, rc = roof(alg_v, ver_ms), roof(alg_c, com_ms)
+    rv["traffic"] = traffic_for("multitoken", "verify")
+    rc["traffic"] = traffic_for("multitoken", "commit")
+    spec_us = (ver_ms + com_ms) * 1e3
+    return {"metric": "draft tokens/s (verify + commit)",
+            "value": round(N * K / (spec_us / 1e6), 1), "unit": "tokens/s",
+            "workload": f"verify K={K} draft tokens then commit all, N={N} H={H} d={d} "
+                        f"{p['dtype']} fp32 state (in place)",
+            "us_per_verify_commit": round(spec_us, 2),
+            "us_for_K_decode_steps": round(K * decode_us, 2),
+            "verify": rv, "commit": rc, "reps": reps}
 
 
 def e2e_prefill(kda, w, steps, stream, world):
@@ -514,7 +569,7 @@ def main():
                     default="prefill")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode sub-benchmark")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode and draft sub-benchmarks")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

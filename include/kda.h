@@ -188,8 +188,10 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
  * S (token t sees the state after tokens 0 .. t); S is read once and not
  * written.  kda_commit_tokens: applies tokens 0 .. n_accept[n] - 1 of session
  * n to S in place (n_accept: device int32 [N], values clamped to [0, K];
- * NULL applies all K); S is read and written once.  Both give the same
- * numbers as the same tokens passed one at a time to kda_decode_step.
+ * NULL applies all K); S is read and written once.  Both agree with the same
+ * tokens passed one at a time to kda_decode_step up to fp32 rounding (the
+ * tokens are taken in closed form over sub-blocks of 8, which sums in another
+ * order).
  * Alignment as for kda_decode_step; n_accept 4-byte aligned.  No workspace.
  */
 #define KDA_MAX_DRAFT_TOKENS 16

@@ -41,6 +41,9 @@ PRESETS = {
     "varlen": dict(n_seq=16, H=96, d=128, dtype="bf16", la=(-0.5, -0.001), s0_std=0.02,
                    len_lo=1024, len_hi=65536, decode_steps=256),
     "decode": dict(N=64, H=96, d=128, dtype="bf16", la=(-0.1, -0.0005), s0_std=0.02, steps=1000),
+    # speculative decode on the decode state: the last verified token plus a
+    # 7-token draft (the draft depth the K3 MTP layer is unrolled to)
+    "draft": dict(N=64, H=96, d=128, dtype="bf16", la=(-0.1, -0.0005), s0_std=0.02, K=8),
 }
 
 DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -139,6 +142,16 @@ def decode_token(N: int, H: int, dk: int, dv: int, dtype="bf16", la=(-0.1, -0.00
     beta = torch.sigmoid(torch.randn((N, H), generator=gen, device=device,
                                      dtype=torch.float32))
     return dict(q=q, k=k, v=v, log_alpha=log_alpha, beta=beta)
+
+
+def draft_tokens(N: int, K: int, H: int, dk: int, dv: int, dtype="bf16",
+                 la=(-0.1, -0.0005), seed: int = 0, device="cpu"):
+    """K consecutive decode tokens per session, stacked on dim 1: q, k, log_alpha
+    [N, K, H, dk], v [N, K, H, dv], beta [N, K, H] (contiguous).  Token t is
+    decode_token(..., step=t)."""
+    toks = [decode_token(N, H, dk, dv, dtype, la, seed, t, device) for t in range(K)]
+    return {key: torch.stack([x[key] for x in toks], dim=1).contiguous()
+            for key in ("q", "k", "v", "log_alpha", "beta")}
 
 
 def decode_state(N: int, H: int, dk: int, dv: int, std=0.02, seed: int = 0, device="cpu"):
