@@ -56,7 +56,8 @@ typedef enum {
     KDA_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. d_k != d_v) */
     KDA_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
     KDA_ERR_CUDA = 4,             /* a CUDA call or kernel launch failed */
-    KDA_ERR_DOMAIN = 5,           /* device status: input outside the supported domain */
+    KDA_ERR_DOMAIN = 5,           /* reserved: no entry point of this version raises it
+                                     (every finite gate is supported) */
     KDA_ERR_TIMEOUT = 6,          /* device status: a kernel wait gave up (not expected) */
     KDA_ERR_BOUNDS = 7            /* device status, bounds-checked build only: an index
                                      outside its tensor was found and the access skipped */
@@ -101,10 +102,16 @@ size_t kda_fwd_workspace_bytes(int N);
  *   workspace  device memory of at least kda_fwd_workspace_bytes(N) bytes,
  *              16-byte aligned; its contents on entry do not matter.
  *
- * Device status (kda_read_device_status): KDA_ERR_DOMAIN when, within some
- * 64-token chunk, the cumulative log-decay of a channel leaves [-80, 80]
- * (the chunk form scales keys by exp(-G) and would overflow fp32 there); the
- * outputs of that head are then undefined.  KDA_ERR_INVALID_ARGUMENT when the
+ * Gate domain: any finite log_alpha <= 0.  The chunk form scales keys by
+ * exp(-G), G the in-chunk cumulative log-decay, which overflows fp32 once |G|
+ * passes 80 -- reachable under K3's per-token bound of -5 ("Kimi K3 的 KDA"
+ * section 6: -320 over 64 tokens).  Such chunks are computed token by token
+ * with the recurrence itself on CUDA cores, in fp32: by the CUDA-core engine
+ * chunk by chunk, by the tensor-core engine for the whole (sequence, head)
+ * that contains one (from S0, after its chunk pass; S_T may still alias S0).
+ * The results are exact to fp32 rounding either way; only the time differs.
+ *
+ * Device status (kda_read_device_status): KDA_ERR_INVALID_ARGUMENT when the
  * device-side cu_seqlens is not non-decreasing or does not end at Ttot; no
  * output is written then.  KDA_ERR_TIMEOUT if a wait inside the tensor-core
  * kernel exceeded its time limit (outputs undefined; the kernel still exits

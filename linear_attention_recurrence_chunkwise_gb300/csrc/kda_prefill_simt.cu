@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
+#include "kda_serial.cuh"
 
 namespace kda {
 namespace {
@@ -97,7 +98,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(FwdParams p) 
     }
 
     const int nchunks = (len + C - 1) / C;
-    bool domain_ok = true;
     for (int ch = 0; ch < nchunks; ++ch) {
         const int64_t t0 = start + (int64_t)ch * C;
         const int valid = min(C, len - ch * C);
@@ -119,13 +119,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(FwdParams p) 
         }
         __syncthreads();
 
+        // ---- a chunk whose cumulative log-decay leaves [-80, 80] in some
+        // channel is taken token by token (exp(-G) would overflow fp32)
+        bool wide = false;
+        if (tid < D) {
+            float G = 0.f;
+            for (int r = 0; r < C; ++r) {
+                G += sm.Kb[r * LD + tid];
+                wide |= !(fabsf(G) <= kLogDecayLimit);
+            }
+        }
+        if (__syncthreads_or(wide)) {
+            for (int idx = tid; idx < valid * D; idx += kThreads) {
+                const int r = idx / D, c = idx % D;
+                sm.Kb[r * LD + c] = expf(sm.Kb[r * LD + c]);  // alpha
+            }
+            constexpr int CP = Serial<D>::kCP;
+            const int vcol = tid % D, c0 = (tid / D) * CP;
+            float st[CP];
+#pragma unroll
+            for (int i = 0; i < CP; ++i) st[i] = sm.S[(c0 + i) * LD + vcol];
+            __syncthreads();
+            // column sums in the (free) solve matrix: red_r then red_o
+            serial_tokens<D, false, false>(st, sm.Kh, sm.Qh, sm.Kb, sm.Vb, sm.bet, LD, valid,
+                                           sm.A, sm.A + 2 * Serial<D>::kParts * D, o,
+                                           ((size_t)t0 * p.H + h) * D, (size_t)p.H * D, n_tok,
+                                           p.status, 1);
+#pragma unroll
+            for (int i = 0; i < CP; ++i) sm.S[(c0 + i) * LD + vcol] = st[i];
+            continue;
+        }
+
         // ---- phase 1b: cumulative log-decay per key channel, scaled operands
         if (tid < D) {
             const int c = tid;
             float G = 0.f;
             for (int r = 0; r < C; ++r) {
                 G += sm.Kb[r * LD + c];
-                if (fabsf(G) > kLogDecayLimit) domain_ok = false;
                 const float gf = expf(G), gi = expf(-G);
                 const float kv = sm.Kh[r * LD + c];
                 sm.Qh[r * LD + c] *= gf;
@@ -285,7 +315,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(FwdParams p) 
             }
         }
     }
-    if (!domain_ok) raise_status(p.status, KDA_ERR_DOMAIN);
     __syncthreads();
     if (p.S_T) {
         for (int idx = tid; idx < D * D; idx += kThreads) {

@@ -52,6 +52,7 @@
 
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
+#include "kda_serial.cuh"
 #include "kda_solve.cuh"
 
 namespace kda {
@@ -181,8 +182,96 @@ __device__ __forceinline__ void pack16(const uint32_t (&u)[16], uint32_t (&w)[8]
     for (int j = 0; j < 8; ++j) w[j] = pack_bf16(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1]));
 }
 
+// Token-serial pass over a whole (sequence, head), from S0: the fallback for a
+// head with a chunk whose cumulative log-decay leaves [-80, 80] (kda_serial.cuh).
+// Runs after teardown, over the block's shared memory: 64 tokens at a time are
+// staged as fp32 by all 384 threads, threads 0-255 step through them with the
+// state in registers, then all threads add the parts' output sums and store o.
+// The chunk pass stored all its outputs (bulk wait, proxy fence) before the
+// block barrier that precedes this, and they are overwritten here.
+struct SerialStage {
+    float k[C][D], q[C][D], a[C][D], v[C][D];
+    float bet[C];
+    float red_r[2 * Serial<D>::kParts * D];
+    float red_o[C * Serial<D>::kParts * D];
+};
+
+__device__ __forceinline__ void serial_head(const FwdParams *pp, uint8_t *smem_raw,
+                                         int64_t start, int len, int h, size_t state_off) {
+    const FwdParams &p = *pp;
+    SerialStage &ss = *reinterpret_cast<SerialStage *>(
+        smem_raw + ((16u - (smem_u32(smem_raw) & 15u)) & 15u));
+    constexpr int CP = Serial<D>::kCP, P = Serial<D>::kParts;
+    const int tid = threadIdx.x, vcol = tid % D, c0 = (tid / D) * CP;
+    const bool stepper = tid < Serial<D>::kThreads;
+    const size_t n_state = (size_t)p.N * p.H * D * D;
+    const size_t n_tok = (size_t)p.Ttot * p.H * D, n_beta = (size_t)p.Ttot * p.H;
+    const uint4 *q = static_cast<const uint4 *>(p.q);  // 8 bf16 per load; rows start on 16 bytes
+    const uint4 *k = static_cast<const uint4 *>(p.k);
+    const uint4 *v = static_cast<const uint4 *>(p.v);
+    const float4 *la = reinterpret_cast<const float4 *>(p.log_alpha);
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+    // S[c0 + i][v] lives at memory [v][c0 + i]
+    float st[CP];
+    const size_t srow = state_off + (size_t)vcol * D + c0;
+#pragma unroll
+    for (int i = 0; i < CP; ++i)
+        st[i] = stepper && p.S0 && in_bounds(p.status, srow + i, n_state) ? p.S0[srow + i] : 0.f;
+    for (int t0 = 0; t0 < len; t0 += C) {
+        const int nt = min(C, len - t0);
+        const size_t row0 = ((size_t)(start + t0) * p.H + h) * D;  // element index of token t0
+        __syncthreads();  // the previous tokens' stage and output sums are read
+        for (int idx = tid; idx < nt * (D / 8); idx += kThreads) {
+            const int r = idx / (D / 8), c = (idx % (D / 8)) * 8;
+            const size_t gi = row0 + (size_t)r * p.H * D + c;
+            const bool ok = in_bounds(p.status, gi + 7, n_tok);
+            float f[8];
+            unpack8(ok ? k[gi / 8] : make_uint4(0, 0, 0, 0), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss.k[r][c + e] = f[e];
+            unpack8(ok ? q[gi / 8] : make_uint4(0, 0, 0, 0), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss.q[r][c + e] = f[e];
+            unpack8(ok ? v[gi / 8] : make_uint4(0, 0, 0, 0), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss.v[r][c + e] = f[e];
+        }
+        for (int idx = tid; idx < nt * (D / 4); idx += kThreads) {
+            const int r = idx / (D / 4), c = (idx % (D / 4)) * 4;
+            const size_t gi = row0 + (size_t)r * p.H * D + c;
+            const float4 g = in_bounds(p.status, gi + 3, n_tok) ? la[gi / 4]
+                                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4 *>(&ss.a[r][c]) =
+                make_float4(expf(g.x), expf(g.y), expf(g.z), expf(g.w));
+        }
+        if (tid < nt) {
+            const size_t bi = (size_t)(start + t0 + tid) * p.H + h;
+            ss.bet[tid] = in_bounds(p.status, bi, n_beta) ? p.beta[bi] : 0.f;
+        }
+        __syncthreads();
+        if (stepper)
+            serial_tokens<D, true, true>(st, &ss.k[0][0], &ss.q[0][0], &ss.a[0][0], &ss.v[0][0],
+                                         ss.bet, D, nt, ss.red_r, ss.red_o, o, 0, 0, 0,
+                                         p.status, 1);
+        __syncthreads();
+        for (int idx = tid; idx < nt * D; idx += kThreads) {
+            const int r = idx / D, vv = idx % D;
+            float ov = 0.f;
+#pragma unroll
+            for (int j = 0; j < P; ++j) ov += ss.red_o[(r * P + j) * D + vv];
+            const size_t oi = row0 + (size_t)r * p.H * D + vv;
+            if (in_bounds(p.status, oi, n_tok)) o[oi] = __float2bfloat16_rn(ov);
+        }
+    }
+    if (stepper && p.S_T) {
+#pragma unroll
+        for (int i = 0; i < CP; ++i)
+            if (in_bounds(p.status, srow + i, n_state)) p.S_T[srow + i] = st[i];
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q,
+    prefill_tc_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_o,
@@ -306,7 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool scanner = pw >= 4;
         const int bt = pt - 128;
         const uint32_t gpark = tmem + lane_addr + kColG;
-        bool domain_ok = true;
 
         // a1 for chunk m: log2-decay cumsum G2[t][c] = log2(e) sum_{t' <= t} log_alpha
         // of this thread's two tokens and the 16 channels from cg, from the landed
@@ -341,7 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lo = fminf(lo, fminf(g[0][e], g[1][e]));
                 hi = fmaxf(hi, fmaxf(g[0][e], g[1][e]));
             }
-            if (-lo > kLog2DecayLimit || hi > kLog2DecayLimit) domain_ok = false;
+            // a chunk outside the chunk form's range sends the whole (sequence,
+            // head) to the token-serial pass after teardown
+            if (!(-lo <= kLog2DecayLimit && hi <= kLog2DecayLimit))
+                *reinterpret_cast<volatile int *>(&sm.domain) = 1;
         };
         // Warps 4-7: gates of chunk m scanned and parked; once every scanning
         // thread has read the gate tile, it takes chunk m + 1.
@@ -484,7 +575,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 scan_ahead(n + 1);
             }
         }
-        if (!domain_ok) sm.domain = 1;
     } else {
         // -------------------------------------------------- serial carry (a6)
         const int et = tid - 32 * kCarryWarp0;
@@ -690,9 +780,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         store_output(nchunks - 1);
-        if (issuer) bulk_wait_group0();
+        if (issuer) {
+            bulk_wait_group0();
+            // order the bulk output stores before any later generic store to o
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
         __syncwarp();
-        if (p.S_T && in_bounds(p.status, state_off + (size_t)v * D + D - 1, n_state)) {
+        // (every chunk's gates were scanned before its T' reached this warp, so
+        // the flag is final here; a flagged head keeps S0 intact for the
+        // token-serial pass, which writes S_T itself)
+        if (p.S_T && !*reinterpret_cast<volatile int *>(&sm.domain) &&
+            in_bounds(p.status, state_off + (size_t)v * D + D - 1, n_state)) {
             float *dst = p.S_T + state_off + (size_t)v * D;
 #pragma unroll
             for (int cb = 0; cb < 8; ++cb) {
@@ -715,16 +813,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_drain(sm.full[n & 1], (n >> 1) & 1);
     if (tid == 32 * kPrepWarp0) wait_drain(sm.gfull, (nchunks - 1) & 1);
     __syncthreads();
-    if (tid == 0) {
-        if (sm.abort) raise_status(p.status, KDA_ERR_TIMEOUT);
-        else if (sm.domain) raise_status(p.status, KDA_ERR_DOMAIN);
-    }
+    if (tid == 0 && sm.abort) raise_status(p.status, KDA_ERR_TIMEOUT);
     if (warp == kPrepWarp0) {
         wait_drain(sm.bar_fin, 0);
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    if (sm.domain && !sm.abort) serial_head(&p, smem_raw, start, len, h, state_off);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {

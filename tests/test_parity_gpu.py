@@ -160,17 +160,52 @@ def test_zero_sizes(kda):
     assert o.numel() == 0 and ST.shape == (0, 2, 64, 64)
 
 
-def test_domain_status(kda):
-    """A gate far below the supported chunk log-decay range is reported."""
-    prob = I.prefill_problem(1, 128, 1, 128, 128, "bf16", (-5.0, -4.0), None, seed=8,
+@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [1, 65, 200])
+def test_wide_gate_domain(kda, engine, dtype, d, T):
+    """Per-token log-decay down to -5 (the K3 bound: -320 over a 64-token chunk,
+    far outside the chunk form's +-80) is exact: such chunks are taken token by
+    token, and the status word stays clear."""
+    if not engine_ok(engine, dtype, d):
+        pytest.skip("engine does not take this dtype/size")
+    prob = I.prefill_problem(2, T, 3, d, d, dtype, (-5.0, -0.5), 0.05, seed=T + d + 11,
                              device=DEV)
-    ws = torch.zeros(kda.kda_fwd_workspace_bytes(1), dtype=torch.uint8, device=DEV)
-    kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, workspace=ws)
-    assert kda.kda_read_device_status(ws) == kda.KDA_ERR_DOMAIN
-    ok = I.prefill_problem(1, 128, 1, 128, 128, "bf16", (-0.5, -0.001), None, seed=8,
-                           device=DEV)
-    kda.kda_fwd(ok.q, ok.k, ok.v, ok.log_alpha, ok.beta, workspace=ws)
+    ws = torch.zeros(kda.kda_fwd_workspace_bytes(2), dtype=torch.uint8, device=DEV)
+    o, ST = run_fwd(kda, prob, engine, workspace=ws)
     assert kda.kda_read_device_status(ws) == kda.KDA_OK
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2])
+    dt = prob.q.dtype
+    assert rel_err(o, o_ref) < tol_o(dt)
+    assert rel_err(ST, S_ref) < tol_s(dt)
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_wide_gate_mixed_chunks_varlen_in_place(kda, engine):
+    """Strong and mild gates mixed across heads and across the chunks of one
+    sequence, packed varlen with empty and ragged sequences, S_T written over
+    S0: the wide chunks take the token-serial path, the rest the chunk form."""
+    lengths = [130, 0, 64, 257, 1]
+    prob = I.prefill_problem(1, 0, 4, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=21,
+                             device=DEV, lengths=lengths)
+    g = torch.Generator().manual_seed(22)
+    la = prob.log_alpha.cpu()
+    strong = -(torch.rand(la.shape, generator=g) * 4.5 + 0.5)     # U(-5, -0.5)
+    la[:, 0] = strong[:, 0]                  # head 0: every chunk wide
+    la[64:128, 2] = strong[64:128, 2]         # head 2: the second chunk of sequence 0
+    la[194 + 100:194 + 110, 3] = -60.0        # head 3: ten tokens of near-total forgetting
+    prob.log_alpha.copy_(la.to(DEV))
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2, 3])
+    S = prob.S0.clone()
+    ws = torch.zeros(kda.kda_fwd_workspace_bytes(len(lengths)), dtype=torch.uint8, device=DEV)
+    o, _ = kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, S, prob.cu_seqlens,
+                       S_T=S, workspace=ws, engine=engine)
+    torch.cuda.synchronize()
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK
+    assert rel_err(o, o_ref) < 2e-2
+    assert rel_err(S, S_ref) < 1e-2
+    assert torch.equal(S[1], prob.S0[1])      # the empty sequence passes its state through
 
 
 def test_bad_device_offsets_write_nothing(kda):
