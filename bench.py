@@ -39,8 +39,9 @@ from linear_attention_recurrence_chunkwise_gb300 import inputs as I  # noqa: E40
 METRIC = "KDA prefill tokens/s and decode state GB/s (H=96,d=128) vs roofline"
 _CSRC = "linear_attention_recurrence_chunkwise_gb300/csrc/"
 KERNEL_SOURCES = {  # every source file a kernel is compiled from
-    "prefill_tc": (_CSRC + "kda_prefill_tc.cu", _CSRC + "kda_solve.cuh", _CSRC + "kda_sm100.cuh"),
-    "prefill_simt": (_CSRC + "kda_prefill_simt.cu",),
+    "prefill_tc": (_CSRC + "kda_prefill_tc.cu", _CSRC + "kda_solve.cuh", _CSRC + "kda_sm100.cuh",
+                   _CSRC + "kda_serial.cuh"),
+    "prefill_simt": (_CSRC + "kda_prefill_simt.cu", _CSRC + "kda_serial.cuh"),
     "decode": (_CSRC + "kda_decode.cu",),
     "multitoken": (_CSRC + "kda_multitoken.cu",),
 }
@@ -267,12 +268,18 @@ def run_ours(args, world, rank):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        time.sleep(0.25)  # let the sampler see the idle->busy edge
+        time.sleep(0.1)  # the sampler's first reading
         with torch.cuda.stream(stream):
-            # untimed steps right before the timed ones, so the GPU is busy (not
-            # idle after the sleep) when the first timed step starts
-            for _ in range(args.warmup):
-                call()
+            # untimed steps for at least 0.3 s right before the timed ones: the
+            # clocks have ramped up from idle when the first timed step starts,
+            # and the sampler reads them under this load
+            t_end = time.time() + 0.3
+            while True:
+                for _ in range(max(args.warmup, 1)):
+                    call()
+                stream.synchronize()
+                if time.time() >= t_end:
+                    break
             start.record(stream)
             for i in range(args.steps):
                 ev[i][0].record(stream)
