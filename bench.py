@@ -6,10 +6,12 @@ tokens/s.  The same JSON line carries a ``decode`` object: one decode step for
 64 sessions x 96 heads (fp32 state [64, 96, 128, 128], 403 MB, in place) --
 metric state-GB/s = 2 * state bytes / step time -- and a ``draft`` object:
 speculative decode on the same state, verify 8 draft tokens then commit them
-(kda_verify_tokens + kda_commit_tokens), metric draft tokens/s.
+(kda_verify_tokens + kda_commit_tokens), metric draft tokens/s -- and a
+``segment_parallel`` object: the long prefill of 12 heads (B=1, T=131072) with
+kda_fwd_cp against the plain kda_fwd.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload prefill|decode|long|varlen]
+                  [--workload prefill|decode|long|long_tp8|varlen]
 
 A step is one kda_fwd over the whole workload (the set-up kernel plus the
 prefill kernel).  Inputs are generated on the device before timing and are
@@ -187,6 +189,8 @@ def make_workload(name, seed, device):
     H, d = prob.q.shape[-2], prob.q.shape[-1]
     lab = {"prefill": "prefill B=1 H=96 T=8192 d=128 bf16, S0=0",
            "long": "long prefill B=1 H=96 T=131072 d=128 bf16, S0~N(0,0.02)",
+           "long_tp8": "long prefill B=1 H=12 T=131072 d=128 bf16, S0~N(0,0.02) "
+                       "(12 of K3's 96 heads: 8-way tensor parallel)",
            "varlen": f"varlen prefill 16 seqs (sum T={Ttot}) H=96 d=128 bf16",
            "tiny": "tiny prefill B=1 H=2 T=256 d=64 fp32"}[name]
     return dict(kind="prefill", prob=prob, Ttot=Ttot, H=H, d=d, label=lab)
@@ -214,15 +218,31 @@ def decode_alg_bytes(w):
 
 # ------------------------------------------------------------------ our arm
 
-def time_prefill(kda, w, steps, warmup, stream):
+def resolve_segments(kda, w, segments):
+    """None for the plain kda_fwd; else the segment count of kda_fwd_cp ('auto':
+    the library's suggestion for this workload)."""
+    if segments is None:
+        return None
+    if segments == "auto":
+        return kda.kda_fwd_cp_segments(w["prob"].n_seq, w["H"], w["Ttot"])
+    return int(segments)
+
+
+def time_prefill(kda, w, steps, warmup, stream, segments=None):
     p = w["prob"]
     o = torch.empty_like(p.v)
     ST = torch.empty((p.n_seq, w["H"], w["d"], w["d"]), dtype=torch.float32, device="cuda")
-    ws = torch.empty(kda.kda_fwd_workspace_bytes(p.n_seq), dtype=torch.uint8, device="cuda")
+    nbytes_ws = kda.kda_fwd_workspace_bytes(p.n_seq) if segments is None else \
+        kda.kda_fwd_cp_workspace_bytes(p.n_seq, w["H"], w["d"], w["d"], segments)
+    ws = torch.empty(nbytes_ws, dtype=torch.uint8, device="cuda")
 
     def call():
-        kda.kda_fwd(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0, p.cu_seqlens, o=o, S_T=ST,
-                    workspace=ws, stream=stream)
+        if segments is None:
+            kda.kda_fwd(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0, p.cu_seqlens, o=o, S_T=ST,
+                        workspace=ws, stream=stream)
+        else:
+            kda.kda_fwd_cp(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0, p.cu_seqlens,
+                           segments=segments, o=o, S_T=ST, workspace=ws, stream=stream)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             call()
@@ -243,8 +263,10 @@ def run_ours(args, world, rank):
     torch.cuda.synchronize()
 
     if w["kind"] == "prefill":
-        call, ev, bufs = time_prefill(kda, w, args.steps, args.warmup, stream)
-        launches_per_step = 2
+        segments = resolve_segments(kda, w, args.segments)
+        call, ev, bufs = time_prefill(kda, w, args.steps, args.warmup, stream, segments)
+        # plain: set-up + prefill kernel; segment-parallel: plan, pass A, scan, pass D
+        launches_per_step = 2 if segments is None or segments == 1 else 4
     else:
         S = w["S"]
         toks = w["tokens"]
@@ -334,10 +356,14 @@ def run_ours(args, world, rank):
             "gpu_launches": launches_per_step * args.steps}
     if w["kind"] == "prefill":
         line["config"].update(tokens_per_step=w["Ttot"], heads=w["H"], d=w["d"])
-        line["e2e"] = e2e_prefill(kda, w, max(2, min(args.steps, 5)), stream, world)
+        if segments is not None:
+            line["config"]["segments"] = segments
+            line["config"]["call"] = "kda_fwd_cp (segment-parallel)"
+        line["e2e"] = e2e_prefill(kda, w, max(2, min(args.steps, 5)), stream, world, segments)
         if args.workload == "prefill" and not args.no_decode:
             line["decode"] = decode_sub(kda, args, stream, pk)
             line["draft"] = draft_sub(kda, args, stream, pk, line["decode"]["us_per_step"])
+            line["segment_parallel"] = cp_sub(kda, args, stream, pk)
     else:
         line["e2e"] = e2e_decode(kda, w, max(2, min(args.steps, 20)), stream, world)
         if not args.no_decode:
@@ -428,9 +454,53 @@ def draft_sub(kda, args, stream, pk, decode_us):
             "verify": rv, "commit": rc, "reps": reps}
 
 
-def e2e_prefill(kda, w, steps, stream, world):
+def cp_sub(kda, args, stream, pk):
+    """Segment-parallel forward on the long prefill of the 12 heads one GPU holds
+    under 8-way tensor parallelism (B=1, H=12, T=131072): kda_fwd_cp with the
+    suggested segment count against the plain kda_fwd (12 blocks, one per head)."""
+    w = make_workload("long_tp8", seed=args.seed, device="cuda")
+    p = w["prob"]
+    N, H, d = p.n_seq, w["H"], w["d"]
+    P = kda.kda_fwd_cp_segments(N, H, w["Ttot"])
+    o = torch.empty_like(p.v)
+    ST = torch.empty((N, H, d, d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.kda_fwd_cp_workspace_bytes(N, H, d, d, P), dtype=torch.uint8,
+                     device="cuda")
+    plain = lambda: kda.kda_fwd(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0, o=o, S_T=ST,
+                                workspace=ws, stream=stream)
+    cp = lambda: kda.kda_fwd_cp(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0, segments=P, o=o,
+                                S_T=ST, workspace=ws, stream=stream)
+    out = {}
+    for name, fn in (("plain", plain), ("cp", cp)):
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                fn()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(3):
+                fn()
+            b.record(stream)
+        stream.synchronize()
+        out[name] = a.elapsed_time(b) / 3
+    alg = prefill_alg_bytes(w)
+    gbs = alg / (out["cp"] / 1e3) / 1e9
+    return {"metric": "tokens/s", "value": round(w["Ttot"] / (out["cp"] / 1e3), 1),
+            "unit": "tokens/s", "workload": w["label"], "segments": P,
+            "ms_segment_parallel": round(out["cp"], 3), "ms_plain": round(out["plain"], 3),
+            "speedup": round(out["plain"] / out["cp"], 2),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
+                         "algorithmic_bytes_per_call": alg,
+                         "note": "the operator's bytes over the whole call (three kernels "
+                                 "of passes A and D plus the scan)"}}
+
+
+def e2e_prefill(kda, w, steps, stream, world, segments=None):
     """Same metric through the public API with pinned host buffers: H2D of the
-    step's inputs, kda_fwd, D2H of o and S_T, all inside the timed region."""
+    step's inputs, kda_fwd (kda_fwd_cp with `segments`), D2H of o and S_T, all
+    inside the timed region."""
     p = w["prob"]
     host = {n: getattr(p, n).to("cpu").pin_memory()
             for n in ("q", "k", "v", "log_alpha", "beta")}
@@ -445,8 +515,10 @@ def e2e_prefill(kda, w, steps, stream, world):
         dev = {n: t.to("cuda", non_blocking=True) for n, t in host.items()}
         S0 = None if host_S0 is None else host_S0.to("cuda", non_blocking=True)
         cu = None if host_cu is None else host_cu.to("cuda", non_blocking=True)
-        o, ST = kda.kda_fwd(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"], S0,
-                            cu, stream=stream)
+        fwd = kda.kda_fwd if segments is None else \
+            (lambda *a, **kw: kda.kda_fwd_cp(*a, segments=segments, **kw))
+        o, ST = fwd(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"], S0, cu,
+                    stream=stream)
         o_h.copy_(o, non_blocking=True)
         ST_h.copy_(ST, non_blocking=True)
     with torch.cuda.stream(stream):
@@ -576,11 +648,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["prefill", "decode", "long", "varlen", "tiny"],
+    ap.add_argument("--workload",
+                    choices=["prefill", "decode", "long", "long_tp8", "varlen", "tiny"],
                     default="prefill")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--segments", default=None,
+                    help="prefill workloads: time kda_fwd_cp with this many segments per "
+                         "sequence ('auto': the library's suggestion) instead of kda_fwd")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode and draft sub-benchmarks")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode, draft and segment-parallel sub-benchmarks")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

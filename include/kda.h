@@ -132,6 +132,54 @@ kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
                             void *workspace, size_t workspace_bytes, void *stream,
                             kda_engine_t engine);
 
+/*
+ * kda_fwd_cp -- segment-parallel ("context-parallel" on one GPU) forward.
+ *
+ * Same arguments, results and conventions as kda_fwd_engine, for prefills that
+ * leave SMs idle: one (sequence, head) is one serial chain of chunks, so with
+ * few heads -- a rank that holds a tensor-parallel share of the heads -- most
+ * of the GPU waits ("Kimi K3模型架构详解" section 11.1: single-GPU SM-level
+ * context parallelism over sequence segments).  Each sequence is cut into
+ * `segments` pieces at 64-token chunk boundaries.  A segment acts on the state
+ * as the affine map S_out = M S_in + S~ (section 3.6: M the segment's
+ * accumulated decay and erase, S~ the state it builds from zero; maps compose
+ * as (M2, b2) o (M1, b1) = (M2 M1, M2 b1 + b2)).  The call runs, on `stream`:
+ * the first segment of every sequence from S0 together with (S~, M) of every
+ * later segment (M as the end state from S0 = I with v = 0); an fp32 scan that
+ * composes the maps into each later segment's start state; then the later
+ * segments again from their start states, which writes their outputs and S_T.
+ * The later segments thus cost about three times a plain pass, in parallel.
+ *
+ * segments: >= 1 (1 is kda_fwd_engine); kda_fwd_cp_segments suggests a value.
+ *   Sequences shorter than `segments` chunks get empty segments (identity
+ *   maps).  Requires d_k = d_v (as every entry point here).
+ * workspace: at least kda_fwd_cp_workspace_bytes(N, H, d_k, d_v, segments)
+ *   bytes, 16-byte aligned, contents on entry irrelevant; it holds the status
+ *   word (kda_read_device_status), the segment task tables and four fp32
+ *   state sets per later segment: about 4 (segments - 1) N H d_k d_v 4 bytes.
+ * S_T may alias S0.  Results agree with kda_fwd to the rounding of the state
+ * hand-off: the maps of the tensor-core engine carry its bf16 operand
+ * rounding, which the scan composes; the tolerances of kda_fwd hold for the
+ * segment counts kda_fwd_cp_segments returns.
+ * Errors: as kda_fwd_engine; KDA_ERR_INVALID_ARGUMENT for segments < 1 or
+ * above 65536, KDA_ERR_WORKSPACE for a short workspace.
+ */
+kda_status_t kda_fwd_cp(const void *q, const void *k, const void *v,
+                        const float *log_alpha, const float *beta, const float *S0,
+                        const int32_t *cu_seqlens, int B, int T, int H, int d_k, int d_v,
+                        int N, kda_dtype_t dtype, void *o, float *S_T, int segments,
+                        void *workspace, size_t workspace_bytes, void *stream,
+                        kda_engine_t engine);
+
+/* Workspace bytes of kda_fwd_cp (0 for invalid sizes). */
+size_t kda_fwd_cp_workspace_bytes(int N, int H, int d_k, int d_v, int segments);
+
+/* A segment count for kda_fwd_cp on the current device: the smallest modelled
+ * time with the first pass in one wave of N H (2 segments - 1) blocks over the
+ * device's SMs; 1 (a plain kda_fwd) whenever N H already fills them.  Ttot is
+ * the total number of tokens (the average sequence length sets the model). */
+int kda_fwd_cp_segments(int N, int H, int64_t Ttot);
+
 /* Largest N kda_fwd_noalloc accepts. */
 #define KDA_NOALLOC_MAX_SEQS 16384
 

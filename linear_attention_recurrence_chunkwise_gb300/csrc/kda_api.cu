@@ -56,12 +56,17 @@ size_t kda_state_bytes(int layers, int N, int H, int d_k, int d_v, int elem_byte
     return total;
 }
 
-kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
-                            const float *log_alpha, const float *beta, const float *S0,
-                            const int32_t *cu_seqlens, int B, int T, int H, int d_k,
-                            int d_v, int N, kda_dtype_t dtype, void *o, float *S_T,
-                            void *workspace, size_t workspace_bytes, void *stream,
-                            kda_engine_t engine) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks shared by kda_fwd and kda_fwd_cp (everything but the
+// workspace size), and the engine choice.  On KDA_OK, p holds the arguments.
+kda_status_t check_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                       const float *beta, const float *S0, const int32_t *cu_seqlens, int B,
+                       int T, int H, int d_k, int d_v, int N, kda_dtype_t dtype, void *o,
+                       float *S_T, void *workspace, kda_engine_t engine, kda::FwdParams &p,
+                       bool &use_tc) {
     if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_INVALID_ARGUMENT;
     if (engine != KDA_ENGINE_AUTO && engine != KDA_ENGINE_TENSORCORE &&
         engine != KDA_ENGINE_CUDACORE)
@@ -84,15 +89,16 @@ kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
             return KDA_ERR_INVALID_ARGUMENT;
     }
     if ((S0 && !aligned16(S0)) || (S_T && !aligned16(S_T))) return KDA_ERR_INVALID_ARGUMENT;
-    if (!workspace || workspace_bytes < kda_fwd_workspace_bytes(N)) return KDA_ERR_WORKSPACE;
+    if (!workspace) return KDA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KDA_ERR_INVALID_ARGUMENT;
 
     const bool tc_ok = kda::prefill_tc_supported(dtype, d_k, d_v) && Ttot <= INT32_MAX;
     if (engine == KDA_ENGINE_TENSORCORE && !tc_ok) return KDA_ERR_UNSUPPORTED;
-    const bool use_tc = engine == KDA_ENGINE_TENSORCORE || (engine == KDA_ENGINE_AUTO && tc_ok);
-    if (fault_injected()) return KDA_ERR_CUDA;
+    use_tc = engine == KDA_ENGINE_TENSORCORE || (engine == KDA_ENGINE_AUTO && tc_ok);
 
-    kda::FwdParams p;
+    p = kda::FwdParams{};
+    p.tasks = nullptr;
+    p.vzero = nullptr;
     p.q = q;
     p.k = k;
     p.v = v;
@@ -112,12 +118,93 @@ kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
     p.N = N;
     p.dk = d_k;
     p.dv = d_v;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
+                            const float *log_alpha, const float *beta, const float *S0,
+                            const int32_t *cu_seqlens, int B, int T, int H, int d_k,
+                            int d_v, int N, kda_dtype_t dtype, void *o, float *S_T,
+                            void *workspace, size_t workspace_bytes, void *stream,
+                            kda_engine_t engine) {
+    kda::FwdParams p;
+    bool use_tc = false;
+    const kda_status_t st = check_fwd(q, k, v, log_alpha, beta, S0, cu_seqlens, B, T, H, d_k,
+                                      d_v, N, dtype, o, S_T, workspace, engine, p, use_tc);
+    if (st != KDA_OK) return st;
+    if (workspace_bytes < kda_fwd_workspace_bytes(N)) return KDA_ERR_WORKSPACE;
+    if (fault_injected()) return KDA_ERR_CUDA;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (kda::launch_schedule(p, s) != cudaSuccess) return KDA_ERR_CUDA;
     if (N == 0) return KDA_OK;
     const cudaError_t e = use_tc ? kda::launch_prefill_tc(p, s)
                                  : kda::launch_prefill_simt(p, dtype, s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+size_t kda_fwd_cp_workspace_bytes(int N, int H, int d_k, int d_v, int segments) {
+    if (segments < 1 || H <= 0 || !supported_dims(d_k, d_v)) return 0;
+    const size_t base = kda_fwd_workspace_bytes(N);
+    if (segments == 1) return base;
+    const size_t cp = kda::cp_layout(N, H, d_k, segments).total;
+    return cp > base ? cp : base;
+}
+
+int kda_fwd_cp_segments(int N, int H, int64_t Ttot) {
+    if (N <= 0 || H <= 0 || Ttot <= 0) return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        return 1;
+    // Modelled time in chunk periods of one block (one block per SM): a plain
+    // pass walks every chunk of a sequence in ceil(N H / SMs) waves; P >= 2
+    // segments walk a segment in pass A (N H (2P - 1) blocks) and again in
+    // pass D (N H (P - 1) blocks), plus P - 2 scan steps of about 2.5 periods
+    // (measured on the long prefill) and a few periods of launch and pipeline
+    // fill.
+    const int64_t units = (int64_t)N * H;
+    const int64_t chunks = (Ttot / N + 63) / 64;  // per sequence, on average
+    auto waves = [&](int64_t blocks) { return (double)((blocks + sms - 1) / sms); };
+    int best = 1;
+    double best_t = waves(units) * (double)chunks;
+    for (int64_t P = 2; P <= chunks && P <= 1024; ++P) {
+        const double seg = (double)((chunks + P - 1) / P);
+        const double t = (waves(units * (2 * P - 1)) + waves(units * (P - 1))) * seg +
+                         2.5 * (double)(P - 2) + 6.0;
+        if (t < best_t) {
+            best_t = t;
+            best = (int)P;
+        }
+    }
+    return best;
+}
+
+kda_status_t kda_fwd_cp(const void *q, const void *k, const void *v, const float *log_alpha,
+                        const float *beta, const float *S0, const int32_t *cu_seqlens, int B,
+                        int T, int H, int d_k, int d_v, int N, kda_dtype_t dtype, void *o,
+                        float *S_T, int segments, void *workspace, size_t workspace_bytes,
+                        void *stream, kda_engine_t engine) {
+    kda::FwdParams p;
+    bool use_tc = false;
+    const kda_status_t st = check_fwd(q, k, v, log_alpha, beta, S0, cu_seqlens, B, T, H, d_k,
+                                      d_v, N, dtype, o, S_T, workspace, engine, p, use_tc);
+    if (st != KDA_OK) return st;
+    if (segments < 1 || segments > 65536) return KDA_ERR_INVALID_ARGUMENT;
+    if ((int64_t)N * H * (2 * (int64_t)segments - 1) > INT32_MAX) return KDA_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < kda_fwd_cp_workspace_bytes(N, H, d_k, d_v, segments))
+        return KDA_ERR_WORKSPACE;
+    if (segments == 1)
+        return kda_fwd_engine(q, k, v, log_alpha, beta, S0, cu_seqlens, B, T, H, d_k, d_v, N,
+                              dtype, o, S_T, workspace, workspace_bytes, stream, engine);
+    if (fault_injected()) return KDA_ERR_CUDA;
+    const cudaError_t e = kda::launch_fwd_cp(p, dtype, use_tc, segments, workspace,
+                                             static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -15,12 +15,30 @@ constexpr float kLogDecayLimit = 80.f;  // |in-chunk cumulative log-decay| suppo
 // launch order of the sequences (longest first).
 constexpr size_t kWsOrderOffset = 16;
 
+// One unit of prefill work in task-table mode (segment-parallel forward): a
+// token range of the packed tensors with its own initial and final state.
+constexpr int32_t kTaskVZero = 1;       // treat v as zero over the range
+constexpr int32_t kTaskS0Identity = 2;  // initial state I (d_k = d_v); S0 is ignored
+constexpr int32_t kTaskNoOutput = 4;    // compute the final state only; o is not written
+constexpr size_t kVZeroBytes = 64 * 128 * 2;  // one 64-token bf16 tile of a 128-wide head
+struct SegTask {
+    int64_t start;    // first token
+    int32_t len;      // tokens
+    int32_t flags;    // kTask* bits
+    const float *S0;  // [H][d_v][d_k] initial state of this range, or nullptr (zeros)
+    float *S_T;       // [H][d_v][d_k] final state, or nullptr (not written)
+};
+
 struct FwdParams {
+    const SegTask *tasks;       // nullptr: one unit per sequence (cu_seqlens / T);
+                                // else N tasks (S0 / S_T / cu_seqlens / order unused)
     const void *q, *k, *v;
     const float *log_alpha, *beta, *S0;
     const int32_t *cu_seqlens;  // nullptr: fixed length T per sequence
     void *o;
     float *S_T;
+    const void *vzero;          // task mode: kVZeroBytes of zeros (the V source of
+                                // kTaskVZero tasks for the tensor-core engine)
     int32_t *status;            // workspace status word
     const int32_t *order;       // workspace launch order, nullptr for fixed length
     int64_t Ttot;
@@ -28,16 +46,45 @@ struct FwdParams {
     int H, N, dk, dv;
 };
 
-// Token range of sequence n (device helper used by every prefill kernel).
+// Token range of sequence (or task) n (device helper used by every prefill kernel).
 __device__ __forceinline__ void seq_range(const FwdParams &p, int n, int64_t &start,
                                           int &len) {
-    if (p.cu_seqlens) {
+    if (p.tasks) {
+        start = p.tasks[n].start;
+        len = p.tasks[n].len;
+    } else if (p.cu_seqlens) {
         start = p.cu_seqlens[n];
         len = p.cu_seqlens[n + 1] - p.cu_seqlens[n];
     } else {
         start = (int64_t)n * p.T;
         len = p.T;
     }
+}
+
+// Where one CTA's state lives: S0 / S_T base pointers with the element offset
+// of its [d_v][d_k] block and the extent the offset is checked against, plus
+// the task flags (0 outside task-table mode).
+struct StateRef {
+    const float *S0;
+    float *S_T;
+    size_t off, ext;
+    int32_t flags;
+};
+
+__device__ __forceinline__ StateRef state_ref(const FwdParams &p, int n, int h, int dk,
+                                              int dv) {
+    const size_t blk = (size_t)dk * dv;
+    if (p.tasks) {
+        const SegTask &t = p.tasks[n];
+        return {t.S0, t.S_T, (size_t)h * blk, (size_t)p.H * blk, t.flags};
+    }
+    return {p.S0, p.S_T, ((size_t)n * p.H + h) * blk, (size_t)p.N * p.H * blk, 0};
+}
+
+// Initial-state element [v][c] of a CTA (identity, given or zero).
+__device__ __forceinline__ float state_init(const StateRef &r, int v, int c, int dk) {
+    if (r.flags & kTaskS0Identity) return v == c ? 1.f : 0.f;
+    return r.S0 ? r.S0[r.off + (size_t)v * dk + c] : 0.f;
 }
 
 __device__ __forceinline__ void raise_status(int32_t *status, int code) {
@@ -61,6 +108,19 @@ __device__ __forceinline__ bool in_bounds(int32_t *status, size_t idx, size_t n)
     return true;
 #endif
 }
+
+// Workspace of the segment-parallel forward (byte offsets; [0, 4) is the status
+// word): task tables of pass A (N (2P - 1) tasks) and pass D (N (P - 1)), the
+// zero V source, and the state sets ([H][d][d] fp32 each) S_a (end of segment
+// 0, per sequence), S~, M and S_in (per later segment).
+struct CpLayout {
+    size_t tasks_a, tasks_d, vzero, s_a, s_t, m_t, s_in, total;
+};
+CpLayout cp_layout(int N, int H, int d, int P);
+// P >= 2 segments per sequence; base carries the validated kda_fwd arguments
+// (status = the workspace).
+cudaError_t launch_fwd_cp(const FwdParams &base, kda_dtype_t dt, bool use_tc, int P,
+                          void *workspace, cudaStream_t s);
 
 cudaError_t launch_schedule(const FwdParams &p, cudaStream_t s);
 cudaError_t launch_prefill_simt(const FwdParams &p, kda_dtype_t dt, cudaStream_t s);

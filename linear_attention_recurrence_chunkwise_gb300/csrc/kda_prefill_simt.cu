@@ -86,15 +86,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(FwdParams p) 
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
     Tin *o = static_cast<Tin *>(p.o);
-    const size_t state_off = ((size_t)n * p.H + h) * D * D;
-    const size_t n_state = (size_t)p.N * p.H * D * D;  // extents, for the bounds checks
+    const StateRef sref = state_ref(p, n, h, D, D);  // S0 / S_T block and task flags
+    const bool vzero = sref.flags & kTaskVZero;
+    if (sref.flags & kTaskNoOutput) o = nullptr;
     const size_t n_tok = (size_t)p.Ttot * p.H * D, n_beta = (size_t)p.Ttot * p.H;
 
     // initial state: memory [v][c] -> logical S[c][v]
     for (int idx = tid; idx < D * D; idx += kThreads) {
         const int vv = idx / D, c = idx % D;
         sm.S[c * LD + vv] =
-            p.S0 && in_bounds(p.status, state_off + idx, n_state) ? p.S0[state_off + idx] : 0.f;
+            in_bounds(p.status, sref.off + idx, sref.ext) ? state_init(sref, vv, c, D) : 0.f;
     }
 
     const int nchunks = (len + C - 1) / C;
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(FwdParams p) 
             const bool ok = r < valid && in_bounds(p.status, gi, n_tok);
             sm.Qh[r * LD + c] = ok ? to_f(q[gi]) : 0.f;
             sm.Kh[r * LD + c] = ok ? to_f(k[gi]) : 0.f;
-            sm.Vb[r * LD + c] = ok ? to_f(v[gi]) : 0.f;
+            sm.Vb[r * LD + c] = ok && !vzero ? to_f(v[gi]) : 0.f;
             sm.Kb[r * LD + c] = ok ? p.log_alpha[gi] : 0.f;
         }
         if (tid < C) {
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(FwdParams p) 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = ty + 16 * i;
-            if (r < valid) {
+            if (r < valid && o) {
                 const size_t go = ((size_t)(t0 + r) * p.H + h) * D;
 #pragma unroll
                 for (int j = 0; j < NJ; ++j)
@@ -316,11 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_simt_kernel(FwdParams p) 
         }
     }
     __syncthreads();
-    if (p.S_T) {
+    if (sref.S_T) {
         for (int idx = tid; idx < D * D; idx += kThreads) {
             const int vv = idx / D, c = idx % D;
-            if (in_bounds(p.status, state_off + idx, n_state))
-                p.S_T[state_off + idx] = sm.S[c * LD + vv];
+            if (in_bounds(p.status, sref.off + idx, sref.ext))
+                sref.S_T[sref.off + idx] = sm.S[c * LD + vv];
         }
     }
 }

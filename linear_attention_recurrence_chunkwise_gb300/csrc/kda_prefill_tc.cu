@@ -197,14 +197,14 @@ struct SerialStage {
 };
 
 __device__ __forceinline__ void serial_head(const FwdParams *pp, uint8_t *smem_raw,
-                                         int64_t start, int len, int h, size_t state_off) {
+                                         int64_t start, int len, int h, const StateRef &sref) {
     const FwdParams &p = *pp;
     SerialStage &ss = *reinterpret_cast<SerialStage *>(
         smem_raw + ((16u - (smem_u32(smem_raw) & 15u)) & 15u));
     constexpr int CP = Serial<D>::kCP, P = Serial<D>::kParts;
     const int tid = threadIdx.x, vcol = tid % D, c0 = (tid / D) * CP;
     const bool stepper = tid < Serial<D>::kThreads;
-    const size_t n_state = (size_t)p.N * p.H * D * D;
+    const bool vzero = sref.flags & kTaskVZero, no_out = sref.flags & kTaskNoOutput;
     const size_t n_tok = (size_t)p.Ttot * p.H * D, n_beta = (size_t)p.Ttot * p.H;
     const uint4 *q = static_cast<const uint4 *>(p.q);  // 8 bf16 per load; rows start on 16 bytes
     const uint4 *k = static_cast<const uint4 *>(p.k);
@@ -213,10 +213,11 @@ __device__ __forceinline__ void serial_head(const FwdParams *pp, uint8_t *smem_r
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
     // S[c0 + i][v] lives at memory [v][c0 + i]
     float st[CP];
-    const size_t srow = state_off + (size_t)vcol * D + c0;
+    const size_t srow = sref.off + (size_t)vcol * D + c0;
 #pragma unroll
     for (int i = 0; i < CP; ++i)
-        st[i] = stepper && p.S0 && in_bounds(p.status, srow + i, n_state) ? p.S0[srow + i] : 0.f;
+        st[i] = stepper && in_bounds(p.status, srow + i, sref.ext)
+                    ? state_init(sref, vcol, c0 + i, D) : 0.f;
     for (int t0 = 0; t0 < len; t0 += C) {
         const int nt = min(C, len - t0);
         const size_t row0 = ((size_t)(start + t0) * p.H + h) * D;  // element index of token t0
@@ -232,7 +233,7 @@ __device__ __forceinline__ void serial_head(const FwdParams *pp, uint8_t *smem_r
             unpack8(ok ? q[gi / 8] : make_uint4(0, 0, 0, 0), f);
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss.q[r][c + e] = f[e];
-            unpack8(ok ? v[gi / 8] : make_uint4(0, 0, 0, 0), f);
+            unpack8(ok && !vzero ? v[gi / 8] : make_uint4(0, 0, 0, 0), f);
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss.v[r][c + e] = f[e];
         }
@@ -254,7 +255,7 @@ __device__ __forceinline__ void serial_head(const FwdParams *pp, uint8_t *smem_r
                                          ss.bet, D, nt, ss.red_r, ss.red_o, o, 0, 0, 0,
                                          p.status, 1);
         __syncthreads();
-        for (int idx = tid; idx < nt * D; idx += kThreads) {
+        for (int idx = tid; idx < (no_out ? 0 : nt * D); idx += kThreads) {
             const int r = idx / D, vv = idx % D;
             float ov = 0.f;
 #pragma unroll
@@ -263,19 +264,23 @@ __device__ __forceinline__ void serial_head(const FwdParams *pp, uint8_t *smem_r
             if (in_bounds(p.status, oi, n_tok)) o[oi] = __float2bfloat16_rn(ov);
         }
     }
-    if (stepper && p.S_T) {
+    if (stepper && sref.S_T) {
 #pragma unroll
         for (int i = 0; i < CP; ++i)
-            if (in_bounds(p.status, srow + i, n_state)) p.S_T[srow + i] = st[i];
+            if (in_bounds(p.status, srow + i, sref.ext)) sref.S_T[srow + i] = st[i];
     }
 }
 
+// kTasks: task-table mode (segment-parallel forward); the plain instantiation
+// compiles none of its per-task choices.
+template <bool kTasks>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_o,
-                      const __grid_constant__ CUtensorMap tm_g) {
+                      const __grid_constant__ CUtensorMap tm_g,
+                      const __grid_constant__ CUtensorMap tm_vz) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Align by offsetting the shared-memory pointer itself (not through an
     // integer round trip), so the compiler keeps every access in the shared
@@ -291,14 +296,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     int len;
     seq_range(p, nseq, start, len);
     const int nchunks = (len + C - 1) / C;
-    const size_t state_off = ((size_t)nseq * p.H + h) * D * D;
-    const size_t n_state = (size_t)p.N * p.H * D * D;  // extents, for the bounds checks
+    StateRef sref;  // S0 / S_T block and task flags
+    if constexpr (kTasks)
+        sref = state_ref(p, nseq, h, D, D);
+    else
+        sref = {p.S0, p.S_T, ((size_t)nseq * p.H + h) * D * D, (size_t)p.N * p.H * D * D, 0};
+    const bool no_out = kTasks && (sref.flags & kTaskNoOutput);
+    // a task with v = 0 reads its V tiles through a map that only holds zeros
+    const CUtensorMap *tmv = &tm_v;
+    if constexpr (kTasks)
+        if (sref.flags & kTaskVZero) tmv = &tm_vz;
     const size_t n_tok = (size_t)p.Ttot * p.H * D, n_beta = (size_t)p.Ttot * p.H;
     if (nchunks == 0) {  // empty sequence: the state passes through
-        if (p.S_T)
+        if (sref.S_T)
             for (int i = tid; i < D * D; i += kThreads)
-                if (in_bounds(p.status, state_off + i, n_state))
-                    p.S_T[state_off + i] = p.S0 ? p.S0[state_off + i] : 0.f;
+                if (in_bounds(p.status, sref.off + i, sref.ext))
+                    sref.S_T[sref.off + i] = state_init(sref, i / D, i % D, D);
         return;
     }
 
@@ -344,16 +357,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem_u32(S.kq + 8192), &tm_q, fb, 0, h, t0);
         tma_load_3d(smem_u32(S.kq + 16384), &tm_k, fb, 64, h, t0);
         tma_load_3d(smem_u32(S.kq + 24576), &tm_q, fb, 64, h, t0);
-        tma_load_3d(smem_u32(S.v), &tm_v, fb, 0, h, t0);
-        tma_load_3d(smem_u32(S.v + 8192), &tm_v, fb, 64, h, t0);
+        tma_load_3d(smem_u32(S.v), tmv, fb, 0, h, t0);
+        tma_load_3d(smem_u32(S.v + 8192), tmv, fb, 64, h, t0);
         if (n + 1 < nchunks) {
             const int t1 = t0 + C;
             tma_prefetch_3d(&tm_k, 0, h, t1);
             tma_prefetch_3d(&tm_k, 64, h, t1);
             tma_prefetch_3d(&tm_q, 0, h, t1);
             tma_prefetch_3d(&tm_q, 64, h, t1);
-            tma_prefetch_3d(&tm_v, 0, h, t1);
-            tma_prefetch_3d(&tm_v, 64, h, t1);
+            if (tmv == &tm_v) {  // (the zero map holds nothing to prefetch)
+                tma_prefetch_3d(&tm_v, 0, h, t1);
+                tma_prefetch_3d(&tm_v, 64, h, t1);
+            }
         }
     };
     auto load_gates = [&](int n) {
@@ -368,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         prefetch_tensormap(&tm_g);
+        prefetch_tensormap(tmv);
         load_gates(0);
         load_stage(0);
         if (nchunks > 1) load_stage(1);
@@ -581,17 +597,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool issuer = et == 0;
         const int v = L;
         {  // initial state: row v of S0 ([v][c] memory) -> TMEM fp32 and bf16 operand
+            const bool ident = kTasks && (sref.flags & kTaskS0Identity);
             const float *src =
-                p.S0 && in_bounds(p.status, state_off + (size_t)v * D + D - 1, n_state)
-                    ? p.S0 + state_off + (size_t)v * D
+                !ident && sref.S0 && in_bounds(p.status, sref.off + (size_t)v * D + D - 1, sref.ext)
+                    ? sref.S0 + sref.off + (size_t)v * D
                     : nullptr;
 #pragma unroll
             for (int cb = 0; cb < 8; ++cb) {
                 uint32_t u[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const float4 x = src ? reinterpret_cast<const float4 *>(src + 16 * cb)[q]
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 x = src ? reinterpret_cast<const float4 *>(src + 16 * cb)[q]
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (ident) {  // row v of I: a one in column v
+                        const int c = 16 * cb + 4 * q;
+                        x = make_float4(c == v ? 1.f : 0.f, c + 1 == v ? 1.f : 0.f,
+                                        c + 2 == v ? 1.f : 0.f, c + 3 == v ? 1.f : 0.f);
+                    }
                     u[4 * q] = __float_as_uint(x.x); u[4 * q + 1] = __float_as_uint(x.y);
                     u[4 * q + 2] = __float_as_uint(x.z); u[4 * q + 3] = __float_as_uint(x.w);
                 }
@@ -625,7 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             fence_proxy_async_smem();
             named_bar_sync(kBarCarry, kCarryThreads);
-            if (valid == C) {
+            if (no_out) {
+                // final state only: the tile was read out (freeing O) but is not stored
+            } else if (valid == C) {
                 if (issuer) {
                     tma_store_3d(&tm_o, smem_u32(sm.ut), 0, h, static_cast<int>(t0));
                     tma_store_3d(&tm_o, smem_u32(sm.ut + 8192), 64, h, static_cast<int>(t0));
@@ -789,9 +813,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (every chunk's gates were scanned before its T' reached this warp, so
         // the flag is final here; a flagged head keeps S0 intact for the
         // token-serial pass, which writes S_T itself)
-        if (p.S_T && !*reinterpret_cast<volatile int *>(&sm.domain) &&
-            in_bounds(p.status, state_off + (size_t)v * D + D - 1, n_state)) {
-            float *dst = p.S_T + state_off + (size_t)v * D;
+        if (sref.S_T && !*reinterpret_cast<volatile int *>(&sm.domain) &&
+            in_bounds(p.status, sref.off + (size_t)v * D + D - 1, sref.ext)) {
+            float *dst = sref.S_T + sref.off + (size_t)v * D;
 #pragma unroll
             for (int cb = 0; cb < 8; ++cb) {
                 uint32_t x[16];
@@ -820,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (sm.domain && !sm.abort) serial_head(&p, smem_raw, start, len, h, state_off);
+    if (sm.domain && !sm.abort) serial_head(&p, smem_raw, start, len, h, sref);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -875,17 +899,24 @@ cudaError_t launch_prefill_tc(const FwdParams &p, cudaStream_t s) {
     if ((size_t)p.N * p.H == 0) return cudaSuccess;
     if (p.Ttot == 0) return launch_prefill_simt(p, KDA_BF16, s);  // nothing to contract
     if (p.Ttot > INT32_MAX) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv, mo, mg;
+    CUtensorMap mq, mk, mv, mo, mg, mvz;
     if (!make_token_map(&mq, p.q, p.H, p.Ttot) || !make_token_map(&mk, p.k, p.H, p.Ttot) ||
         !make_token_map(&mv, p.v, p.H, p.Ttot) || !make_token_map(&mo, p.o, p.H, p.Ttot) ||
         !make_gate_map(&mg, p.log_alpha, p.H, p.Ttot))
         return cudaErrorInvalidValue;
+    // V of kTaskVZero tasks: one head x 64 tokens of zeros; every other tile
+    // coordinate lies outside it and is zero-filled by the copy
+    if (p.vzero) {
+        if (!make_token_map(&mvz, p.vzero, 1, 64)) return cudaErrorInvalidValue;
+    } else {
+        mvz = mv;
+    }
     const size_t smem = sizeof(TcSmem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = p.tasks ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<<<(unsigned)((size_t)p.N * p.H), kThreads, smem, s>>>(p, mq, mk, mv, mo,
-                                                                             mg);
+    kern<<<(unsigned)((size_t)p.N * p.H), kThreads, smem, s>>>(p, mq, mk, mv, mo, mg, mvz);
     return cudaGetLastError();
 }
 

@@ -88,8 +88,9 @@ __device__ __forceinline__ float4 serial_ld4(const float *p) {
 //  - kDeferO: token r's per-part partial sums of o are left in
 //    red_o[(r * kParts + part) * D + v] (red_o: float[ntok][kParts][D]); the
 //    caller adds the parts after a barrier.
-//  - otherwise: o[o_base + r * o_stride + v] is stored here (a second barrier
-//    per token; n_o is o's extent, for the bounds-checked build).
+//  - otherwise: o[o_base + r * o_stride + v] is stored here, unless o is null
+//    (a second barrier per token; n_o is o's extent, for the bounds-checked
+//    build).
 template <int D, bool kVec4, bool kDeferO, typename Tout>
 __device__ __forceinline__ void serial_tokens(float (&s)[Serial<D>::kCP], const float *K,
                                               const float *Q, const float *A, const float *V,
@@ -137,7 +138,7 @@ __device__ __forceinline__ void serial_tokens(float (&s)[Serial<D>::kCP], const 
         } else {
             red_o[part * D + v] = op;
             serial_bar(bar_id, Serial<D>::kThreads);
-            if (part == 0) {
+            if (part == 0 && o) {
                 float ov = 0.f;
 #pragma unroll
                 for (int j = 0; j < P; ++j) ov += red_o[j * D + v];

@@ -38,6 +38,10 @@ PRESETS = {
     "tiny": dict(B=1, H=2, T=256, d=64, dtype="f32", la=(-0.5, -0.001), s0_std=None),
     "prefill": dict(B=1, H=96, T=8192, d=128, dtype="bf16", la=(-0.5, -0.001), s0_std=None),
     "long": dict(B=1, H=96, T=131072, d=128, dtype="bf16", la=(-0.05, -0.0001), s0_std=0.02),
+    # the long prefill on the 12 heads one GPU holds when tensor parallelism
+    # splits K3's 96 heads over 8 GPUs (the segment-parallel workload)
+    "long_tp8": dict(B=1, H=12, T=131072, d=128, dtype="bf16", la=(-0.05, -0.0001),
+                     s0_std=0.02),
     "varlen": dict(n_seq=16, H=96, d=128, dtype="bf16", la=(-0.5, -0.001), s0_std=0.02,
                    len_lo=1024, len_hi=65536, decode_steps=256),
     "decode": dict(N=64, H=96, d=128, dtype="bf16", la=(-0.1, -0.0005), s0_std=0.02, steps=1000),
@@ -162,7 +166,8 @@ def decode_state(N: int, H: int, dk: int, dv: int, std=0.02, seed: int = 0, devi
 
 
 def preset_problem(name: str, seed: int = 0, device="cpu") -> Problem:
-    """Prefill problem of a named preset ('tiny', 'prefill', 'long', 'varlen')."""
+    """Prefill problem of a named preset ('tiny', 'prefill', 'long', 'long_tp8',
+    'varlen')."""
     p = PRESETS[name]
     if name == "varlen":
         lengths = varlen_lengths(p["n_seq"], p["len_lo"], p["len_hi"], seed)

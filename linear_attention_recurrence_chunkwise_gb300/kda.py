@@ -30,6 +30,7 @@ ENGINES = {"auto": 0, "tensorcore": 1, "cudacore": 2}
 
 # every symbol include/kda.h declares
 EXPORTED = ["kda_fwd_workspace_bytes", "kda_fwd", "kda_fwd_engine", "kda_fwd_noalloc",
+            "kda_fwd_cp", "kda_fwd_cp_workspace_bytes", "kda_fwd_cp_segments",
             "kda_decode_step", "kda_verify_tokens", "kda_commit_tokens",
             "kda_read_device_status", "kda_state_bytes", "kda_status_string"]
 KDA_NOALLOC_MAX_SEQS = 16384
@@ -71,6 +72,12 @@ def load_library(path: str) -> ctypes.CDLL:
     lib.kda_fwd.argtypes = fwd_args
     lib.kda_fwd_engine.restype = ci
     lib.kda_fwd_engine.argtypes = fwd_args + [ci]
+    lib.kda_fwd_cp.restype = ci
+    lib.kda_fwd_cp.argtypes = fwd_args[:16] + [ci, vp, sz, vp, ci]
+    lib.kda_fwd_cp_workspace_bytes.restype = sz
+    lib.kda_fwd_cp_workspace_bytes.argtypes = [ci] * 5
+    lib.kda_fwd_cp_segments.restype = ci
+    lib.kda_fwd_cp_segments.argtypes = [ci, ci, ctypes.c_int64]
     lib.kda_fwd_noalloc.restype = ci
     lib.kda_fwd_noalloc.argtypes = fwd_args[:16] + [vp, vp]
     lib.kda_decode_step.restype = ci
@@ -133,17 +140,9 @@ def _check(t, name, dtype=None, device=None):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
-def kda_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, o=None, S_T=None,
-            workspace=None, return_state: bool = True, engine: str = "auto", stream=None,
-            lib=None):
-    """Chunkwise KDA forward (prefill).
-
-    q, k, log_alpha [B, T, H, d_k] or packed [Ttot, H, d_k]; v [.., H, d_v];
-    beta [.., H]; S0 [N, H, d_v, d_k] fp32 or None; cu_seqlens int32 [N+1]
-    (device) or None.  Returns (o, S_T) (S_T None when return_state is False).
-    Output tensors and the workspace are allocated with torch unless given.
-    `lib` selects another build of the library (see load_library).
-    """
+def _fwd_args(q, k, v, log_alpha, beta, S0, cu_seqlens, o, S_T, return_state):
+    """Checks and sizes shared by the forward entry points: (B, T, H, d_k, d_v,
+    N, o, S_T), with o and S_T allocated with torch when not given."""
     dev = q.device
     dt = q.dtype
     _check(q, "q", dt), _check(k, "k", dt, dev), _check(v, "v", dt, dev)
@@ -175,18 +174,66 @@ def kda_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, o=None, S_T=N
     if S_T is None and return_state:
         S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=dev)
     _check(S_T, "S_T", torch.float32, dev)
+    return B, T, H, d_k, d_v, N, o, S_T
+
+
+def kda_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, o=None, S_T=None,
+            workspace=None, return_state: bool = True, engine: str = "auto", stream=None,
+            lib=None):
+    """Chunkwise KDA forward (prefill).
+
+    q, k, log_alpha [B, T, H, d_k] or packed [Ttot, H, d_k]; v [.., H, d_v];
+    beta [.., H]; S0 [N, H, d_v, d_k] fp32 or None; cu_seqlens int32 [N+1]
+    (device) or None.  Returns (o, S_T) (S_T None when return_state is False).
+    Output tensors and the workspace are allocated with torch unless given.
+    `lib` selects another build of the library (see load_library).
+    """
+    B, T, H, d_k, d_v, N, o, S_T = _fwd_args(q, k, v, log_alpha, beta, S0, cu_seqlens, o,
+                                             S_T, return_state)
     lib = lib or load()
     if workspace is None:
         workspace = torch.empty(int(lib.kda_fwd_workspace_bytes(N)), dtype=torch.uint8,
-                                device=dev)
-    _check(workspace, "workspace", None, dev)
+                                device=q.device)
+    _check(workspace, "workspace", None, q.device)
     rc = lib.kda_fwd_engine(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                             _ptr(S0), _ptr(cu_seqlens), B, T, H, d_k, d_v, N,
-                            _dtype_code(dt), _ptr(o), _ptr(S_T), _ptr(workspace),
+                            _dtype_code(q.dtype), _ptr(o), _ptr(S_T), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream),
                             ENGINES[engine])
     if rc != KDA_OK:
         raise KdaError(rc, "kda_fwd")
+    return o, S_T
+
+
+def kda_fwd_cp_workspace_bytes(N: int, H: int, d_k: int, d_v: int, segments: int) -> int:
+    return int(load().kda_fwd_cp_workspace_bytes(N, H, d_k, d_v, segments))
+
+
+def kda_fwd_cp_segments(N: int, H: int, Ttot: int) -> int:
+    return int(load().kda_fwd_cp_segments(N, H, Ttot))
+
+
+def kda_fwd_cp(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, segments=None, o=None,
+               S_T=None, workspace=None, return_state: bool = True, engine: str = "auto",
+               stream=None, lib=None):
+    """Segment-parallel KDA forward on one GPU (same arguments and results as
+    kda_fwd).  `segments` defaults to kda_fwd_cp_segments' choice."""
+    B, T, H, d_k, d_v, N, o, S_T = _fwd_args(q, k, v, log_alpha, beta, S0, cu_seqlens, o,
+                                             S_T, return_state)
+    lib = lib or load()
+    if segments is None:
+        segments = int(lib.kda_fwd_cp_segments(N, H, B * T))
+    if workspace is None:
+        need = int(lib.kda_fwd_cp_workspace_bytes(N, H, d_k, d_v, segments))
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", None, q.device)
+    rc = lib.kda_fwd_cp(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                        _ptr(cu_seqlens), B, T, H, d_k, d_v, N, _dtype_code(q.dtype), _ptr(o),
+                        _ptr(S_T), int(segments), _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), _stream(stream),
+                        ENGINES[engine])
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_fwd_cp")
     return o, S_T
 
 

@@ -104,6 +104,51 @@ def test_fwd_argument_errors(kda):
     assert fwd_call(lib, engine=1, dt=0) == E_UNS                      # tensor cores: bf16 only
 
 
+def cp_call(lib, segments=2, **kw):
+    a = dict(q=P[0], k=P[1], v=P[2], la=P[3], beta=P[4], S0=None, cu=None, B=1, T=64, H=2,
+             dk=64, dv=64, N=1, dt=0, o=P[5], ST=P[6], ws=P[7], wsb=1 << 30, stream=None,
+             engine=0)
+    a.update(kw)
+    return lib.kda_fwd_cp(a["q"], a["k"], a["v"], a["la"], a["beta"], a["S0"], a["cu"],
+                          a["B"], a["T"], a["H"], a["dk"], a["dv"], a["N"], a["dt"], a["o"],
+                          a["ST"], segments, a["ws"], a["wsb"], a["stream"], a["engine"])
+
+
+def test_cp_workspace_bytes(kda):
+    """Segment-parallel workspace: the plain one for one segment; otherwise
+    task tables, a 16 KB zero tile and four [H][d][d] fp32 state sets per later
+    segment of every sequence (S~, M, start state) plus one per sequence."""
+    assert kda.kda_fwd_cp_workspace_bytes(3, 4, 64, 64, 1) == kda.kda_fwd_workspace_bytes(3)
+    for N, H, d, P in [(1, 12, 128, 6), (5, 2, 64, 3), (16, 96, 128, 2)]:
+        b = kda.kda_fwd_cp_workspace_bytes(N, H, d, d, P)
+        states = (N + 3 * N * (P - 1)) * H * d * d * 4
+        assert states + 16384 <= b <= states + 16384 + 64 * N * (3 * P) + 8 * 256
+        assert b % 256 == 0
+    assert kda.kda_fwd_cp_workspace_bytes(1, 1, 64, 128, 2) == 0      # d_k != d_v
+    assert kda.kda_fwd_cp_workspace_bytes(1, 1, 64, 64, 0) == 0
+
+
+def test_cp_argument_errors(kda):
+    lib = kda.load()
+    E_INV, E_UNS, E_WS = 1, 2, 3
+    assert cp_call(lib, segments=0) == E_INV
+    assert cp_call(lib, segments=70000) == E_INV
+    assert cp_call(lib, q=None) == E_INV
+    assert cp_call(lib, dk=96, dv=96) == E_UNS
+    assert cp_call(lib, engine=1, dt=0) == E_UNS
+    assert cp_call(lib, ws=None) == E_WS
+    need = kda.kda_fwd_cp_workspace_bytes(1, 2, 64, 64, 4)
+    assert cp_call(lib, segments=4, wsb=need - 1) == E_WS
+    assert cp_call(lib, N=2) == E_INV                                 # N != B without cu_seqlens
+
+
+def test_cp_segments_without_gpu(kda):
+    """With no device to size against, the suggestion is a plain pass."""
+    assert kda.kda_fwd_cp_segments(1, 12, 131072) >= 1
+    assert kda.kda_fwd_cp_segments(0, 12, 131072) == 1
+    assert kda.kda_fwd_cp_segments(1, 12, 0) == 1
+
+
 def test_decode_argument_errors(kda):
     lib = kda.load()
 

@@ -425,6 +425,110 @@ def test_workload_long_sampled_heads(kda, engine):
     assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(ST).all())
 
 
+# ------------------------------------------------ segment-parallel forward
+
+def run_cp(kda, prob, engine, segments, **kw):
+    o, ST = kda.kda_fwd_cp(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0,
+                           prob.cu_seqlens, segments=segments, engine=engine, **kw)
+    torch.cuda.synchronize()
+    return o, ST
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("segments", [2, 3, 5])
+def test_cp_matches_oracle(kda, engine, dtype, d, segments):
+    """kda_fwd_cp over 2, 3 and 5 segments per sequence (ragged T, nonzero S0,
+    two sequences) against the oracle, at kda_fwd's tolerances."""
+    if not engine_ok(engine, dtype, d):
+        pytest.skip("engine does not take this dtype/size")
+    prob = I.prefill_problem(2, 333, 3, d, d, dtype, (-0.5, -0.001), 0.05, seed=segments + d,
+                             device=DEV)
+    ws = torch.zeros(kda.kda_fwd_cp_workspace_bytes(2, 3, d, d, segments), dtype=torch.uint8,
+                     device=DEV)
+    o, ST = run_cp(kda, prob, engine, segments, workspace=ws)
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2])
+    dt = prob.q.dtype
+    assert rel_err(o, o_ref) < tol_o(dt)
+    assert rel_err(ST, S_ref) < tol_s(dt)
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_cp_varlen_short_empty_in_place(kda, engine):
+    """Packed sequences shorter than the segment count (empty segments act as
+    identity maps), an empty sequence, a ragged tail, S_T written over S0."""
+    lengths = [0, 1, 64, 130, 700, 65]
+    prob = I.prefill_problem(1, 0, 4, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=31,
+                             device=DEV, lengths=lengths)
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2, 3])
+    S = prob.S0.clone()
+    o, _ = kda.kda_fwd_cp(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, S,
+                          prob.cu_seqlens, segments=4, S_T=S, engine=engine)
+    torch.cuda.synchronize()
+    assert rel_err(o, o_ref) < 2e-2
+    assert rel_err(S, S_ref) < 1e-2
+    assert torch.equal(S[0], prob.S0[0])      # the empty sequence passes its state through
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_cp_wide_gates(kda, engine):
+    """Gates past the chunk form's range inside segment-parallel runs: the
+    token-serial path honours the zero-v, identity-start and state-only tasks."""
+    prob = I.prefill_problem(1, 400, 3, 128, 128, "bf16", (-5.0, -0.5), 0.05, seed=41,
+                             device=DEV)
+    o, ST = run_cp(kda, prob, engine, 3)
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2])
+    assert rel_err(o, o_ref) < 2e-2
+    assert rel_err(ST, S_ref) < 1e-2
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_cp_slow_gates_compose(kda, engine):
+    """Slow gates (log alpha in U(-0.01, -0.0001)) over 128-token segments keep
+    each segment's map M far from zero, so the start states come from the scan's
+    composition M S_in + S~ and not from forgetting: 8 segments against the
+    oracle (bf16 on both engines)."""
+    prob = I.prefill_problem(1, 1024, 3, 128, 128, "bf16", (-0.01, -0.0001), 0.05, seed=61,
+                             device=DEV)
+    o, ST = run_cp(kda, prob, engine, 8)
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2])
+    eo, es = rel_err(o, o_ref), rel_err(ST, S_ref)
+    print(f"[parity] cp slow gates {engine}: o {eo:.2e} S {es:.2e}")
+    assert eo < 2e-2
+    assert es < 1e-2
+
+
+def test_cp_fp32_agrees_with_plain(kda):
+    """On the fp32 CUDA-core engine every step of the segment maps and the scan
+    is fp32, so kda_fwd_cp and kda_fwd agree to fp32 rounding; slow gates keep
+    the maps far from zero."""
+    prob = I.prefill_problem(1, 1000, 2, 64, 64, "f32", (-0.01, -0.0001), 0.05, seed=51,
+                             device=DEV)
+    o1, S1 = run_fwd(kda, prob, "cudacore")
+    o2, S2 = run_cp(kda, prob, "cudacore", 6)
+    assert rel_err(o2, o1.double().cpu().numpy()) < 1e-5
+    assert rel_err(S2, S1.double().cpu().numpy()) < 1e-5
+
+
+def test_workload_long_tp8_segment_parallel(kda):
+    """The segment-parallel workload at full size (B=1, H=12, T=131072, nonzero
+    S0, long-memory gates) with the suggested segment count: 3 sampled heads
+    against the oracle."""
+    prob = I.preset_problem("long_tp8", seed=0, device=DEV)
+    P = kda.kda_fwd_cp_segments(1, 12, 131072)
+    assert P > 1
+    o, ST = run_cp(kda, prob, "auto", P)
+    heads = I.sampled_heads(12, 3, seed=0)
+    o_ref, S_ref = oracle_on_heads(prob, heads)
+    idx = torch.tensor(heads, device=DEV)
+    eo, es = rel_err(o.index_select(2, idx), o_ref), rel_err(ST.index_select(1, idx), S_ref)
+    print(f"[parity] long_tp8 segments={P}: o {eo:.2e} S {es:.2e}")
+    assert eo < 2e-2
+    assert es < 1e-2
+
+
 def test_workload_decode_sampled_sessions(kda):
     """64 sessions x 96 heads, fp32 state, 1000 in-place steps: 12 sampled
     (session, head) pairs follow the oracle step by step."""
