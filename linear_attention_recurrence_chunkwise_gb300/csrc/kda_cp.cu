@@ -104,7 +104,7 @@ constexpr int kScanRows = 16;
 template <int D>
 __global__ void __launch_bounds__(kScanThreads) cp_scan_kernel(int N, int P, int H,
                                                                 CpLayout L, uint8_t *ws) {
-    const int32_t *status = reinterpret_cast<const int32_t *>(ws);
+    int32_t *status = reinterpret_cast<int32_t *>(ws);
     if (*status == KDA_ERR_INVALID_ARGUMENT) return;
     extern __shared__ __align__(16) float cp_smem[];
     float *Mbuf = cp_smem;           // two M_j [a][c] buffers
@@ -119,6 +119,12 @@ __global__ void __launch_bounds__(kScanThreads) cp_scan_kernel(int N, int P, int
     const float *mt = reinterpret_cast<const float *>(ws + L.m_t);
     float *sin = reinterpret_cast<float *>(ws + L.s_in);
     auto seg = [&](int j) { return ((size_t)n * (P - 1) + (j - 1)) * blk; };  // segment j's sets
+    // extents for the bounds-checked build: the per-sequence set and the
+    // per-later-segment sets; a block whose rows would leave them does nothing
+    const size_t n_sets = (size_t)N * (P - 1) * blk;
+    if (!in_bounds(status, n * blk + hoff + (size_t)kScanRows * D - 1, (size_t)N * blk) ||
+        (P > 1 && !in_bounds(status, seg(P - 1) + hoff + (size_t)kScanRows * D - 1, n_sets)))
+        return;
     // M_j into buffer (j - 1) % 2; every thread copies the same pieces each time
     auto stage_m = [&](int j) {
         const float *mj = mt + seg(j) + (size_t)h * D * D;

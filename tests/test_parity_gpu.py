@@ -267,6 +267,29 @@ def test_bounds_checked_build(kda, engine):
         assert rel_err(ST, S_ref) < 1e-2
 
 
+@pytest.mark.parametrize("engine", ENGINES)
+def test_bounds_checked_build_segment_parallel(kda, engine):
+    """The bounds-checked build through kda_fwd_cp: task-table addressing of
+    token ranges and state blocks, empty segments, the zero-v tile, wide-gate
+    chunks on the token-serial path -- no report, results match the oracle."""
+    lib = kda.load_library(kbuild.build(bounds_check=True))
+    cases = [(I.prefill_problem(1, 0, 2, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=6,
+                                device=DEV, lengths=[0, 130, 1, 64, 300]), 4),
+             (I.prefill_problem(2, 200, 2, 128, 128, "bf16", (-5.0, -0.5), 0.05, seed=7,
+                                device=DEV), 3)]
+    for prob, P in cases:
+        n = prob.S0.shape[0]
+        ws = torch.zeros(int(lib.kda_fwd_cp_workspace_bytes(n, 2, 128, 128, P)),
+                         dtype=torch.uint8, device=DEV)
+        o, ST = kda.kda_fwd_cp(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0,
+                               prob.cu_seqlens, segments=P, workspace=ws, engine=engine,
+                               lib=lib)
+        assert kda.kda_read_device_status(ws, lib=lib) == kda.KDA_OK
+        o_ref, S_ref = oracle_on_heads(prob, [0, 1])
+        assert rel_err(o, o_ref) < 2e-2
+        assert rel_err(ST, S_ref) < 1e-2
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("K", [1, 4, 8, 11, 16])
