@@ -24,7 +24,11 @@
  *    never allocates, frees or synchronises, except kda_read_device_status,
  *    which synchronises the given stream to read the status word.
  *  - `stream` is a cudaStream_t passed as void*; NULL selects the legacy
- *    default stream.  All work is enqueued asynchronously on it.
+ *    default stream.  All work is enqueued asynchronously on it.  kda_fwd,
+ *    kda_fwd_engine, kda_fwd_cp and kda_decode_step only enqueue kernels, so
+ *    a stream capture records them into a CUDA graph whose replays give the
+ *    same results as eager calls (make one eager call first: it performs the
+ *    one-time host set-up).
  *  - The state is fp32 and laid out [N, H, d_v, d_k] (key channel innermost):
  *    memory element [n][h][v][c] holds the logical S[c][v].  This is the
  *    [batch, heads, value_dim, key_dim] layout "Kimi K3 混合线性注意力" section 3

@@ -267,6 +267,57 @@ def test_bounds_checked_build(kda, engine):
         assert rel_err(ST, S_ref) < 1e-2
 
 
+def test_cuda_graph_capture(kda):
+    """kda_fwd, kda_fwd_cp and kda_decode_step enqueue kernels only (no
+    allocation, no synchronisation), so each can be captured in a CUDA graph;
+    replays reproduce the eager results bit for bit (three replays of the
+    decode step = three in-place steps)."""
+    prob = I.prefill_problem(1, 300, 4, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=71,
+                             device=DEV)
+    o_e, S_e = run_fwd(kda, prob, "auto")
+    oc_e, Sc_e = run_cp(kda, prob, "auto", 3)
+    N, H, d = 6, 4, 128
+    S_dec0 = I.decode_state(N, H, d, d, 0.02, seed=72, device=DEV)
+    x = I.decode_token(N, H, d, d, "bf16", seed=72, step=0, device=DEV)
+    S_eager = S_dec0.clone()
+    for _ in range(3):
+        od_e = kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S_eager)
+    torch.cuda.synchronize()
+
+    o, ST = torch.empty_like(o_e), torch.empty_like(S_e)
+    oc, STc = torch.empty_like(o_e), torch.empty_like(S_e)
+    ws = torch.zeros(kda.kda_fwd_workspace_bytes(1), dtype=torch.uint8, device=DEV)
+    wsc = torch.zeros(kda.kda_fwd_cp_workspace_bytes(1, 4, 128, 128, 3), dtype=torch.uint8,
+                      device=DEV)
+    S_dec, od = S_dec0.clone(), torch.empty_like(od_e)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # first calls outside capture (one-time host set-up)
+        kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0, o=o, S_T=ST,
+                    workspace=ws)
+        kda.kda_fwd_cp(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0, segments=3,
+                       o=oc, S_T=STc, workspace=wsc)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g_fwd, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_fwd):
+        kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0, o=o, S_T=ST,
+                    workspace=ws)
+        kda.kda_fwd_cp(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0, segments=3,
+                       o=oc, S_T=STc, workspace=wsc)
+    with torch.cuda.graph(g_dec):
+        kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S_dec, o=od)
+    o.zero_(), ST.zero_(), oc.zero_(), STc.zero_()
+    torch.cuda.synchronize()
+    g_fwd.replay()
+    for _ in range(3):
+        g_dec.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_e) and torch.equal(ST, S_e)
+    assert torch.equal(oc, oc_e) and torch.equal(STc, Sc_e)
+    assert torch.equal(S_dec, S_eager) and torch.equal(od, od_e)
+
+
 @pytest.mark.parametrize("engine", ENGINES)
 def test_bounds_checked_build_segment_parallel(kda, engine):
     """The bounds-checked build through kda_fwd_cp: task-table addressing of
