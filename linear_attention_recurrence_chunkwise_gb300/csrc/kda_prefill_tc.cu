@@ -418,11 +418,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto gate_scan = [&](int m, int cg, float (&g)[2][16]) {
             const int validm = min(C, len - m * C);
             read_gates(sm.gt, lane, fl, cg, g);
+            if (validm == C) {
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const bool live = 2 * lane + (i ^ fl) < validm;  // the tile runs past the sequence end
+                for (int i = 0; i < 2; ++i)
 #pragma unroll
-                for (int e = 0; e < 16; ++e) g[i][e] = live ? g[i][e] * kLog2e : 0.f;
+                    for (int e = 0; e < 16; ++e) g[i][e] *= kLog2e;
+            } else {  // the tile runs past the sequence end
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const bool live = 2 * lane + (i ^ fl) < validm;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) g[i][e] = live ? g[i][e] * kLog2e : 0.f;
+                }
             }
             float inc[16];
 #pragma unroll
@@ -435,15 +442,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane >= o) inc[e] += up;
                 }
             }
+            // slot i holds token 2 l + (i ^ fl): the odd token's G2 is the
+            // inclusive sum, the even token's that minus the odd token's
+            // log-decay -- as weights (one of fl, 1 - fl is 0) instead of
+            // selects, with the same single rounding
+            const float wf = fl ? 1.f : 0.f, wn = 1.f - wf;
             float lo = 0.f, hi = 0.f;
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-                const float x1 = fl ? g[0][e] : g[1][e];  // log-decay of token 2 l + 1
-                const float ge = inc[e] - x1;              // G2 at token 2 l
-                g[0][e] = fl ? inc[e] : ge;
-                g[1][e] = fl ? ge : inc[e];
-                lo = fminf(lo, fminf(g[0][e], g[1][e]));
-                hi = fmaxf(hi, fmaxf(g[0][e], g[1][e]));
+                const float s0 = fmaf(-wn, g[1][e], inc[e]);  // slot 0
+                const float s1 = fmaf(-wf, g[0][e], inc[e]);  // slot 1
+                g[0][e] = s0;
+                g[1][e] = s1;
+                // with log-decay <= 0 the odd token's G2 (the inclusive sum) is
+                // the lower of the pair
+                lo = fminf(lo, inc[e]);
+                hi = fmaxf(hi, inc[e]);
             }
             // a chunk outside the chunk form's range sends the whole (sequence,
             // head) to the token-serial pass after teardown
@@ -491,9 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_phase_warp(sm.full[s], (n >> 1) & 1, abort);
             // Kb, M and gamma of chunk n - 2 (same slot) are no longer read by the carry
             if (n >= 2) wait_phase_warp(sm.tailfree[s], ((n >> 1) - 1) & 1, abort);
-            if (lane == 31)  // token 63 closes the chunk (lane 31 keeps it in slot 0)
+            // token 63 closes the chunk (lane 31 keeps it in slot 0); the same
+            // ex2 as the operands' Gamma (an accurate exp2f here serialised the
+            // warp on one lane)
+            if (lane == 31)
 #pragma unroll
-                for (int e = 0; e < 16; ++e) S.gam[c0 + e] = exp2f(g[0][e]);
+                for (int e = 0; e < 16; ++e) S.gam[c0 + e] = ex2_approx(g[0][e]);
             if (pt < C) S.bet[pt] = bet;
 
             // a2: scaled operands, written over the landed tiles (same swizzle)
@@ -560,10 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                __uint_as_float(x[4 * j4 + 2]), __uint_as_float(x[4 * j4 + 3]));
                         mul2(w.x, w.y, br, br);
                         mul2(w.z, w.w, br, br);
-                        w.x = j + 0 < r ? w.x : 0.f;
-                        w.y = j + 1 < r ? w.y : 0.f;
-                        w.z = j + 2 < r ? w.z : 0.f;
-                        w.w = j + 3 < r ? w.w : 0.f;
+                        // stored as tf32 (the solve's operand precision, so it
+                        // converts nothing); entries on and above the diagonal
+                        // are never read by the solve, which overwrites them
+                        w = make_float4(__uint_as_float(to_tf32(w.x)), __uint_as_float(to_tf32(w.y)),
+                                        __uint_as_float(to_tf32(w.z)), __uint_as_float(to_tf32(w.w)));
                         *reinterpret_cast<float4 *>(&sm.as[r * LDA + j]) = w;
                     }
                 } else {  // M[r][j] = R[64 + r][j], j <= r

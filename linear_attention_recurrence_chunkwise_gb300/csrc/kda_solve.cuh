@@ -52,16 +52,16 @@ __device__ __forceinline__ void mma_xt(float (&p)[2][4], const float *tl, const 
     constexpr int ld = kSolveLd;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        uint32_t a[4];  // A operand = T_LJ^T: element (m, k) = T_LJ[k][m]
-        a[0] = to_tf32(tl[(8 * ks + t) * ld + g]);
-        a[1] = to_tf32(tl[(8 * ks + t) * ld + g + 8]);
-        a[2] = to_tf32(tl[(8 * ks + t + 4) * ld + g]);
-        a[3] = to_tf32(tl[(8 * ks + t + 4) * ld + g + 8]);
+        uint32_t a[4];  // A operand = T_LJ^T: element (m, k) = T_LJ[k][m] (stored as tf32)
+        a[0] = __float_as_uint(tl[(8 * ks + t) * ld + g]);
+        a[1] = __float_as_uint(tl[(8 * ks + t) * ld + g + 8]);
+        a[2] = __float_as_uint(tl[(8 * ks + t + 4) * ld + g]);
+        a[3] = __float_as_uint(tl[(8 * ks + t + 4) * ld + g + 8]);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {  // B operand = A_KL^T: (k, n) = A_KL[n][k]
-            uint32_t b[2];
-            b[0] = to_tf32(ak[(8 * nt + g) * ld + 8 * ks + t]);
-            b[1] = to_tf32(ak[(8 * nt + g) * ld + 8 * ks + t + 4]);
+            uint32_t b[2];  // (A is stored as tf32)
+            b[0] = __float_as_uint(ak[(8 * nt + g) * ld + 8 * ks + t]);
+            b[1] = __float_as_uint(ak[(8 * nt + g) * ld + 8 * ks + t + 4]);
             mma_tf32_16x8x8(p[nt], a, b);
         }
     }
@@ -81,11 +81,11 @@ __device__ __forceinline__ void mma_tx(float (&z)[2][4], const float *tk, const 
     for (int ks = 0; ks < 2; ++ks) {
         const float2 r0 = *reinterpret_cast<const float2 *>(tk + g * ld + 8 * ks + 2 * t);
         const float2 r1 = *reinterpret_cast<const float2 *>(tk + (g + 8) * ld + 8 * ks + 2 * t);
-        uint32_t a[4];
-        a[0] = to_tf32(r0.x);
-        a[1] = to_tf32(r1.x);
-        a[2] = to_tf32(r0.y);
-        a[3] = to_tf32(r1.y);
+        uint32_t a[4];  // T_IK, stored as tf32
+        a[0] = __float_as_uint(r0.x);
+        a[1] = __float_as_uint(r1.x);
+        a[2] = __float_as_uint(r0.y);
+        a[3] = __float_as_uint(r1.y);
 #pragma unroll
         for (int nz = 0; nz < 2; ++nz) {
             uint32_t b[2];
@@ -126,8 +126,10 @@ __device__ __forceinline__ void store_tprime(uint8_t *tp, const float *beta, int
     }
 }
 
-// On entry `as` (fp32, row stride kSolveLd) holds A, zero on and above the
-// diagonal, and beta[64] the token weights.  On exit `tp` holds T' (bf16,
+// On entry `as` (fp32 values rounded to tf32, row stride kSolveLd) holds A
+// strictly below the diagonal (what lies on and above it is never read), and
+// beta[64] the token weights.  The blocks of T it writes back for later steps
+// are rounded to tf32 too: they are read only as tensor-core operands.  On exit `tp` holds T' (bf16,
 // [r][j], 128-byte swizzle) and `as` is scratch.  Called by the 128 threads
 // (pt = 0 .. 127) of four warps, which synchronise among themselves on the
 // named barrier `bar`.  The caller makes the tile visible to the tensor cores
@@ -173,8 +175,9 @@ __device__ __forceinline__ void solve_tprime64(float *as, const float *beta, uin
             }
         }
         __syncwarp();
+        // T_bb is read back only as a tensor-core operand: stored as tf32
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Ab[r * ld + c] = x[r];
+        for (int r = 0; r < 16; ++r) Ab[r * ld + c] = __uint_as_float(to_tf32(x[r]));
         const float bc = beta[16 * b + c];
 #pragma unroll
         for (int r = 0; r < 16; ++r)
@@ -192,10 +195,11 @@ __device__ __forceinline__ void solve_tprime64(float *as, const float *beta, uin
         float *dst = t_block(as, bi, bj);
 #pragma unroll
         for (int nz = 0; nz < 2; ++nz) {
+            // (read back only as a tensor-core operand: stored as tf32)
             *reinterpret_cast<float2 *>(dst + g * ld + 8 * nz + 2 * t) =
-                make_float2(-z[nz][0], -z[nz][1]);
+                make_float2(__uint_as_float(to_tf32(-z[nz][0])), __uint_as_float(to_tf32(-z[nz][1])));
             *reinterpret_cast<float2 *>(dst + (g + 8) * ld + 8 * nz + 2 * t) =
-                make_float2(-z[nz][2], -z[nz][3]);
+                make_float2(__uint_as_float(to_tf32(-z[nz][2])), __uint_as_float(to_tf32(-z[nz][3])));
         }
         store_tprime(tp, beta, bi, bj, z, lane);
     }
