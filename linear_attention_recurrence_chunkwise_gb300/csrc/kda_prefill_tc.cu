@@ -653,14 +653,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int valid = min(C, len - n * C);
             uint8_t *stage = sm.ut + (v >> 6) * 8192;
             const int vc = v & 63;
+            // this column's byte offset in a row r of the swizzled tile depends
+            // on r only through r % 8: eight bases, then constant offsets
+            uint8_t *base[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) base[k] = stage + sw128_offset(k, vc) - k * 128;
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t x[32];
                 tmem_ld32(tmem + lane_addr + kColO + 32 * cb, x);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    *reinterpret_cast<__nv_bfloat16 *>(stage + sw128_offset(32 * cb + j, vc)) =
+                for (int j = 0; j < 32; ++j) {
+                    const int r = 32 * cb + j;
+                    *reinterpret_cast<__nv_bfloat16 *>(base[r & 7] + (r >> 3) * 1024 + (r & 7) * 128) =
                         __float2bfloat16_rn(__uint_as_float(x[j]));
+                }
             }
             tc_fence_before();
             fence_proxy_async_smem();
@@ -714,10 +721,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cb = 0; cb < 2; ++cb) {
                 uint32_t x[32];
                 tmem_ld32(tmem + lane_addr + kColW + 32 * cb, x);
-                float f[32];
+                // packed to bf16 pairs, then negated by flipping both sign bits
+                uint8_t *tile = S.kq + (v >> 6) * 16384;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) f[j] = -__uint_as_float(x[j]);
-                store_row<32>(S.kq + (v >> 6) * 16384, v & 63, 32 * cb, f);
+                for (int j = 0; j < 32; j += 8) {
+                    uint4 w;
+                    w.x = pack_bf16(__uint_as_float(x[j]), __uint_as_float(x[j + 1])) ^ 0x80008000u;
+                    w.y = pack_bf16(__uint_as_float(x[j + 2]), __uint_as_float(x[j + 3])) ^ 0x80008000u;
+                    w.z = pack_bf16(__uint_as_float(x[j + 4]), __uint_as_float(x[j + 5])) ^ 0x80008000u;
+                    w.w = pack_bf16(__uint_as_float(x[j + 6]), __uint_as_float(x[j + 7])) ^ 0x80008000u;
+                    *reinterpret_cast<uint4 *>(tile + sw128_offset(v & 63, 32 * cb + j)) = w;
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
