@@ -59,6 +59,13 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
     return __float2bfloat16_rn(x);
 }
 
+// 2^x by the MUFU ex2 (about 2 ulp; alpha = 2^(log_alpha log2 e))
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t tf32_bits(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(2 * D, 2) draft_kernel(
                     kv = to_f(k[gi]);
                     if (!kCommit) qv = to_f(q[gi]);
                 }
-                a[t] = live ? expf(la) : 1.f;
+                a[t] = live ? ex2_fast(la * 1.4426950408889634f) : 1.f;
                 kk[t] = live ? kv : 0.f;
                 qq[t] = live ? qv : 0.f;
             }
