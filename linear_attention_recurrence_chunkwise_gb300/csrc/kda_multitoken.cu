@@ -39,7 +39,9 @@
 // instead of t, t + 4, the same registers are the A fragments of m16n8k8
 // products, so the 2 n dot products of a row are tensor-core products of the
 // state with the decayed keys and queries -- fp32 accuracy from three tf32
-// products per tile (high x high, high x low, low x high).  The solve and the
+// products per tile (high x high, high x low, low x high), except in a bf16
+// verify, which only reads the state and rounds its outputs to bf16: one tf32
+// product per tile there.  The solve and the
 // state update stay in fp32 on the CUDA cores (the update adds into the same
 // registers, round to nearest).
 #include <cuda_bf16.h>
@@ -175,6 +177,10 @@ __global__ void __launch_bounds__(2 * D, 2) draft_kernel(
     int tokens_aligned) {
     constexpr int kNT = D / 8;  // 8-channel slices of a row
     constexpr int kThreads = 2 * D;
+    // verify with bf16 outputs (the state only read): one tf32 product per
+    // dot; its 2^-11 operand rounding sits under the outputs' bf16 rounding.
+    // Everything that updates the state keeps the three-product fp32 form.
+    constexpr bool kOneTf32 = !kCommit && sizeof(Tin) == 2;
     extern __shared__ __align__(16) uint8_t draft_smem[];
     DraftSmem<D, Tin> &sm = *reinterpret_cast<DraftSmem<D, Tin> *>(draft_smem);
     // the next pair's state, landed by cp.async while this pair is worked on;
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(2 * D, 2) draft_kernel(
                     uint32_t hi, lo;
                     split_tf32(kk[t] * run, hi, lo);
                     sm.xk[0][t][c] = __uint_as_float(hi);
-                    sm.xk[1][t][c] = __uint_as_float(lo);
+                    if (!kOneTf32) sm.xk[1][t][c] = __uint_as_float(lo);
                 }
             } else {
                 float run = 1.f;
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(2 * D, 2) draft_kernel(
                         uint32_t hi, lo;
                         split_tf32(qq[t] * run, hi, lo);
                         sm.xq[0][t][c] = __uint_as_float(hi);
-                        sm.xq[1][t][c] = __uint_as_float(lo);
+                        if (!kOneTf32) sm.xq[1][t][c] = __uint_as_float(lo);
                     }
                 }
                 if (update) {
@@ -365,17 +371,27 @@ __global__ void __launch_bounds__(2 * D, 2) draft_kernel(
             float cp3[3][4] = {}, cq3[3][4] = {};
 #pragma unroll
             for (int i = 0; i < kNT; ++i) {
-                uint32_t ah[4], al[4];
-                split_tf32(sa[i].x, ah[0], al[0]);
-                split_tf32(sb[i].x, ah[1], al[1]);
-                split_tf32(sa[i].y, ah[2], al[2]);
-                split_tf32(sb[i].y, ah[3], al[3]);
                 const int col = 8 * i + 2 * tg;  // B fragment: token g, channels col, col + 1
-                mma_3xtf32(cp3, ah, al, *reinterpret_cast<const float2 *>(&sm.xk[0][g][col]),
-                           *reinterpret_cast<const float2 *>(&sm.xk[1][g][col]));
-                if (!kCommit)
-                    mma_3xtf32(cq3, ah, al, *reinterpret_cast<const float2 *>(&sm.xq[0][g][col]),
-                               *reinterpret_cast<const float2 *>(&sm.xq[1][g][col]));
+                if constexpr (kOneTf32) {
+                    const uint32_t ah[4] = {tf32_bits(sa[i].x), tf32_bits(sb[i].x),
+                                            tf32_bits(sa[i].y), tf32_bits(sb[i].y)};
+                    const float2 bk = *reinterpret_cast<const float2 *>(&sm.xk[0][g][col]);
+                    const float2 bq = *reinterpret_cast<const float2 *>(&sm.xq[0][g][col]);
+                    mma_tf32(cp3[0], ah, __float_as_uint(bk.x), __float_as_uint(bk.y));
+                    mma_tf32(cq3[0], ah, __float_as_uint(bq.x), __float_as_uint(bq.y));
+                } else {
+                    uint32_t ah[4], al[4];
+                    split_tf32(sa[i].x, ah[0], al[0]);
+                    split_tf32(sb[i].x, ah[1], al[1]);
+                    split_tf32(sa[i].y, ah[2], al[2]);
+                    split_tf32(sb[i].y, ah[3], al[3]);
+                    mma_3xtf32(cp3, ah, al, *reinterpret_cast<const float2 *>(&sm.xk[0][g][col]),
+                               *reinterpret_cast<const float2 *>(&sm.xk[1][g][col]));
+                    if (!kCommit)
+                        mma_3xtf32(cq3, ah, al,
+                                   *reinterpret_cast<const float2 *>(&sm.xq[0][g][col]),
+                                   *reinterpret_cast<const float2 *>(&sm.xq[1][g][col]));
+                }
             }
             float cp[4], cq[4];
 #pragma unroll
