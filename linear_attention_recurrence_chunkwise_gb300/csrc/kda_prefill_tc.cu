@@ -551,14 +551,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (pt == 0) {
                 tc_fence_after();
                 const uint32_t id = idesc_bf16(128, 64, false, false);
+                // one descriptor per operand; the k-th slice adds its byte offset
+                // / 16 to the start-address field (no carry: shared addresses
+                // stay far below 2^18)
+                const uint64_t a0 = desc_sw128(smem_u32(S.kq), 16, 1024);
+                const uint64_t b0 = desc_sw128(smem_u32(S.kb), 16, 1024);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t a =
-                        desc_sw128(smem_u32(S.kq) + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-                    const uint64_t b =
-                        desc_sw128(smem_u32(S.kb) + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
-                    mma_bf16(tmem + kColR, a, b, id, k > 0);
-                }
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16(tmem + kColR, a0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2),
+                             b0 + (uint64_t)((k >> 2) * 512 + (k & 3) * 2), id, k > 0);
                 mma_commit(smem_u32(&sm.bar_r));
             }
             wait_phase_warp(sm.bar_r, n & 1, abort);
@@ -702,13 +703,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wait_phase(sm.tpfull, n & 1, abort);
                 tc_fence_after();
                 const uint32_t id = idesc_bf16(128, 64, true, false);
+                // (per slice k: the byte offset / 16 added to the start-address field)
+                const uint64_t aw0 = desc_sw128(smem_u32(S.kq), 16384, 1024);
+                const uint64_t av0 = desc_sw128(smem_u32(S.v), 8192, 1024);
+                const uint64_t b0 = desc_sw128(smem_u32(sm.tp), 16, 1024);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const uint64_t aw = desc_sw128(smem_u32(S.kq) + k * 2048, 16384, 1024);
-                    const uint64_t av = desc_sw128(smem_u32(S.v) + k * 2048, 8192, 1024);
-                    const uint64_t b = desc_sw128(smem_u32(sm.tp) + k * 32, 16, 1024);
-                    mma_bf16(tmem + kColW, aw, b, id, k > 0);
-                    mma_bf16(tmem + kColU, av, b, id, k > 0);
+                    const uint64_t b = b0 + (uint64_t)(2 * k);
+                    mma_bf16(tmem + kColW, aw0 + (uint64_t)(128 * k), b, id, k > 0);
+                    mma_bf16(tmem + kColU, av0 + (uint64_t)(128 * k), b, id, k > 0);
                 }
                 mma_commit(smem_u32(&sm.ready[s]));
             }
@@ -739,12 +742,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (issuer) {  // U^T += S^T (-W)^T, S^T read from tensor memory
                 tc_fence_after();
                 const uint32_t id_u = idesc_bf16(128, 64, false, true);
+                const uint64_t bw0 = desc_sw128(smem_u32(S.kq), 8192, 1024);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t bw =
-                        desc_sw128(smem_u32(S.kq) + (k >> 2) * 16384 + (k & 3) * 2048, 8192, 1024);
-                    mma_bf16_tmem_a(tmem + kColU, tmem + kColSb + 8 * k, bw, id_u, 1);
-                }
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16_tmem_a(tmem + kColU, tmem + kColSb + 8 * k,
+                                    bw0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 128), id_u, 1);
                 mma_commit(smem_u32(&sm.bar_u));
             }
             __syncwarp();
@@ -752,12 +754,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (issuer) {  // O^T = S^T Qh^T
                 tc_fence_after();
                 const uint32_t id_o = idesc_bf16(128, 64, false, false);
+                const uint64_t bq0 = desc_sw128(smem_u32(S.kq) + 8192, 16, 1024);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t bq = desc_sw128(
-                        smem_u32(S.kq) + 8192 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-                    mma_bf16_tmem_a(tmem + kColO, tmem + kColSb + 8 * k, bq, id_o, k > 0);
-                }
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16_tmem_a(tmem + kColO, tmem + kColSb + 8 * k,
+                                    bq0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2), id_o, k > 0);
                 mma_commit(smem_u32(&sm.bar_o));
             }
             __syncwarp();
@@ -784,13 +785,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t id_o = idesc_bf16(128, 64, false, false);
                 const uint32_t id_s = idesc_bf16(128, 128, false, true);
+                const uint64_t bm0 = desc_sw128(smem_u32(S.m), 16, 1024);
+                const uint64_t bk0 = desc_sw128(smem_u32(S.kb), 8192, 1024);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint32_t a = tmem + kColU + 8 * k;
-                    const uint64_t bm = desc_sw128(smem_u32(S.m) + k * 32, 16, 1024);
-                    const uint64_t bk = desc_sw128(smem_u32(S.kb) + k * 2048, 8192, 1024);
-                    mma_bf16_tmem_a(tmem + kColO, a, bm, id_o, 1);
-                    mma_bf16_tmem_a(tmem + kColS, a, bk, id_s, 1);
+                    mma_bf16_tmem_a(tmem + kColO, a, bm0 + (uint64_t)(2 * k), id_o, 1);
+                    mma_bf16_tmem_a(tmem + kColS, a, bk0 + (uint64_t)(128 * k), id_s, 1);
                 }
                 mma_commit(smem_u32(&sm.bar_s));
                 // the U and O products (the last readers of the q / k / v tiles of
