@@ -546,6 +546,27 @@ def test_cp_varlen_short_empty_in_place(kda, engine):
     assert torch.equal(S[0], prob.S0[0])      # the empty sequence passes its state through
 
 
+def test_cp_edge_sizes(kda):
+    """kda_fwd_cp on degenerate sizes: no sequences, sequences of zero tokens,
+    and more segments than chunks (every sequence shorter than the split)."""
+    e = torch.empty(0, 2, 64, device=DEV)
+    o, ST = kda.kda_fwd_cp(e, e, e, e, torch.empty(0, 2, device=DEV), None,
+                           torch.zeros(1, dtype=torch.int32, device=DEV), segments=3)
+    torch.cuda.synchronize()
+    assert o.numel() == 0 and ST.shape == (0, 2, 64, 64)
+    prob = I.prefill_problem(1, 0, 2, 64, 64, "f32", (-0.5, -0.001), 0.05, seed=81,
+                             device=DEV, lengths=[0, 0, 3])
+    o, ST = run_cp(kda, prob, "cudacore", 7)
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1])
+    assert rel_err(o, o_ref) < 1e-4 and rel_err(ST, S_ref) < 1e-4
+    assert torch.equal(ST[:2], prob.S0[:2])
+    prob = I.prefill_problem(2, 100, 2, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=82,
+                             device=DEV)
+    o, ST = run_cp(kda, prob, "tensorcore", 16)     # 2 chunks per sequence, 16 segments
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1])
+    assert rel_err(o, o_ref) < 2e-2 and rel_err(ST, S_ref) < 1e-2
+
+
 @pytest.mark.parametrize("engine", ENGINES)
 def test_cp_wide_gates(kda, engine):
     """Gates past the chunk form's range inside segment-parallel runs: the
