@@ -794,11 +794,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16_tmem_a(tmem + kColS, a, bk0 + (uint64_t)(128 * k), id_s, 1);
                 }
                 mma_commit(smem_u32(&sm.bar_s));
+            } else if (et == 32 && n + 2 < nchunks) {
                 // the U and O products (the last readers of the q / k / v tiles of
                 // this slot) are done: refill it with chunk n + 2 while the carry
-                // finishes chunk n
+                // finishes chunk n (from a second warp, so that the copies go
+                // out while the products above are being issued)
                 wait_phase(sm.bar_o, n & 1, abort);
-                if (n + 2 < nchunks) load_stage(n + 2);
+                load_stage(n + 2);
             }
             __syncwarp();
             wait_phase_warp(sm.bar_s, n & 1, abort);

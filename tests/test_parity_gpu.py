@@ -34,6 +34,14 @@ def engine_ok(engine, dtype, d):
     return engine != "tensorcore" or (dtype == "bf16" and d == 128)
 
 
+def assert_engine_rejects(kda, call):
+    """The tensor-core engine asked for a dtype or head size it does not take:
+    the call returns KDA_ERR_UNSUPPORTED before any launch."""
+    with pytest.raises(kda.KdaError) as e:
+        call()
+    assert e.value.status == kda.KDA_ERR_UNSUPPORTED
+
+
 def run_fwd(kda, prob, engine, **kw):
     o, ST = kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0,
                         prob.cu_seqlens, engine=engine, **kw)
@@ -48,10 +56,10 @@ def run_fwd(kda, prob, engine, **kw):
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 333])
 def test_prefill_small(kda, engine, dtype, d, T):
-    if not engine_ok(engine, dtype, d):
-        pytest.skip("engine does not take this dtype/size")
     prob = I.prefill_problem(2, T, 3, d, d, dtype, (-0.5, -0.001), 0.05, seed=T + d,
                              device=DEV)
+    if not engine_ok(engine, dtype, d):
+        return assert_engine_rejects(kda, lambda: run_fwd(kda, prob, engine))
     o, ST = run_fwd(kda, prob, engine)
     o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2])
     dt = prob.q.dtype
@@ -168,11 +176,11 @@ def test_wide_gate_domain(kda, engine, dtype, d, T):
     """Per-token log-decay down to -5 (the K3 bound: -320 over a 64-token chunk,
     far outside the chunk form's +-80) is exact: such chunks are taken token by
     token, and the status word stays clear."""
-    if not engine_ok(engine, dtype, d):
-        pytest.skip("engine does not take this dtype/size")
     prob = I.prefill_problem(2, T, 3, d, d, dtype, (-5.0, -0.5), 0.05, seed=T + d + 11,
                              device=DEV)
     ws = torch.zeros(kda.kda_fwd_workspace_bytes(2), dtype=torch.uint8, device=DEV)
+    if not engine_ok(engine, dtype, d):
+        return assert_engine_rejects(kda, lambda: run_fwd(kda, prob, engine, workspace=ws))
     o, ST = run_fwd(kda, prob, engine, workspace=ws)
     assert kda.kda_read_device_status(ws) == kda.KDA_OK
     o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2])
@@ -458,9 +466,9 @@ def test_decode_small(kda, dtype, d):
 @pytest.mark.parametrize("engine", ENGINES)
 def test_workload_tiny_fp32(kda, engine):
     """B=1, H=2, T=256, d=64, fp32: every element against the oracle at 1e-4."""
-    if not engine_ok(engine, "f32", 64):
-        pytest.skip("tensor-core engine takes bf16, d = 128 only")
     prob = I.preset_problem("tiny", seed=0, device=DEV)
+    if not engine_ok(engine, "f32", 64):
+        return assert_engine_rejects(kda, lambda: run_fwd(kda, prob, engine))
     o, ST = run_fwd(kda, prob, engine)
     o_ref, S_ref = oracle_on_heads(prob, [0, 1])
     eo, es = rel_err(o, o_ref), rel_err(ST, S_ref)
@@ -515,12 +523,13 @@ def run_cp(kda, prob, engine, segments, **kw):
 def test_cp_matches_oracle(kda, engine, dtype, d, segments):
     """kda_fwd_cp over 2, 3 and 5 segments per sequence (ragged T, nonzero S0,
     two sequences) against the oracle, at kda_fwd's tolerances."""
-    if not engine_ok(engine, dtype, d):
-        pytest.skip("engine does not take this dtype/size")
     prob = I.prefill_problem(2, 333, 3, d, d, dtype, (-0.5, -0.001), 0.05, seed=segments + d,
                              device=DEV)
     ws = torch.zeros(kda.kda_fwd_cp_workspace_bytes(2, 3, d, d, segments), dtype=torch.uint8,
                      device=DEV)
+    if not engine_ok(engine, dtype, d):
+        return assert_engine_rejects(kda, lambda: run_cp(kda, prob, engine, segments,
+                                                         workspace=ws))
     o, ST = run_cp(kda, prob, engine, segments, workspace=ws)
     assert kda.kda_read_device_status(ws) == kda.KDA_OK
     o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2])
