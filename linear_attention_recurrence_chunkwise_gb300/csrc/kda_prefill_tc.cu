@@ -35,12 +35,13 @@
 //   warps 8-11  the serial carry of chunk n (a6): the W / U~ MMAs, -W out of
 //               tensor memory into the operand tile, the U, O and S MMAs, the
 //               gamma scaling of the state, and the output, staged in shared
-//               memory and written with a TMA store.  Their MMA-issuing thread
-//               also refills the q/k/v stage a chunk has just released (TMA, 64
-//               tokens x 64 channels per box, 128-byte swizzle).  Issuing an MMA
-//               keeps a thread busy for about as long as the MMA runs, so the
-//               W / U~ products are issued here, where the carry would otherwise
-//               wait for the chunk-local warps.
+//               memory and written with a TMA store.  One thread of the second
+//               carry warp refills the q/k/v stage a chunk has just released
+//               (TMA, 64 tokens x 64 channels per box, 128-byte swizzle) while
+//               the MMA-issuing thread of the first sends the S update.
+//               Issuing an MMA keeps a thread busy for about as long as the MMA
+//               runs, so the W / U~ products are issued here, where the carry
+//               would otherwise wait for the chunk-local warps.
 // The chunk-local work of the next chunk overlaps the carry of the current one.
 //
 // Every wait is bounded in time; on a timeout the kernel records
