@@ -725,3 +725,84 @@ def test_workload_varlen_then_decode(kda, engine):
     print(f"[parity] varlen decode {engine}: worst o {worst:.2e} S after 256 steps {es:.2e}")
     assert worst < 2e-2
     assert es < 1e-2
+
+
+# ------------------------- closed form at full size: every token of every head
+#
+# With q_t = k_t and beta_t = 1 the output reads back the token's own value,
+# for any gates and any initial state: after the decay, r = S~^T k_t, and
+# S_t^T k_t = r + (v_t - r)(k_t^T k_t) = v_t when |k_t| = 1 ("Kimi Delta
+# Attention 完全拆解", section 从线性注意力到 Delta Rule: with a unit key and
+# beta = 1 the erase removes the state's whole component along k_t before the
+# write).  The keys are
+# unit vectors rounded to the input dtype, so o_t = v_t up to that rounding
+# times |v_t - r| and the kernels' own rounding.  Unlike the oracle
+# comparisons, which sample heads, these check every output of a full-size call.
+
+def read_back_err(o, v):
+    o, v = o.float(), v.float()
+    return ((o - v).abs().max() / v.abs().max()).item()
+
+
+def unit_beta(prob):
+    prob.q = prob.k.clone()
+    prob.beta = torch.ones_like(prob.beta)
+    return prob
+
+
+@pytest.mark.parametrize("engine,dtype", [("tensorcore", "bf16"), ("cudacore", "bf16"),
+                                          ("cudacore", "f32")])
+def test_workload_prefill_every_output_reads_back_v(kda, engine, dtype):
+    """B=1, H=96, T=8192, d=128, nonzero S0: o_t = v_t on all 786,432 token-heads."""
+    p = I.PRESETS["prefill"]
+    prob = unit_beta(I.prefill_problem(1, p["T"], p["H"], p["d"], p["d"], dtype, p["la"], 0.02,
+                                       seed=7, device=DEV))
+    o, ST = run_fwd(kda, prob, engine)
+    err = read_back_err(o, prob.v)
+    print(f"[closed form] prefill {engine} {dtype}: max |o - v| / max |v| = {err:.2e}")
+    assert err < tol_o(prob.q.dtype)
+    assert bool(torch.isfinite(ST).all())
+
+
+def test_workload_long_tp8_segment_parallel_reads_back_v(kda):
+    """B=1, H=12, T=131072 through kda_fwd_cp (the automatic segment count):
+    o_t = v_t on every token, across every segment boundary the scan composes."""
+    prob = unit_beta(I.preset_problem("long_tp8", seed=8, device=DEV))
+    o, ST = run_cp(kda, prob, "auto", None)
+    err = read_back_err(o, prob.v)
+    print(f"[closed form] segment-parallel long_tp8: {err:.2e}")
+    assert err < 2e-2
+    assert bool(torch.isfinite(ST).all())
+
+
+def test_workload_decode_and_draft_read_back_v(kda):
+    """64 sessions x 96 heads, fp32 state: three decode steps, then a verify of
+    8 draft tokens and their commit, all with q = k and beta = 1: every output
+    of every session and head is its own v."""
+    p = I.PRESETS["decode"]
+    N, H, d = p["N"], p["H"], p["d"]
+    S = I.decode_state(N, H, d, d, p["s0_std"], seed=9, device=DEV)
+    for s in range(3):
+        x = I.decode_token(N, H, d, d, p["dtype"], p["la"], seed=9, step=s, device=DEV)
+        o = kda.kda_decode_step(x["k"], x["k"], x["v"], x["log_alpha"],
+                                torch.ones_like(x["beta"]), S)
+        torch.cuda.synchronize()
+        err = read_back_err(o, x["v"])
+        print(f"[closed form] decode step {s}: {err:.2e}")
+        assert err < 2e-2
+    K = I.PRESETS["draft"]["K"]
+    x = I.draft_tokens(N, K, H, d, d, p["dtype"], p["la"], seed=10, device=DEV)
+    ins = (x["k"], x["k"], x["v"], x["log_alpha"], torch.ones_like(x["beta"]))
+    o = kda.kda_verify_tokens(*ins, S)
+    kda.kda_commit_tokens(*ins, S)
+    torch.cuda.synchronize()
+    err = read_back_err(o, x["v"])
+    print(f"[closed form] verify of {K} draft tokens: {err:.2e}")
+    assert err < 2e-2
+    # after the commit, one more step reads back too (the committed state is a
+    # valid state; any state gives the property)
+    y = I.decode_token(N, H, d, d, p["dtype"], p["la"], seed=11, step=0, device=DEV)
+    o = kda.kda_decode_step(y["k"], y["k"], y["v"], y["log_alpha"], torch.ones_like(y["beta"]), S)
+    torch.cuda.synchronize()
+    assert read_back_err(o, y["v"]) < 2e-2
+    assert bool(torch.isfinite(S).all())
