@@ -19,6 +19,8 @@
 // query read) are 3-step shuffles among the 8 lanes of a row.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "kda_internal.h"
 
 namespace kda {
@@ -111,24 +113,26 @@ __global__ void __launch_bounds__(128) decode_step_kernel(
 template <int D, typename Tin>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *la,
                          const float *beta, float *S, int NH, void *o, cudaStream_t s) {
-    // resident blocks on the whole GPU, looked up once per device (every thread
-    // that races here computes the same value)
+    // resident blocks on the whole GPU, looked up once per device (threads that
+    // race here all compute and store the same value)
     constexpr int kMaxDevices = 64;
-    static int resident[kMaxDevices];
+    static std::atomic<int> resident[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (resident[dev] == 0) {
+    int res = resident[dev].load(std::memory_order_relaxed);
+    if (res == 0) {
         int sms = 0, per = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_step_kernel<D, Tin>,
                                                               128, 0);
         if (e != cudaSuccess) return e;
-        resident[dev] = sms * (per > 0 ? per : 1);
+        res = sms * (per > 0 ? per : 1);
+        resident[dev].store(res, std::memory_order_relaxed);
     }
-    const int grid = NH < resident[dev] ? NH : resident[dev];
+    const int grid = NH < res ? NH : res;
     decode_step_kernel<D, Tin><<<grid, 128, 0, s>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k),
         static_cast<const Tin *>(v), la, beta, S, static_cast<Tin *>(o), NH);

@@ -46,6 +46,8 @@
 // registers, round to nearest).
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "kda_internal.h"
 
 namespace kda {
@@ -486,13 +488,15 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
                          const float *beta, float *S, const int32_t *n_accept, void *o, int N,
                          int K, int H, cudaStream_t s) {
     constexpr int kMaxDevices = 64;
-    static int resident[kMaxDevices];  // every thread that races here computes the same value
+    // resident blocks per device (threads that race here all store the same value)
+    static std::atomic<int> resident[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     constexpr size_t kSmem = sizeof(DraftSmem<D, Tin>) + (size_t)D * D * sizeof(float);
-    if (resident[dev] == 0) {
+    int res = resident[dev].load(std::memory_order_relaxed);
+    if (res == 0) {
         int sms = 0, per = 0;
         e = cudaFuncSetAttribute(draft_kernel<D, Tin, kCommit>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
@@ -502,12 +506,13 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                 &per, draft_kernel<D, Tin, kCommit>, 2 * D, kSmem);
         if (e != cudaSuccess) return e;
-        resident[dev] = sms * (per > 0 ? per : 1);
+        res = sms * (per > 0 ? per : 1);
+        resident[dev].store(res, std::memory_order_relaxed);
     }
     // token rows are staged by 16-byte copies when every row starts on 16 bytes
     const int pf = ((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)la) % 16 == 0;
     const int pairs = N * H;
-    const int grid = pairs < resident[dev] ? pairs : resident[dev];
+    const int grid = pairs < res ? pairs : res;
     draft_kernel<D, Tin, kCommit><<<grid, 2 * D, kSmem, s>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v),
         la, beta, S, n_accept, static_cast<Tin *>(o), N, K, H, pf);
