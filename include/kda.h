@@ -250,7 +250,8 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
  * NULL applies all K); S is read and written once.  Both agree with the same
  * tokens passed one at a time to kda_decode_step up to fp32 rounding (the
  * tokens are taken in closed form over sub-blocks of 8, which sums in another
- * order).
+ * order), except the outputs of a bf16 verify: it reads the state through bf16
+ * products, so they agree to about the rounding of their own bf16 type.
  * Alignment as for kda_decode_step; n_accept 4-byte aligned.  No workspace.
  */
 #define KDA_MAX_DRAFT_TOKENS 16

@@ -40,8 +40,9 @@
 // products, so the 2 n dot products of a row are tensor-core products of the
 // state with the decayed keys and queries -- fp32 accuracy from three tf32
 // products per tile (high x high, high x low, low x high), except in a bf16
-// verify, which only reads the state and rounds its outputs to bf16: one tf32
-// product per tile there.  The solve and the
+// verify, which only reads the state and rounds its outputs to bf16: bf16
+// products there (m16n8k16, whose A fragment is the same registers taken 16
+// channels at a time).  The solve and the
 // state update stay in fp32 on the CUDA cores (the update adds into the same
 // registers, round to nearest).
 #include <cuda_bf16.h>
@@ -81,6 +82,23 @@ __device__ __forceinline__ uint32_t tf32_bits(float x) {
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
     hi = tf32_bits(x);
     lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
+// bf16 pair {lo, hi} (lo in the low half), rounded to nearest
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// d (16 x 8, fp32) += a (16 x 16) b (16 x 8), bf16 operands
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // d (16 x 8, fp32) += a (16 x 8) b (8 x 8), tf32 operands
@@ -140,7 +158,8 @@ __device__ __forceinline__ float halving_sum(float (&x)[kLen], int lane) {
 template <int D, typename Tin>
 struct DraftSmem {
     static constexpr int kLd = D + 8;  // padded rows: conflict-free fragment loads
-    // tensor-core operands as a tf32 high part [0] and the rest [1]
+    // tensor-core operands as a tf32 high part [0] and the rest [1] (a bf16
+    // verify keeps its bf16 keys and queries in [1], rows of D + 8 elements)
     float xk[2][kSub][kLd];  // D(-1, t) k_t
     float xq[2][kSub][kLd];  // D(-1, t) q_t
     float kb[2][kSub][kLd];  // D(t, n-1) k_t
@@ -179,10 +198,13 @@ __global__ void __launch_bounds__(2 * D, 2) draft_kernel(
     int tokens_aligned) {
     constexpr int kNT = D / 8;  // 8-channel slices of a row
     constexpr int kThreads = 2 * D;
-    // verify with bf16 outputs (the state only read): one tf32 product per
-    // dot; its 2^-11 operand rounding sits under the outputs' bf16 rounding.
-    // Everything that updates the state keeps the three-product fp32 form.
-    constexpr bool kOneTf32 = !kCommit && sizeof(Tin) == 2;
+    // verify with bf16 outputs (the state only read): the dots are bf16
+    // products (state rows and decayed keys / queries rounded to bf16, as the
+    // tensor-core prefill reads its state), under the outputs' own bf16
+    // rounding.  Everything that updates the state keeps the three-product
+    // fp32 form.
+    constexpr bool kBf16Dots = !kCommit && sizeof(Tin) == 2;
+    constexpr int kLdb = D + 8;  // bf16 operand rows, over the (then unused) low-part arrays
     extern __shared__ __align__(16) uint8_t draft_smem[];
     DraftSmem<D, Tin> &sm = *reinterpret_cast<DraftSmem<D, Tin> *>(draft_smem);
     // the next pair's state, landed by cp.async while this pair is worked on;
@@ -278,10 +300,15 @@ __global__ void __launch_bounds__(2 * D, 2) draft_kernel(
 #pragma unroll
                 for (int t = 0; t < kSub; ++t) {
                     run *= a[t];
-                    uint32_t hi, lo;
-                    split_tf32(kk[t] * run, hi, lo);
-                    sm.xk[0][t][c] = __uint_as_float(hi);
-                    if (!kOneTf32) sm.xk[1][t][c] = __uint_as_float(lo);
+                    if constexpr (kBf16Dots) {
+                        reinterpret_cast<__nv_bfloat16 *>(&sm.xk[1][0][0])[t * kLdb + c] =
+                            __float2bfloat16_rn(kk[t] * run);
+                    } else {
+                        uint32_t hi, lo;
+                        split_tf32(kk[t] * run, hi, lo);
+                        sm.xk[0][t][c] = __uint_as_float(hi);
+                        sm.xk[1][t][c] = __uint_as_float(lo);
+                    }
                 }
             } else {
                 float run = 1.f;
@@ -289,10 +316,15 @@ __global__ void __launch_bounds__(2 * D, 2) draft_kernel(
                 for (int t = 0; t < kSub; ++t) {
                     run *= a[t];
                     if (!kCommit) {
-                        uint32_t hi, lo;
-                        split_tf32(qq[t] * run, hi, lo);
-                        sm.xq[0][t][c] = __uint_as_float(hi);
-                        if (!kOneTf32) sm.xq[1][t][c] = __uint_as_float(lo);
+                        if constexpr (kBf16Dots) {
+                            reinterpret_cast<__nv_bfloat16 *>(&sm.xq[1][0][0])[t * kLdb + c] =
+                                __float2bfloat16_rn(qq[t] * run);
+                        } else {
+                            uint32_t hi, lo;
+                            split_tf32(qq[t] * run, hi, lo);
+                            sm.xq[0][t][c] = __uint_as_float(hi);
+                            sm.xq[1][t][c] = __uint_as_float(lo);
+                        }
                     }
                 }
                 if (update) {
@@ -371,17 +403,27 @@ __global__ void __launch_bounds__(2 * D, 2) draft_kernel(
             // 8 i + 2 j, j >= 4 is 8 i + 2 (j - 4) + 1, for the state (A) and the
             // keys / queries (B) alike.
             float cp3[3][4] = {}, cq3[3][4] = {};
+            if constexpr (kBf16Dots) {
+                // bf16 products, 16 channels per step: lane (g, tg) holds channels
+                // 16 j + 2 tg, + 1 (slice 2 j) and 16 j + 8 + 2 tg, + 1 (slice 2 j + 1)
+                const __nv_bfloat16 *xkb = reinterpret_cast<const __nv_bfloat16 *>(&sm.xk[1][0][0]);
+                const __nv_bfloat16 *xqb = reinterpret_cast<const __nv_bfloat16 *>(&sm.xq[1][0][0]);
 #pragma unroll
-            for (int i = 0; i < kNT; ++i) {
-                const int col = 8 * i + 2 * tg;  // B fragment: token g, channels col, col + 1
-                if constexpr (kOneTf32) {
-                    const uint32_t ah[4] = {tf32_bits(sa[i].x), tf32_bits(sb[i].x),
-                                            tf32_bits(sa[i].y), tf32_bits(sb[i].y)};
-                    const float2 bk = *reinterpret_cast<const float2 *>(&sm.xk[0][g][col]);
-                    const float2 bq = *reinterpret_cast<const float2 *>(&sm.xq[0][g][col]);
-                    mma_tf32(cp3[0], ah, __float_as_uint(bk.x), __float_as_uint(bk.y));
-                    mma_tf32(cq3[0], ah, __float_as_uint(bq.x), __float_as_uint(bq.y));
-                } else {
+                for (int j = 0; j < kNT / 2; ++j) {
+                    const uint32_t a[4] = {pack_bf16x2(sa[2 * j].x, sa[2 * j].y),
+                                           pack_bf16x2(sb[2 * j].x, sb[2 * j].y),
+                                           pack_bf16x2(sa[2 * j + 1].x, sa[2 * j + 1].y),
+                                           pack_bf16x2(sb[2 * j + 1].x, sb[2 * j + 1].y)};
+                    const int e = g * kLdb + 16 * j + 2 * tg;
+                    mma_bf16(cp3[j % 3], a, *reinterpret_cast<const uint32_t *>(xkb + e),
+                             *reinterpret_cast<const uint32_t *>(xkb + e + 8));
+                    mma_bf16(cq3[j % 3], a, *reinterpret_cast<const uint32_t *>(xqb + e),
+                             *reinterpret_cast<const uint32_t *>(xqb + e + 8));
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kNT; ++i) {
+                    const int col = 8 * i + 2 * tg;  // B fragment: token g, channels col, col + 1
                     uint32_t ah[4], al[4];
                     split_tf32(sa[i].x, ah[0], al[0]);
                     split_tf32(sb[i].x, ah[1], al[1]);
