@@ -140,6 +140,13 @@ def _check(t, name, dtype=None, device=None):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _check_shape(t, name, shape):
+    """The library sees only pointers: a tensor of another shape would be read
+    or written out of its bounds, so the shape is checked here."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be {list(shape)}, got {list(t.shape)}")
+
+
 def _fwd_args(q, k, v, log_alpha, beta, S0, cu_seqlens, o, S_T, return_state):
     """Checks and sizes shared by the forward entry points: (B, T, H, d_k, d_v,
     N, o, S_T), with o and S_T allocated with torch when not given."""
@@ -155,6 +162,8 @@ def _fwd_args(q, k, v, log_alpha, beta, S0, cu_seqlens, o, S_T, return_state):
     if cu_seqlens is not None:
         if q.dim() != 3:
             raise ValueError("with cu_seqlens, q must be packed [Ttot, H, d_k]")
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+            raise ValueError("cu_seqlens must be [N + 1] with N >= 0")
         B, T = 1, q.shape[0]
         N = cu_seqlens.numel() - 1
     else:
@@ -168,12 +177,15 @@ def _fwd_args(q, k, v, log_alpha, beta, S0, cu_seqlens, o, S_T, return_state):
     if k.shape != q.shape or log_alpha.shape != q.shape or v.shape[:-1] != q.shape[:-1] \
             or beta.shape != q.shape[:-1]:
         raise ValueError("q, k, v, log_alpha, beta shapes disagree")
+    _check_shape(S0, "S0", (N, H, d_v, d_k))
     if o is None:
         o = torch.empty(v.shape, dtype=dt, device=dev)
     _check(o, "o", dt, dev)
+    _check_shape(o, "o", v.shape)
     if S_T is None and return_state:
         S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=dev)
     _check(S_T, "S_T", torch.float32, dev)
+    _check_shape(S_T, "S_T", (N, H, d_v, d_k))
     return B, T, H, d_k, d_v, N, o, S_T
 
 
@@ -247,29 +259,12 @@ def kda_fwd_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, o=Non
     allocate avoid by passing them).  `device_status` is an optional device
     int32 tensor that receives the call's status word.  Returns (o, S_T).
     """
-    dev = q.device
     dt = q.dtype
-    _check(q, "q", dt), _check(k, "k", dt, dev), _check(v, "v", dt, dev)
-    _check(log_alpha, "log_alpha", torch.float32, dev)
-    _check(beta, "beta", torch.float32, dev)
-    _check(S0, "S0", torch.float32, dev)
-    _check(cu_seqlens, "cu_seqlens", torch.int32, dev)
-    _check(device_status, "device_status", torch.int32, dev)
-    H, d_k = q.shape[-2], q.shape[-1]
-    d_v = v.shape[-1]
-    if cu_seqlens is not None:
-        B, T, N = 1, q.shape[0], cu_seqlens.numel() - 1
-    elif q.dim() == 4:
-        B, T = q.shape[0], q.shape[1]
-        N = B
-    else:
-        B, T, N = 1, q.shape[0], 1
-    if o is None:
-        o = torch.empty(v.shape, dtype=dt, device=dev)
-    if S_T is None:
-        S_T = torch.empty((N, H, d_v, d_k), dtype=torch.float32, device=dev)
-    _check(o, "o", dt, dev)
-    _check(S_T, "S_T", torch.float32, dev)
+    _check(device_status, "device_status", torch.int32, q.device)
+    if device_status is not None and device_status.numel() < 1:
+        raise ValueError("device_status must hold at least one int32")
+    B, T, H, d_k, d_v, N, o, S_T = _fwd_args(q, k, v, log_alpha, beta, S0, cu_seqlens, o,
+                                             S_T, True)
     rc = load().kda_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                                 _ptr(S0), _ptr(cu_seqlens), B, T, H, d_k, d_v, N,
                                 _dtype_code(dt), _ptr(o), _ptr(S_T), _ptr(device_status),
@@ -290,13 +285,19 @@ def kda_decode_step(q, k, v, log_alpha, beta, S, *, o=None, stream=None):
     _check(log_alpha, "log_alpha", torch.float32, dev)
     _check(beta, "beta", torch.float32, dev)
     _check(S, "S", torch.float32, dev)
+    if q.dim() != 3:
+        raise ValueError("decode inputs are [N, H, d]")
     N, H, d_k = q.shape
     d_v = v.shape[-1]
+    if k.shape != q.shape or log_alpha.shape != q.shape or v.shape[:-1] != q.shape[:-1] \
+            or beta.shape != q.shape[:-1]:
+        raise ValueError("q, k, v, log_alpha, beta shapes disagree")
     if S.shape != (N, H, d_v, d_k):
         raise ValueError(f"S must be [N, H, d_v, d_k] = {(N, H, d_v, d_k)}")
     if o is None:
         o = torch.empty((N, H, d_v), dtype=dt, device=dev)
     _check(o, "o", dt, dev)
+    _check_shape(o, "o", (N, H, d_v))
     rc = load().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                                 _ptr(S), N, H, d_k, d_v, _dtype_code(dt), _ptr(o),
                                 _stream(stream))
@@ -331,6 +332,7 @@ def kda_verify_tokens(q, k, v, log_alpha, beta, S, *, o=None, stream=None):
     if o is None:
         o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     _check(o, "o", q.dtype, q.device)
+    _check_shape(o, "o", v.shape)
     rc = load().kda_verify_tokens(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                                   _ptr(S), N, K, H, d_k, d_v, _dtype_code(q.dtype), _ptr(o),
                                   _stream(stream))

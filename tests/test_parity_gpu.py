@@ -806,3 +806,36 @@ def test_workload_decode_and_draft_read_back_v(kda):
     torch.cuda.synchronize()
     assert read_back_err(o, y["v"]) < 2e-2
     assert bool(torch.isfinite(S).all())
+
+
+def test_binding_rejects_mis_shaped_buffers(kda):
+    """The C ABI takes bare pointers, so the binding checks every buffer's shape
+    before the call: a wrong-sized o, S_T, S0 or decode / draft operand raises
+    ValueError and nothing is launched (the caller's buffers stay untouched)."""
+    prob = I.prefill_problem(1, 100, 2, 64, 64, "f32", (-0.5, -0.001), 0.05, seed=1, device=DEV)
+    args = (prob.q, prob.k, prob.v, prob.log_alpha, prob.beta)
+    o_bad = torch.full((1, 99, 2, 64), 7.0, device=DEV)
+    with pytest.raises(ValueError):
+        kda.kda_fwd(*args, prob.S0, o=o_bad)
+    assert bool((o_bad == 7.0).all())
+    with pytest.raises(ValueError):
+        kda.kda_fwd(*args, prob.S0, S_T=torch.empty(1, 2, 64, 32, device=DEV))
+    with pytest.raises(ValueError):
+        kda.kda_fwd(*args, prob.S0[:, :1].contiguous())
+    with pytest.raises(ValueError):
+        kda.kda_fwd_cp(*args, prob.S0, segments=2, o=o_bad)
+    with pytest.raises(ValueError):
+        kda.kda_fwd_noalloc(*args, torch.zeros(2, 2, 64, 64, device=DEV))
+    x = I.decode_token(2, 2, 64, 64, "f32", seed=1, device=DEV)
+    S = torch.zeros(2, 2, 64, 64, device=DEV)
+    with pytest.raises(ValueError):
+        kda.kda_decode_step(x["q"], x["k"][:1].contiguous(), x["v"], x["log_alpha"], x["beta"], S)
+    with pytest.raises(ValueError):
+        kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S,
+                            o=torch.empty(2, 2, 32, device=DEV))
+    y = I.draft_tokens(2, 3, 2, 64, 64, "f32", seed=1, device=DEV)
+    with pytest.raises(ValueError):
+        kda.kda_verify_tokens(y["q"], y["k"], y["v"], y["log_alpha"], y["beta"], S,
+                              o=torch.empty(2, 3, 2, 32, device=DEV))
+    torch.cuda.synchronize()
+    assert bool((S == 0).all())
