@@ -94,7 +94,7 @@ struct __align__(1024) TcStage {
 struct __align__(1024) TcSmem {
     TcStage st[2];
     uint8_t tp[8192];   // T' bf16 [r][j]; fp32 scratch while solving
-    uint8_t ut[16384];  // U^T bf16 [v][j]; then the staged output tile [r][v]
+    uint8_t ut[16384];  // the staged output tile [r][v] (two 64-channel slabs)
     uint8_t gt[32768];  // log_alpha tile: 4 boxes of 32 channels x 64 tokens (fp32, swizzled)
     float as[C * LDA];  // solve matrix / inverse blocks (fp32)
     uint64_t full[2], ready[2], gfull, tpfull;
