@@ -687,19 +687,25 @@ def oracle_sample(w, budget_heads=None):
     return run, nsess / S.shape[0], f"{nsess} of {S.shape[0]} sessions, all heads", cores
 
 
-def cpu_baseline(w, args, steps=1):
+def cpu_baseline(w, args, target_s=10.0, max_repeats=50):
+    """The oracle on a bounded sample, repeated for about target_s seconds of CPU
+    work, scaled to the whole workload."""
     run, frac, sample, cores = oracle_sample(w)
     run()  # warm (and builds the oracle library if needed)
+    repeats = 0
     t0 = time.perf_counter()
-    for _ in range(steps):
+    while True:
         run()
-    dt = (time.perf_counter() - t0) / steps / frac  # seconds for the whole workload
+        repeats += 1
+        elapsed = time.perf_counter() - t0
+        if elapsed >= target_s or repeats >= max_repeats:
+            break
+    dt = elapsed / repeats / frac  # seconds for the whole workload
+    extra = {"cores": cores, "kind": "oracle", "sample": f"{sample}, {repeats} repeats",
+             "seconds_sampled": round(elapsed, 2)}
     if w["kind"] == "prefill":
-        return {"value": round(w["Ttot"] / dt, 2), "unit": "tokens/s", "cores": cores,
-                "kind": "oracle", "sample": sample,
-                "seconds_sampled": round(dt * frac, 2)}
-    return {"value": round(2 * nbytes(w["S"]) / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
-            "kind": "oracle", "sample": sample, "seconds_sampled": round(dt * frac, 2)}
+        return {"value": round(w["Ttot"] / dt, 2), "unit": "tokens/s", **extra}
+    return {"value": round(2 * nbytes(w["S"]) / dt / 1e9, 4), "unit": "GB/s", **extra}
 
 
 def run_reference(args, world, rank):
