@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 2; ++i)
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) g[i][e] *= kLog2e;
+                    for (int e = 0; e < 16; e += 2) mul2(g[i][e], g[i][e + 1], kLog2e, kLog2e);
             } else {  // the tile runs past the sequence end
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
@@ -432,15 +432,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 16; ++e) g[i][e] = live ? g[i][e] * kLog2e : 0.f;
                 }
             }
+            // packed pairs of channels throughout (the same roundings as scalar
+            // instructions, half the issue slots)
             float inc[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) inc[e] = g[0][e] + g[1][e];  // this lane's total
+            for (int e = 0; e < 16; e += 2) {  // this lane's total
+                inc[e] = g[0][e];
+                inc[e + 1] = g[0][e + 1];
+                add2(inc[e], inc[e + 1], g[1][e], g[1][e + 1]);
+            }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {  // inclusive scan across the warp
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float up = __shfl_up_sync(0xffffffffu, inc[e], o);
-                    if (lane >= o) inc[e] += up;
+                for (int e = 0; e < 16; e += 2) {
+                    const float up0 = __shfl_up_sync(0xffffffffu, inc[e], o);
+                    const float up1 = __shfl_up_sync(0xffffffffu, inc[e + 1], o);
+                    if (lane >= o) add2(inc[e], inc[e + 1], up0, up1);
                 }
             }
             // slot i holds token 2 l + (i ^ fl): the odd token's G2 is the
@@ -448,22 +455,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             // log-decay -- as weights (one of fl, 1 - fl is 0) instead of
             // selects, with the same single rounding
             const float wf = fl ? 1.f : 0.f, wn = 1.f - wf;
-            float lo = 0.f, hi = 0.f;
+            float amax = 0.f;  // largest |G2| of the odd tokens (the inclusive sums)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float s0 = fmaf(-wn, g[1][e], inc[e]);  // slot 0
-                const float s1 = fmaf(-wf, g[0][e], inc[e]);  // slot 1
-                g[0][e] = s0;
-                g[1][e] = s1;
-                // with log-decay <= 0 the odd token's G2 (the inclusive sum) is
-                // the lower of the pair
-                lo = fminf(lo, inc[e]);
-                hi = fmaxf(hi, inc[e]);
+            for (int e = 0; e < 16; e += 2) {
+                float s00 = inc[e], s01 = inc[e + 1], s10 = inc[e], s11 = inc[e + 1];
+                fma2(s00, s01, -wn, -wn, g[1][e], g[1][e + 1]);  // slot 0
+                fma2(s10, s11, -wf, -wf, g[0][e], g[0][e + 1]);  // slot 1
+                g[0][e] = s00;
+                g[0][e + 1] = s01;
+                g[1][e] = s10;
+                g[1][e + 1] = s11;
+                amax = fmaxf(amax, fmaxf(fabsf(inc[e]), fabsf(inc[e + 1])));
             }
             // a chunk outside the chunk form's range sends the whole (sequence,
             // head) to the token-serial pass after teardown
-            if (!(-lo <= kLog2DecayLimit && hi <= kLog2DecayLimit))
-                *reinterpret_cast<volatile int *>(&sm.domain) = 1;
+            if (!(amax <= kLog2DecayLimit)) *reinterpret_cast<volatile int *>(&sm.domain) = 1;
         };
         // Warps 4-7: gates of chunk m scanned and parked; once every scanning
         // thread has read the gate tile, it takes chunk m + 1.

@@ -310,6 +310,30 @@ __device__ __forceinline__ void mul2(float &a0, float &a1, float b0, float b1) {
         : "f"(b0), "f"(b1));
 }
 
+// (a0, a1) += (b0, b1), packed, round to nearest
+__device__ __forceinline__ void add2(float &a0, float &a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 x, y;\n\t"
+        "mov.b64 x, {%0, %1};\n\t"
+        "mov.b64 y, {%2, %3};\n\t"
+        "add.rn.f32x2 x, x, y;\n\t"
+        "mov.b64 {%0, %1}, x;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
+// (c0, c1) = (a0, a1) * (b0, b1) + (c0, c1), packed, round to nearest
+__device__ __forceinline__ void fma2(float &c0, float &c1, float a0, float a1, float b0,
+                                     float b1) {
+    asm("{\n\t.reg .b64 x, y, z;\n\t"
+        "mov.b64 x, {%2, %3};\n\t"
+        "mov.b64 y, {%4, %5};\n\t"
+        "mov.b64 z, {%0, %1};\n\t"
+        "fma.rn.f32x2 z, x, y, z;\n\t"
+        "mov.b64 {%0, %1}, z;\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
