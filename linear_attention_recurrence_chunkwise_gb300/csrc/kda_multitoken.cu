@@ -350,7 +350,37 @@ __global__ void __launch_bounds__(2 * D, 2) draft_kernel(
             }
             if (tid < kSub)
                 sm.beta[tid] = tid < nb ? beta[(size_t)(n * K + t0 + tid) * H + h] : 0.f;
-            if (!kCommit || half == 0) {
+            if constexpr (kCommit) {
+                // commit needs A alone: its 28 entries split by rows between the
+                // halves (rows 1-5, 15 entries, on half 0; rows 6-7, 13, on half 1)
+                float x[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] = 0.f;
+                if (half == 0) {
+#pragma unroll
+                    for (int t = 1; t <= 5; ++t) {
+                        float dec = 1.f;
+#pragma unroll
+                        for (int j = t - 1; j >= 0; --j) {
+                            dec *= a[j + 1];
+                            x[t * (t - 1) / 2 + j] = kk[t] * kk[j] * dec;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int t = 6; t < kSub; ++t) {
+                        float dec = 1.f;
+#pragma unroll
+                        for (int j = t - 1; j >= 0; --j) {
+                            dec *= a[j + 1];
+                            x[t * (t - 1) / 2 + j - 15] = kk[t] * kk[j] * dec;
+                        }
+                    }
+                }
+                float sum16 = halving_sum<16>(x, lane);  // over this half-warp
+                sum16 += __shfl_xor_sync(0xffffffffu, sum16, 16);
+                sm.part[half][c >> 5][lane] = sum16;
+            } else {
                 // half 0: A[t][j] and M[t][t] for t < 4; half 1: M[t][j] (j < t)
                 // and M[t][t] for t >= 4 -- this channel's terms
                 float x[32];
@@ -370,7 +400,15 @@ __global__ void __launch_bounds__(2 * D, 2) draft_kernel(
                 sm.part[half][c >> 5][lane] = halving_sum<32>(x, lane);
             }
             __syncthreads();
-            if (tid < (kCommit ? 28 : 64)) {
+            if (kCommit && tid < 28) {
+                const int hh = tid < 15 ? 0 : 1, l = tid < 15 ? tid : tid - 15;
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < D / 32; ++w) sum += sm.part[hh][w][l];
+                int t, j;
+                lower_entry(tid, t, j);
+                sm.A[t][j] = sum;
+            } else if (!kCommit && tid < 64) {
                 const int hh = tid >> 5, l = tid & 31;
                 float sum = 0.f;
 #pragma unroll
