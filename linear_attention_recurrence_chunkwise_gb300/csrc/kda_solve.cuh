@@ -128,12 +128,17 @@ __device__ __forceinline__ void store_tprime(uint8_t *tp, const float *beta, int
 
 // On entry `as` (fp32 values rounded to tf32, row stride kSolveLd) holds A
 // strictly below the diagonal (what lies on and above it is never read), and
-// beta[64] the token weights.  The blocks of T it writes back for later steps
-// are rounded to tf32 too: they are read only as tensor-core operands.  On exit `tp` holds T' (bf16,
-// [r][j], 128-byte swizzle) and `as` is scratch.  Called by the 128 threads
-// (pt = 0 .. 127) of four warps, which synchronise among themselves on the
-// named barrier `bar`.  The caller makes the tile visible to the tensor cores
-// (fence.proxy.async) and synchronises the four warps.
+// beta[64] (16-byte aligned) the token weights.  The blocks of T it writes
+// back for later steps are rounded to tf32 too: they are read only as
+// tensor-core operands.  On exit `tp` holds T' (bf16, [r][j], 128-byte
+// swizzle) and `as` is scratch.  Called by the 128 threads (pt = 0 .. 127) of
+// four warps, which synchronise among themselves on the named barrier `bar`.
+// The caller makes the tile visible to the tensor cores (fence.proxy.async)
+// and synchronises the four warps.  kOffloadDiag moves the bf16 stores of the
+// diagonal blocks of T' from the substituting warps (0, 1) of step 1 to the
+// idle warps (2, 3) of step 2, which then read the tf32 T_bb back (one more
+// rounding): faster when every SM of the GPU is busy, slower otherwise.
+template <bool kOffloadDiag>
 __device__ __forceinline__ void solve_tprime64(float *as, const float *beta, uint8_t *tp, int pt,
                                                uint32_t bar) {
     constexpr int ld = kSolveLd;
@@ -175,17 +180,41 @@ __device__ __forceinline__ void solve_tprime64(float *as, const float *beta, uin
             }
         }
         __syncwarp();
-        // T_bb is read back only as a tensor-core operand: stored as tf32
+        // T_bb is read back as a tensor-core operand (and, with kOffloadDiag,
+        // for its bf16 copy in T'): stored as tf32
 #pragma unroll
         for (int r = 0; r < 16; ++r) Ab[r * ld + c] = __uint_as_float(to_tf32(x[r]));
-        const float bc = beta[16 * b + c];
+        if constexpr (!kOffloadDiag) {
+            const float bc = beta[16 * b + c];
 #pragma unroll
-        for (int r = 0; r < 16; ++r)
-            *reinterpret_cast<__nv_bfloat16 *>(tp + tp_offset(16 * b + r, 16 * b + c)) =
-                __float2bfloat16_rn(x[r] * bc);
+            for (int r = 0; r < 16; ++r)
+                *reinterpret_cast<__nv_bfloat16 *>(tp + tp_offset(16 * b + r, 16 * b + c)) =
+                    __float2bfloat16_rn(x[r] * bc);
+        }
     }
     sm100::named_bar_sync(bar, 128);
-    // 2. T_10 (warp 0) and T_32 (warp 1)
+    // 2. T_10 (warp 0) and T_32 (warp 1); with kOffloadDiag, warps 2 and 3
+    //    meanwhile write the diagonal blocks of T' = T diag(beta) in bf16 from
+    //    the tf32 T_bb, 8 columns of a row per piece, two pieces per thread
+    if constexpr (kOffloadDiag) {
+        if (warp >= 2) {
+#pragma unroll
+            for (int q = pt - 64; q < 128; q += 64) {
+                const int b = q >> 5, r = (q >> 1) & 15, h = q & 1;
+                const float *src = as + (16 * b + r) * ld + 16 * b + 8 * h;
+                const float4 t0 = *reinterpret_cast<const float4 *>(src);
+                const float4 t1 = *reinterpret_cast<const float4 *>(src + 4);
+                const float4 b0 = *reinterpret_cast<const float4 *>(beta + 16 * b + 8 * h);
+                const float4 b1 = *reinterpret_cast<const float4 *>(beta + 16 * b + 8 * h + 4);
+                uint4 w;
+                w.x = sm100::pack_bf16(t0.x * b0.x, t0.y * b0.y);
+                w.y = sm100::pack_bf16(t0.z * b0.z, t0.w * b0.w);
+                w.z = sm100::pack_bf16(t1.x * b1.x, t1.y * b1.y);
+                w.w = sm100::pack_bf16(t1.z * b1.z, t1.w * b1.w);
+                *reinterpret_cast<uint4 *>(tp + tp_offset(16 * b + r, 16 * b + 8 * h)) = w;
+            }
+        }
+    }
     if (warp < 2) {
         const int bi = 2 * warp + 1, bj = 2 * warp;
         float p[2][4] = {}, z[2][4] = {};
