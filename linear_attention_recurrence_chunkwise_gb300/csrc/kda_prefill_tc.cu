@@ -591,11 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                __uint_as_float(x[4 * j4 + 2]), __uint_as_float(x[4 * j4 + 3]));
                         mul2(w.x, w.y, br, br);
                         mul2(w.z, w.w, br, br);
-                        // stored as tf32 (the solve's operand precision, so it
-                        // converts nothing); entries on and above the diagonal
-                        // are never read by the solve, which overwrites them
-                        w = make_float4(__uint_as_float(to_tf32(w.x)), __uint_as_float(to_tf32(w.y)),
-                                        __uint_as_float(to_tf32(w.z)), __uint_as_float(to_tf32(w.w)));
+                        // stored in fp32 (the solve's tensor cores read the
+                        // tf32 part); entries on and above the diagonal are
+                        // never read by the solve, which overwrites them
                         *reinterpret_cast<float4 *>(&sm.as[r * LDA + j]) = w;
                     }
                 } else {  // M[r][j] = R[64 + r][j], j <= r

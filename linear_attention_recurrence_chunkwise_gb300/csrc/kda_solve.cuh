@@ -26,13 +26,9 @@ namespace kda {
 
 constexpr int kSolveLd = 68;  // fp32 row stride of the matrix
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// d (16 x 8, fp32) += a (16 x 8, tf32) * b (8 x 8, tf32)
+// d (16 x 8, fp32) += a (16 x 8, tf32) * b (8 x 8, tf32).  The operands are
+// passed as fp32 bit patterns: the tensor cores read their tf32 part (the low
+// 13 mantissa bits are dropped), which spares a conversion per operand.
 __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4],
                                                 const uint32_t (&b)[2]) {
     asm volatile(
@@ -52,14 +48,14 @@ __device__ __forceinline__ void mma_xt(float (&p)[2][4], const float *tl, const 
     constexpr int ld = kSolveLd;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        uint32_t a[4];  // A operand = T_LJ^T: element (m, k) = T_LJ[k][m] (stored as tf32)
+        uint32_t a[4];  // A operand = T_LJ^T: element (m, k) = T_LJ[k][m]
         a[0] = __float_as_uint(tl[(8 * ks + t) * ld + g]);
         a[1] = __float_as_uint(tl[(8 * ks + t) * ld + g + 8]);
         a[2] = __float_as_uint(tl[(8 * ks + t + 4) * ld + g]);
         a[3] = __float_as_uint(tl[(8 * ks + t + 4) * ld + g + 8]);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {  // B operand = A_KL^T: (k, n) = A_KL[n][k]
-            uint32_t b[2];  // (A is stored as tf32)
+            uint32_t b[2];
             b[0] = __float_as_uint(ak[(8 * nt + g) * ld + 8 * ks + t]);
             b[1] = __float_as_uint(ak[(8 * nt + g) * ld + 8 * ks + t + 4]);
             mma_tf32_16x8x8(p[nt], a, b);
@@ -81,7 +77,7 @@ __device__ __forceinline__ void mma_tx(float (&z)[2][4], const float *tk, const 
     for (int ks = 0; ks < 2; ++ks) {
         const float2 r0 = *reinterpret_cast<const float2 *>(tk + g * ld + 8 * ks + 2 * t);
         const float2 r1 = *reinterpret_cast<const float2 *>(tk + (g + 8) * ld + 8 * ks + 2 * t);
-        uint32_t a[4];  // T_IK, stored as tf32
+        uint32_t a[4];  // T_IK
         a[0] = __float_as_uint(r0.x);
         a[1] = __float_as_uint(r1.x);
         a[2] = __float_as_uint(r0.y);
@@ -89,8 +85,8 @@ __device__ __forceinline__ void mma_tx(float (&z)[2][4], const float *tk, const 
 #pragma unroll
         for (int nz = 0; nz < 2; ++nz) {
             uint32_t b[2];
-            b[0] = to_tf32(p[ks][2 * nz]);
-            b[1] = to_tf32(p[ks][2 * nz + 1]);
+            b[0] = __float_as_uint(p[ks][2 * nz]);
+            b[1] = __float_as_uint(p[ks][2 * nz + 1]);
             mma_tf32_16x8x8(z[nz], a, b);
         }
     }
@@ -126,18 +122,18 @@ __device__ __forceinline__ void store_tprime(uint8_t *tp, const float *beta, int
     }
 }
 
-// On entry `as` (fp32 values rounded to tf32, row stride kSolveLd) holds A
-// strictly below the diagonal (what lies on and above it is never read), and
-// beta[64] (16-byte aligned) the token weights.  The blocks of T it writes
-// back for later steps are rounded to tf32 too: they are read only as
-// tensor-core operands.  On exit `tp` holds T' (bf16, [r][j], 128-byte
+// On entry `as` (fp32, row stride kSolveLd) holds A strictly below the
+// diagonal (what lies on and above it is never read), and beta[64] (16-byte
+// aligned) the token weights.  The blocks of T it writes back for later steps
+// are fp32 too, read by the tensor cores at tf32 precision (the forward
+// substitution of step 1 uses A in full).  On exit `tp` holds T' (bf16, [r][j], 128-byte
 // swizzle) and `as` is scratch.  Called by the 128 threads (pt = 0 .. 127) of
 // four warps, which synchronise among themselves on the named barrier `bar`.
 // The caller makes the tile visible to the tensor cores (fence.proxy.async)
 // and synchronises the four warps.  kOffloadDiag moves the bf16 stores of the
 // diagonal blocks of T' from the substituting warps (0, 1) of step 1 to the
-// idle warps (2, 3) of step 2, which then read the tf32 T_bb back (one more
-// rounding): faster when every SM of the GPU is busy, slower otherwise.
+// idle warps (2, 3) of step 2, which read T_bb back: faster when every SM of
+// the GPU is busy, slower otherwise.
 template <bool kOffloadDiag>
 __device__ __forceinline__ void solve_tprime64(float *as, const float *beta, uint8_t *tp, int pt,
                                                uint32_t bar) {
@@ -181,9 +177,10 @@ __device__ __forceinline__ void solve_tprime64(float *as, const float *beta, uin
         }
         __syncwarp();
         // T_bb is read back as a tensor-core operand (and, with kOffloadDiag,
-        // for its bf16 copy in T'): stored as tf32
+        // by warps 2 and 3 for its bf16 copy in T')
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Ab[r * ld + c] = __uint_as_float(to_tf32(x[r]));
+        for (int r = 0; r < 16; ++r)
+            Ab[r * ld + c] = x[r];
         if constexpr (!kOffloadDiag) {
             const float bc = beta[16 * b + c];
 #pragma unroll
@@ -195,7 +192,7 @@ __device__ __forceinline__ void solve_tprime64(float *as, const float *beta, uin
     sm100::named_bar_sync(bar, 128);
     // 2. T_10 (warp 0) and T_32 (warp 1); with kOffloadDiag, warps 2 and 3
     //    meanwhile write the diagonal blocks of T' = T diag(beta) in bf16 from
-    //    the tf32 T_bb, 8 columns of a row per piece, two pieces per thread
+    //    T_bb, 8 columns of a row per piece, two pieces per thread
     if constexpr (kOffloadDiag) {
         if (warp >= 2) {
 #pragma unroll
@@ -224,11 +221,11 @@ __device__ __forceinline__ void solve_tprime64(float *as, const float *beta, uin
         float *dst = t_block(as, bi, bj);
 #pragma unroll
         for (int nz = 0; nz < 2; ++nz) {
-            // (read back only as a tensor-core operand: stored as tf32)
+            // (read back only as a tensor-core operand)
             *reinterpret_cast<float2 *>(dst + g * ld + 8 * nz + 2 * t) =
-                make_float2(__uint_as_float(to_tf32(-z[nz][0])), __uint_as_float(to_tf32(-z[nz][1])));
+                make_float2(-z[nz][0], -z[nz][1]);
             *reinterpret_cast<float2 *>(dst + (g + 8) * ld + 8 * nz + 2 * t) =
-                make_float2(__uint_as_float(to_tf32(-z[nz][2])), __uint_as_float(to_tf32(-z[nz][3])));
+                make_float2(-z[nz][2], -z[nz][3]);
         }
         store_tprime(tp, beta, bi, bj, z, lane);
     }
