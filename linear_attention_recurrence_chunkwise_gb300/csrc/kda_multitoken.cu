@@ -71,10 +71,11 @@ __device__ __forceinline__ float ex2_fast(float x) {
     return y;
 }
 
+// x rounded to the nearest tf32 value (ties away from zero), as its fp32 bit
+// pattern: add half a unit of the 13 dropped bits, then drop them (two integer
+// instructions; a carry into the exponent is the correct rounding up)
 __device__ __forceinline__ uint32_t tf32_bits(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
+    return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
 }
 
 // x = hi + lo, hi the nearest tf32 value (its low part, below tf32 resolution
