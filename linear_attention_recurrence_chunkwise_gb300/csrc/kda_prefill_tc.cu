@@ -518,12 +518,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_phase_warp(sm.full[s], (n >> 1) & 1, abort);
             // Kb, M and gamma of chunk n - 2 (same slot) are no longer read by the carry
             if (n >= 2) wait_phase_warp(sm.tailfree[s], ((n >> 1) - 1) & 1, abort);
-            // token 63 closes the chunk (lane 31 keeps it in slot 0); the same
-            // ex2 as the operands' Gamma (an accurate exp2f here serialised the
-            // warp on one lane)
-            if (lane == 31)
-#pragma unroll
-                for (int e = 0; e < 16; ++e) S.gam[c0 + e] = ex2_approx(g[0][e]);
             if (pt < C) S.bet[pt] = bet;
 
             // a2: scaled operands, written over the landed tiles (same swizzle)
@@ -534,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int t = 2 * lane + (i ^ fl);
                 const uint32_t off = slab * 16384 + sw128_offset(t, col + 8 * k);
                 const uint32_t offv = slab * 8192 + sw128_offset(t, col + 8 * k);
-                float kf[8], qf[8], kb[8];
+                float kf[8], qf[8], kb[8], gfv[8];
                 if (t < valid) {
                     unpack8(*reinterpret_cast<const uint4 *>(S.kq + off), kf);
                     unpack8(*reinterpret_cast<const uint4 *>(S.kq + off + 8192), qf);
@@ -547,6 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 8; e += 2) {
                     const float gf0 = ex2_approx(gr[e]), gf1 = ex2_approx(gr[e + 1]);
                     const float gi0 = ex2_approx(-gr[e]), gi1 = ex2_approx(-gr[e + 1]);
+                    gfv[e] = gf0;
+                    gfv[e + 1] = gf1;
                     kb[e] = kf[e];
                     kb[e + 1] = kf[e + 1];
                     mul2(kb[e], kb[e + 1], gi0, gi1);
@@ -556,6 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4 *>(S.kq + off) = pack8(kf);
                 *reinterpret_cast<uint4 *>(S.kq + off + 8192) = pack8(qf);
                 *reinterpret_cast<uint4 *>(S.kb + offv) = pack8(kb);
+                // gamma: token 63 closes the chunk, and lane 31 holds it in
+                // slot 0 -- its Gamma, just computed, is the chunk's decay
+                if (i == 0 && lane == 31) {
+                    float4 *gd = reinterpret_cast<float4 *>(S.gam + c0 + 8 * k);
+                    gd[0] = make_float4(gfv[0], gfv[1], gfv[2], gfv[3]);
+                    gd[1] = make_float4(gfv[4], gfv[5], gfv[6], gfv[7]);
+                }
             }
             fence_proxy_async_smem();
             named_bar_sync(kBarPrep, kPrepThreads);
