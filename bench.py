@@ -196,6 +196,39 @@ def make_workload(name, seed, device):
     return dict(kind="prefill", prob=prob, Ttot=Ttot, H=H, d=d, label=lab)
 
 
+def line_config(w, world):
+    """The `config` object of the JSON line (identical for both arms)."""
+    c = {"workload": w["label"], "l2": "inputs larger than L2, no flush",
+         "parallelism": f"replicas x{world} (independent problems per rank)"}
+    if w["kind"] == "prefill":
+        c.update(tokens_per_step=w["Ttot"], heads=w["H"], d=w["d"])
+    else:
+        c.update(sessions=w["N"], heads=w["H"], d=w["d"])
+    return c
+
+
+def time_calls(fn, reps, stream, warm=2):
+    """Mean device time of one call of fn (CUDA events on `stream`)."""
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
+    stream.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+    stream.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def hbm_roof(alg, ms, pk, **extra):
+    gbs = alg / (ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+            "frac": round(gbs / pk["hbm"], 4), "algorithmic_bytes_per_launch": alg, **extra}
+
+
 def prefill_alg_bytes(w):
     p = w["prob"]
     return nbytes(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0, p.cu_seqlens) + \
@@ -354,12 +387,10 @@ def run_ours(args, world, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if args.workload != "tiny" else "f32",
             "data": "synthetic (seeded, device-generated)",
-            "config": {"workload": w["label"], "l2": "inputs larger than L2, no flush",
-                       "parallelism": f"replicas x{world} (independent problems per rank)"},
+            "config": line_config(w, world),
             "roofline": roofline, "clocks": clk.summary(),
             "gpu_launches": launches_per_step * args.steps}
     if w["kind"] == "prefill":
-        line["config"].update(tokens_per_step=w["Ttot"], heads=w["H"], d=w["d"])
         if segments is not None:
             line["config"]["segments"] = segments
             line["config"]["call"] = "kda_fwd_cp (segment-parallel)"
@@ -369,9 +400,12 @@ def run_ours(args, world, rank):
         else:
             line["e2e"] = e2e_prefill(kda, w, e2e_steps, stream, world, segments)
         if args.workload == "prefill" and not args.no_decode:
-            line["decode"] = decode_sub(kda, args, stream, pk)
+            cpu = rank == 0 and world == 1 and not args.no_cpu
+            line["decode"] = decode_sub(kda, args, stream, pk, cpu)
             line["draft"] = draft_sub(kda, args, stream, pk, line["decode"]["us_per_step"])
             line["segment_parallel"] = cp_sub(kda, args, stream, pk)
+            line["long"] = long_sub(kda, args, stream, pk, cpu)
+            line["varlen"] = varlen_sub(kda, args, stream, pk, cpu)
     else:
         line["e2e"] = e2e_decode(kda, w, max(2, min(args.steps, 20)), stream, world)
         if not args.no_decode:
@@ -381,38 +415,53 @@ def run_ours(args, world, rank):
     return line
 
 
-def decode_sub(kda, args, stream, pk):
+def decode_sub(kda, args, stream, pk, cpu=False):
     w = make_workload("decode", seed=args.seed, device="cuda")
     S, toks = w["S"], w["tokens"]
     o = torch.empty_like(toks[0]["v"])
     steps = 1000  # back to back, in place; an event between steps gives the median
-    with torch.cuda.stream(stream):
-        for i in range(5):
-            x = toks[i % len(toks)]
-            kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S, o=o,
-                                stream=stream)
-    torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-    with torch.cuda.stream(stream):
-        ev[0].record(stream)
-        for i in range(steps):
-            x = toks[i % len(toks)]
-            kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S, o=o,
-                                stream=stream)
-            ev[i + 1].record(stream)
-    stream.synchronize()
-    ms = ev[0].elapsed_time(ev[-1]) / steps
-    p50 = statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+
+    def run(states):
+        with torch.cuda.stream(stream):
+            for i in range(5):
+                x = toks[i % len(toks)]
+                kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                    states[i % len(states)], o=o, stream=stream)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for i in range(steps):
+                x = toks[i % len(toks)]
+                kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                    states[i % len(states)], o=o, stream=stream)
+                ev[i + 1].record(stream)
+        stream.synchronize()
+        ms = ev[0].elapsed_time(ev[-1]) / steps
+        p50 = statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+        return ms, p50
+    ms, p50 = run([S])
+    # two states taken in turn (806 MB, over six times the L2): no block of the
+    # state a step reads can still sit in L2 from the step before
+    S2 = I.decode_state(w["N"], w["H"], w["d"], w["d"], I.PRESETS["decode"]["s0_std"],
+                        args.seed + 1, "cuda")
+    ms2, p50_2 = run([S, S2])
+    del S2
     alg = decode_alg_bytes(w)
-    gbs = alg / (ms / 1e3) / 1e9
-    return {"metric": "decode state GB/s", "value": round(2 * nbytes(S) / (ms / 1e3) / 1e9, 1),
-            "unit": "GB/s", "us_per_step": round(ms * 1e3, 2),
-            "us_per_step_p50": round(p50 * 1e3, 2), "steps": steps,
-            "workload": w["label"],
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
-                         "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4),
-                         "traffic": traffic_for("decode", "decode"),
-                         "algorithmic_bytes_per_launch": alg}}
+    out = {"metric": "decode state GB/s", "value": round(2 * nbytes(S) / (ms / 1e3) / 1e9, 1),
+           "unit": "GB/s", "us_per_step": round(ms * 1e3, 2),
+           "us_per_step_p50": round(p50 * 1e3, 2), "steps": steps,
+           "workload": w["label"],
+           "roofline": hbm_roof(alg, ms, pk, traffic=traffic_for("decode", "decode")),
+           "alternating_states": {
+               "value": round(2 * nbytes(S) / (ms2 / 1e3) / 1e9, 1), "unit": "GB/s",
+               "us_per_step": round(ms2 * 1e3, 2), "us_per_step_p50": round(p50_2 * 1e3, 2),
+               "states": 2, "roofline": hbm_roof(alg, ms2, pk),
+               "note": "steps alternate between two 403 MB states, so no state block is "
+                       "re-read from L2"}}
+    if cpu:
+        out["cpu_baseline"] = cpu_baseline(w, args, target_s=5.0)
+    return out
 
 
 def draft_sub(kda, args, stream, pk, decode_us):
@@ -505,6 +554,84 @@ def cp_sub(kda, args, stream, pk):
                          "algorithmic_bytes_per_call": alg,
                          "note": "the operator's bytes over the whole call (three kernels "
                                  "of passes A and D plus the scan)"}}
+
+
+def prefill_roofline(w, ms, pk):
+    r = hbm_roof(prefill_alg_bytes(w), ms, pk)
+    tf = prefill_flops(w) / (ms / 1e3) / 1e12
+    r["tensor"] = {"achieved_tflops": round(tf, 2), "peak_tflops": pk["bf16"],
+                   "frac": round(tf / pk["bf16"], 4), "flops_per_launch": prefill_flops(w),
+                   "flop_count": "6Td^2+3TCd+TC^2 per head (pages' formula)"}
+    return r
+
+
+def long_sub(kda, args, stream, pk, cpu=False):
+    """The long prefill with carry-in: B=1, H=96, T=131072, S0 ~ N(0, 0.02),
+    long-memory gates (one kda_fwd per call)."""
+    w = make_workload("long", seed=args.seed, device="cuda")
+    p = w["prob"]
+    o = torch.empty_like(p.v)
+    ST = torch.empty_like(p.S0)
+    ws = torch.empty(kda.kda_fwd_workspace_bytes(p.n_seq), dtype=torch.uint8, device="cuda")
+    ms = time_calls(lambda: kda.kda_fwd(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0, o=o, S_T=ST,
+                                        workspace=ws, stream=stream), 5, stream)
+    out = {"metric": "tokens/s", "value": round(w["Ttot"] / (ms / 1e3), 1), "unit": "tokens/s",
+           "workload": w["label"], "ms_per_call": round(ms, 3),
+           "roofline": prefill_roofline(w, ms, pk)}
+    if cpu:
+        out["cpu_baseline"] = cpu_baseline(w, args, target_s=4.0, tokens=16384)
+    del w, p, o, ST
+    torch.cuda.empty_cache()
+    return out
+
+
+def varlen_sub(kda, args, stream, pk, cpu=False):
+    """The varlen batch: 16 packed sequences (lengths log-uniform in [1024,
+    65536]), H=96, per-sequence S0; then 256 decode steps on the 16 returned
+    states (B=16)."""
+    w = make_workload("varlen", seed=args.seed, device="cuda")
+    p = w["prob"]
+    o = torch.empty_like(p.v)
+    ST = torch.empty_like(p.S0)
+    ws = torch.empty(kda.kda_fwd_workspace_bytes(p.n_seq), dtype=torch.uint8, device="cuda")
+    ms = time_calls(lambda: kda.kda_fwd(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0,
+                                        p.cu_seqlens, o=o, S_T=ST, workspace=ws,
+                                        stream=stream), 5, stream)
+    pv = I.PRESETS["varlen"]
+    N, H, d = p.n_seq, w["H"], w["d"]
+    toks = [I.decode_token(N, H, d, d, pv["dtype"], pv["la"], args.seed + 1, s, "cuda")
+            for s in range(pv["decode_steps"])]
+    od = torch.empty_like(toks[0]["v"])
+    S = ST.clone()
+    ctr = [0]
+
+    def dec():
+        x = toks[ctr[0] % len(toks)]
+        ctr[0] += 1
+        kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], S, o=od,
+                            stream=stream)
+    ctr[0] = 0
+    dms = time_calls(dec, pv["decode_steps"], stream, warm=0)  # the 256 steps, once
+    x = toks[0]
+    dalg = 2 * nbytes(S) + nbytes(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], od)
+    out = {"metric": "tokens/s", "value": round(w["Ttot"] / (ms / 1e3), 1), "unit": "tokens/s",
+           "workload": w["label"], "ms_per_call": round(ms, 3),
+           "sequence_lengths": (p.cu_seqlens[1:] - p.cu_seqlens[:-1]).tolist(),
+           "roofline": prefill_roofline(w, ms, pk),
+           "decode": {"metric": "decode state GB/s",
+                      "value": round(2 * nbytes(S) / (dms / 1e3) / 1e9, 1), "unit": "GB/s",
+                      "us_per_step": round(dms * 1e3, 2), "steps": pv["decode_steps"],
+                      "workload": f"256 decode steps, N={N} H={H} d={d} {pv['dtype']} on the "
+                                  f"returned fp32 states (in place)",
+                      "roofline": hbm_roof(dalg, dms, pk, note="the 16 x 96 states (101 MB) "
+                                           "fit in L2, so steps may re-read them from L2")}}
+    if cpu:
+        out["cpu_baseline"] = cpu_baseline(w, args, target_s=4.0, heads=4)
+        dw = dict(kind="decode", S=ST, tokens=toks[:1], N=N, H=H, d=d, label="")
+        out["decode"]["cpu_baseline"] = cpu_baseline(dw, args, target_s=2.0)
+    del w, p, o, ST, S, toks
+    torch.cuda.empty_cache()
+    return out
 
 
 def e2e_prefill(kda, w, steps, stream, world, segments=None):
@@ -655,18 +782,26 @@ def e2e_decode(kda, w, steps, stream, world):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(w, budget_heads=None):
-    """Bounded sample of the workload for the fp64 oracle and its scale factor."""
+def oracle_sample(w, heads=None, tokens=None):
+    """Bounded sample of the workload for the fp64 oracle: the first `heads`
+    heads (default 2 per core) over the first `tokens` tokens of a single
+    sequence (default all), or every sequence of a packed batch; for decode,
+    one session per core.  Returns (run, fraction of the workload, text, cores)."""
     import oracle
     cores = oracle.max_threads()
     if w["kind"] == "prefill":
         p = w["prob"]
         H = w["H"]
-        nh = min(H, budget_heads or max(1, 2 * cores))
+        nh = min(H, heads or max(1, 2 * cores))
         idx = torch.arange(nh, device=p.q.device)
-        q, k, v = (t.index_select(-2, idx) for t in (p.q, p.k, p.v))
-        g = p.log_alpha.index_select(-2, idx)
-        b = p.beta.index_select(-1, idx)
+        sl = lambda t: t
+        T_s = w["Ttot"]
+        if tokens is not None and p.cu_seqlens is None and p.q.dim() == 4 and p.q.shape[0] == 1:
+            T_s = min(tokens, p.q.shape[1])
+            sl = lambda t: t[:, :T_s]
+        q, k, v = (sl(t).index_select(-2, idx) for t in (p.q, p.k, p.v))
+        g = sl(p.log_alpha).index_select(-2, idx)
+        b = sl(p.beta).index_select(-1, idx)
         S0 = None if p.S0 is None else p.S0.index_select(1, idx)
         cu = None if p.cu_seqlens is None else p.cu_seqlens.cpu().numpy()
         args = [oracle._f64(x) for x in (q, k, v, g, b)]
@@ -674,7 +809,9 @@ def oracle_sample(w, budget_heads=None):
 
         def run():
             oracle.fwd(*args, s0, cu)
-        return run, nh / H, f"{nh} of {H} heads, all {w['Ttot']} tokens", cores
+        tok = f"all {w['Ttot']} tokens" if T_s == w["Ttot"] else \
+            f"the first {T_s} of {w['Ttot']} tokens"
+        return run, (nh / H) * (T_s / w["Ttot"]), f"{nh} of {H} heads, {tok}", cores
     S = w["S"]
     x = w["tokens"][0]
     nsess = min(S.shape[0], max(1, cores))
@@ -687,10 +824,10 @@ def oracle_sample(w, budget_heads=None):
     return run, nsess / S.shape[0], f"{nsess} of {S.shape[0]} sessions, all heads", cores
 
 
-def cpu_baseline(w, args, target_s=10.0, max_repeats=50):
+def cpu_baseline(w, args, target_s=10.0, max_repeats=50, heads=None, tokens=None):
     """The oracle on a bounded sample, repeated for about target_s seconds of CPU
     work, scaled to the whole workload."""
-    run, frac, sample, cores = oracle_sample(w)
+    run, frac, sample, cores = oracle_sample(w, heads, tokens)
     run()  # warm (and builds the oracle library if needed)
     repeats = 0
     t0 = time.perf_counter()
@@ -709,29 +846,37 @@ def cpu_baseline(w, args, target_s=10.0, max_repeats=50):
 
 
 def run_reference(args, world, rank):
-    """The oracle, as it stands, on the host cores (rank 0 only)."""
+    """The oracle, as it stands, on the host cores (rank 0 only).  A step is the
+    oracle over a bounded sample of the workload; `ms_per_step` is the
+    sample's own time, and `value` scales the sample's throughput to the
+    workload's unit (`sample_fraction` gives the factor)."""
     if rank != 0:
         return None
     w = make_workload(args.workload, seed=args.seed,
                       device="cuda" if torch.cuda.is_available() else "cpu")
     run, frac, sample, cores = oracle_sample(w)
-    run()  # one untimed call (builds and warms the oracle library)
+    for _ in range(max(1, args.warmup)):  # untimed (the first builds the oracle library)
+        run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         run()
-    dt = (time.perf_counter() - t0) / args.steps / frac
+    dt_sample = (time.perf_counter() - t0) / args.steps
+    dt = dt_sample / frac  # the whole workload at this rate
     if w["kind"] == "prefill":
         value, unit = w["Ttot"] / dt, "tokens/s"
     else:
         value, unit = 2 * nbytes(w["S"]) / dt / 1e9, "GB/s"
     return {"metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt_sample * 1e3, 2),
+            "sample_fraction": round(frac, 6),
+            "ms_per_workload": round(dt * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded)", "impl": "reference",
-            "config": {"workload": w["label"]},
+            "config": line_config(w, world),
             "cpu_baseline": {"value": round(value, 3), "unit": unit, "cores": cores,
                              "kind": "oracle",
-                             "sample": sample + " per step, scaled to the workload"},
+                             "sample": sample + " per step (ms_per_step is the sample's "
+                                                "time; value is scaled to the workload)"},
             "e2e": {"value": round(value, 3), "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

@@ -207,7 +207,8 @@ int kda_fwd_cp_segments(int N, int H, int64_t Ttot);
  *
  * The first call on a device looks up the scratch array's device address
  * (once per device, with that device current); make that first call before
- * any stream capture.  Every call shares the one array: calls that follow one
+ * any stream capture.  The address is kept with the id of the device's
+ * context: after a cudaDeviceReset the next call looks it up again.  Every call shares the one array: calls that follow one
  * another are independent (each clears what must start at zero), but calls
  * that overlap on the GPU -- for example on two streams at once -- race.
  */

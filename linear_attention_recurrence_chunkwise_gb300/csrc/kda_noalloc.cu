@@ -15,6 +15,7 @@
 // over between calls that run one after another.  Calls that overlap on the
 // GPU (for example on two streams at once) share the array and race; issue
 // them one after another.
+#include <cuda.h>
 #include <stdint.h>
 
 #include <mutex>
@@ -33,22 +34,55 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices];
+unsigned long long g_scratch_ctx[kMaxDevices];  // context id the address belongs to
+
+using PfnCtxGetCurrent = CUresult (*)(CUcontext *);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long *);
+
+template <typename Fn>
+Fn driver_entry(const char *name) {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(f);
+}
+
+// Unique id of the context current on this thread (ids are never reused), or
+// 0 when it cannot be read.
+unsigned long long current_context_id() {
+    static const PfnCtxGetCurrent get_current = driver_entry<PfnCtxGetCurrent>("cuCtxGetCurrent");
+    static const PfnCtxGetId get_id = driver_entry<PfnCtxGetId>("cuCtxGetId");
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 // Device address of the scratch array on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up with
-// cudaGetSymbolAddress -- once per device, with that device current -- and
-// cached.
+// cudaGetSymbolAddress at set-up -- once per device, with that device current
+// -- and cached together with the id of the device's context.  Destroying
+// that context (cudaDeviceReset) unloads the library's device code; the next
+// call sees a new context id and looks the address up again instead of using
+// the stale one.  When the id cannot be read the lookup runs on every call.
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    const unsigned long long ctx = current_context_id();
+    if (g_scratch_addr[dev] == nullptr || ctx == 0 || ctx != g_scratch_ctx[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
         g_scratch_addr[dev] = p;
+        // the lookup initialises the context if no call has yet: read the id again
+        g_scratch_ctx[dev] = ctx ? ctx : current_context_id();
     }
     *out = g_scratch_addr[dev];
     return cudaSuccess;

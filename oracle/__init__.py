@@ -44,10 +44,12 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD_DIR, "libkda_oracle.so")
+# test-only build of the same file with the planted mistakes compiled in
+_SO_PLANTS = os.path.join(_BUILD_DIR, "libkda_oracle_plants.so")
 _lock = threading.Lock()
-_handle = None
+_handles = {}
 
-# Planted-mistake codes understood by kda_oracle.c (tests only).
+# Planted-mistake codes understood by the test-only build (mutation check).
 PLANTS = {
     "no_decay": 1,
     "erase_then_decay": 2,
@@ -60,25 +62,26 @@ PLANTS = {
 }
 
 
-def build(force: bool = False) -> str:
-    """Compile kda_oracle.c into a shared library with gcc (-O2, OpenMP)."""
+def build(force: bool = False, plants: bool = False) -> str:
+    """Compile kda_oracle.c into a shared library with gcc (-O2, OpenMP).  With
+    plants=True: the test-only build with the planted mistakes."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
-    if (not force and os.path.exists(_SO)
-            and os.path.getmtime(_SO) >= os.path.getmtime(_SRC)):
-        return _SO
-    tmp = _SO + f".tmp{os.getpid()}"
+    so = _SO_PLANTS if plants else _SO
+    if (not force and os.path.exists(so)
+            and os.path.getmtime(so) >= os.path.getmtime(_SRC)):
+        return so
+    tmp = so + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-           "-o", tmp, _SRC, "-lm"]
+           "-o", tmp, _SRC, "-lm"] + (["-DKDA_ORACLE_PLANTS"] if plants else [])
     subprocess.run(cmd, check=True)
-    os.replace(tmp, _SO)
-    return _SO
+    os.replace(tmp, so)
+    return so
 
 
-def _lib():
-    global _handle
+def _lib(plants: bool = False):
     with _lock:
-        if _handle is None:
-            path = build()
+        if plants not in _handles:
+            path = build(plants=plants)
             lib = ctypes.CDLL(path)
             dp = ctypes.POINTER(ctypes.c_double)
             lp = ctypes.POINTER(ctypes.c_int64)
@@ -90,8 +93,8 @@ def _lib():
             lib.kda_oracle_decode_step.argtypes = [dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, dp]
             lib.kda_oracle_max_threads.restype = ci
             lib.kda_oracle_max_threads.argtypes = []
-            _handle = lib
-    return _handle
+            _handles[plants] = lib
+    return _handles[plants]
 
 
 def _f64(x) -> np.ndarray:
@@ -146,7 +149,7 @@ def fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, erase: bool = True,
     s0 = None if S0 is None else _f64(S0).reshape(N, H, dv, dk)
     o = np.zeros(lead + (H, dv), dtype=np.float64)
     ST = np.zeros((N, H, dv, dk), dtype=np.float64)
-    rc = _lib().kda_oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(s0),
+    rc = _lib(plants=bool(plant)).kda_oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(s0),
                                cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                N, H, dk, dv, int(bool(erase)), int(plant), _ptr(o), _ptr(ST))
     if rc != 0:

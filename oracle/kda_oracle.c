@@ -32,9 +32,12 @@
  * ("Kimi K3 的 KDA", section 5; "完全拆解", degenerate cases).  It exists only
  * so that tests can check the pages' no-erase closed forms.
  *
- * The `plant` argument is for the test suite's mutation check: a nonzero value
- * plants one deliberate, plausible mistake so that the tests can show that the
- * pins catch it.  plant = 0 is the method.
+ * The `plant` argument serves the test suite's mutation check.  Only a second,
+ * test-only build of this file (compiled with -DKDA_ORACLE_PLANTS into
+ * libkda_oracle_plants.so) contains planted mistakes: there a nonzero value
+ * plants one deliberate, plausible slip so that the tests can show that the
+ * pins catch it.  In the oracle proper, kda_token below is the method alone
+ * and a nonzero `plant` is rejected.
  */
 #include <math.h>
 #include <stddef.h>
@@ -45,8 +48,42 @@
 #include <omp.h>
 #endif
 
+/* One token for one (sequence, head): the five steps of the method.  S is the
+ * [dv][dk] memory image (mem[v*dk + c] = S[c][v]); old is scratch of dv. */
+static void kda_token(double *S, const double *q, const double *k, const double *v,
+                      const double *g, double beta, int dk, int dv, int erase,
+                      double *o, double *old)
+{
+    int c, j;
+
+    /* step 1: decay each key channel c of the old state by alpha_c */
+    for (j = 0; j < dv; ++j)
+        for (c = 0; c < dk; ++c) S[(size_t)j * dk + c] *= exp(g[c]);
+
+    /* step 2: old = Sbar^T k (the decayed state's answer along the current key) */
+    for (j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (c = 0; c < dk; ++c) acc += S[(size_t)j * dk + c] * k[c];
+        old[j] = erase ? acc : 0.0;
+    }
+
+    /* steps 3-4: erase the conflicting part along k, write the new value */
+    for (j = 0; j < dv; ++j) {
+        const double err = v[j] - old[j];
+        for (c = 0; c < dk; ++c) S[(size_t)j * dk + c] += beta * k[c] * err;
+    }
+
+    /* step 5: read the updated state with the query */
+    for (j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (c = 0; c < dk; ++c) acc += S[(size_t)j * dk + c] * q[c];
+        o[j] = acc;
+    }
+}
+
+#ifdef KDA_ORACLE_PLANTS
+/* Test-only: the token step with one planted mistake (mutation check). */
 enum {
-    PLANT_NONE = 0,
     PLANT_NO_DECAY = 1,          /* alpha ignored */
     PLANT_ERASE_THEN_DECAY = 2,  /* (I - b k k^T) applied before Diag(alpha) */
     PLANT_ERASE_SIGN = 3,        /* v + old instead of v - old */
@@ -54,20 +91,18 @@ enum {
     PLANT_TRANSPOSED_OLD = 5,    /* old[v] = sum_c Sbar[v][c] k[c]  (needs dk == dv) */
     PLANT_DECAY_VALUE_AXIS = 6,  /* Diag(alpha) applied along v (needs dk == dv) */
     PLANT_BETA_ON_ERASE_ONLY = 7,/* write term without beta */
-    PLANT_STALE_GATE = 8         /* alpha of the previous token */
+    PLANT_STALE_GATE = 8,        /* alpha of the previous token */
+    PLANT_LAST = 8
 };
 
-/* One token for one (sequence, head).  S is the [dv][dk] memory image.
- * g_prev is only used by PLANT_STALE_GATE. */
-static void kda_token(double *S, const double *q, const double *k, const double *v,
-                      const double *g, const double *g_prev, double beta,
-                      int dk, int dv, int erase, int plant, double *o, double *old)
+static void planted_token(double *S, const double *q, const double *k, const double *v,
+                          const double *g, const double *g_prev, double beta,
+                          int dk, int dv, int erase, int plant, double *o, double *old)
 {
     int c, j;
     const double *gate = (plant == PLANT_STALE_GATE) ? g_prev : g;
 
     if (plant == PLANT_ERASE_THEN_DECAY) {
-        /* deliberately wrong order: erase/write on the undecayed state, then decay */
         for (j = 0; j < dv; ++j) {
             double acc = 0.0;
             for (c = 0; c < dk; ++c) acc += S[(size_t)j * dk + c] * k[c];
@@ -84,8 +119,6 @@ static void kda_token(double *S, const double *q, const double *k, const double 
         }
         return;
     }
-
-    /* step 1: decay each key channel c of the old state by alpha_c */
     if (plant != PLANT_NO_DECAY) {
         for (j = 0; j < dv; ++j)
             for (c = 0; c < dk; ++c) {
@@ -93,8 +126,6 @@ static void kda_token(double *S, const double *q, const double *k, const double 
                 S[(size_t)j * dk + c] *= a;
             }
     }
-
-    /* read-before-write mistake: read the decayed state */
     if (plant == PLANT_READ_BEFORE_WRITE) {
         for (j = 0; j < dv; ++j) {
             double acc = 0.0;
@@ -102,8 +133,6 @@ static void kda_token(double *S, const double *q, const double *k, const double 
             o[j] = acc;
         }
     }
-
-    /* step 2: old = Sbar^T k (the decayed state's answer along the current key) */
     for (j = 0; j < dv; ++j) {
         double acc = 0.0;
         if (plant == PLANT_TRANSPOSED_OLD) {
@@ -113,21 +142,15 @@ static void kda_token(double *S, const double *q, const double *k, const double 
         }
         old[j] = erase ? acc : 0.0;
     }
-
-    /* steps 3-4: erase the conflicting part along k, write the new value */
     for (j = 0; j < dv; ++j) {
-        double err;
-        if (plant == PLANT_ERASE_SIGN) err = v[j] + old[j];
-        else err = v[j] - old[j];
+        const double err = (plant == PLANT_ERASE_SIGN) ? v[j] + old[j] : v[j] - old[j];
         for (c = 0; c < dk; ++c) {
-            double upd;
-            if (plant == PLANT_BETA_ON_ERASE_ONLY) upd = k[c] * v[j] - beta * k[c] * old[j];
-            else upd = beta * k[c] * err;
+            const double upd = (plant == PLANT_BETA_ON_ERASE_ONLY)
+                                   ? k[c] * v[j] - beta * k[c] * old[j]
+                                   : beta * k[c] * err;
             S[(size_t)j * dk + c] += upd;
         }
     }
-
-    /* step 5: read the updated state with the query */
     if (plant != PLANT_READ_BEFORE_WRITE) {
         for (j = 0; j < dv; ++j) {
             double acc = 0.0;
@@ -136,6 +159,9 @@ static void kda_token(double *S, const double *q, const double *k, const double 
         }
     }
 }
+#else
+enum { PLANT_LAST = 0 };
+#endif
 
 /*
  * Forward over packed sequences.
@@ -155,7 +181,10 @@ int kda_oracle_fwd(const double *q, const double *k, const double *v,
     int bad = 0;
     if (!q || !k || !v || !log_alpha || !beta || !cu_seqlens || !o) return -1;
     if (N < 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+    if (plant < 0 || plant > PLANT_LAST) return -1;
+#ifdef KDA_ORACLE_PLANTS
     if ((plant == PLANT_TRANSPOSED_OLD || plant == PLANT_DECAY_VALUE_AXIS) && dk != dv) return -1;
+#endif
     if (cu_seqlens[0] != 0) return -1;
     for (p = 0; p < N; ++p)
         if (cu_seqlens[p + 1] < cu_seqlens[p]) return -1;
@@ -175,9 +204,16 @@ int kda_oracle_fwd(const double *q, const double *k, const double *v,
         else memset(S, 0, sizeof(double) * state);
         for (t = cu_seqlens[n]; t < cu_seqlens[n + 1]; ++t) {
             const size_t row = (size_t)t * H + h;
-            const double *g_prev = (t > cu_seqlens[n]) ? log_alpha + (row - H) * dk : zero_gate;
-            kda_token(S, q + row * dk, k + row * dk, v + row * dv, log_alpha + row * dk, g_prev,
-                      beta[row], dk, dv, erase, plant, o + row * dv, old);
+#ifdef KDA_ORACLE_PLANTS
+            if (plant) {
+                const double *g_prev = (t > cu_seqlens[n]) ? log_alpha + (row - H) * dk : zero_gate;
+                planted_token(S, q + row * dk, k + row * dk, v + row * dv, log_alpha + row * dk,
+                              g_prev, beta[row], dk, dv, erase, plant, o + row * dv, old);
+                continue;
+            }
+#endif
+            kda_token(S, q + row * dk, k + row * dk, v + row * dv, log_alpha + row * dk,
+                      beta[row], dk, dv, erase, o + row * dv, old);
         }
         if (S_T) memcpy(S_T + ((size_t)n * H + h) * state, S, sizeof(double) * state);
         free(S);
@@ -204,8 +240,8 @@ int kda_oracle_decode_step(const double *q, const double *k, const double *v,
         double *old = (double *)malloc(sizeof(double) * dv);
         if (!old) { bad |= 1; continue; }
         kda_token(S + (size_t)p * dk * dv, q + (size_t)p * dk, k + (size_t)p * dk,
-                  v + (size_t)p * dv, log_alpha + (size_t)p * dk, log_alpha + (size_t)p * dk,
-                  beta[p], dk, dv, 1, PLANT_NONE, o + (size_t)p * dv, old);
+                  v + (size_t)p * dv, log_alpha + (size_t)p * dk, beta[p], dk, dv, 1,
+                  o + (size_t)p * dv, old);
         free(old);
     }
     return bad ? -1 : 0;

@@ -41,6 +41,8 @@ def call_noalloc(lib, prob, o, S_T, status, stream):
 
 
 def test_noalloc_matches_kda_fwd_on_two_calls_in_a_row(kda):
+    """Two calls in a row, each against kda_fwd on the same inputs: the same
+    kernels run on the same data, so o and S_T agree bit for bit."""
     lib = kda.load()
     stream = torch.cuda.current_stream()
     cases = [([300, 64, 1, 129, 0], 21), ([1000, 7, 250], 22)]
@@ -56,8 +58,41 @@ def test_noalloc_matches_kda_fwd_on_two_calls_in_a_row(kda):
         torch.cuda.synchronize()
         assert rc == kda.KDA_OK
         assert int(status.item()) == kda.KDA_OK
+        assert torch.equal(o, o_ref)
+        assert torch.equal(S_T, S_ref)
+        # and within the oracle's tolerance of kda_fwd, as every engine is
         assert rel_err(o, o_ref.double().cpu().numpy()) < 2e-2
-        assert rel_err(S_T, S_ref.double().cpu().numpy()) < 1e-2
+
+
+def test_noalloc_error_status_then_a_clean_call(kda):
+    """Device-side cu_seqlens that decrease: the call returns KDA_OK on the host
+    (it cannot see device memory), reports KDA_ERR_INVALID_ARGUMENT through
+    device_status and writes no output.  The status lives in the shared scratch
+    array; the next, valid call clears it, reports KDA_OK and matches kda_fwd."""
+    lib = kda.load()
+    stream = torch.cuda.current_stream()
+    prob = I.prefill_problem(1, 0, 2, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=23,
+                             device=DEV, lengths=[50, 50])
+    good_cu = prob.cu_seqlens
+    prob.cu_seqlens = torch.tensor([0, 70, 60], dtype=torch.int32, device=DEV)  # decreasing
+    o = torch.full_like(prob.v, 7.0)
+    S_T = torch.full_like(prob.S0, 7.0)
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    rc = call_noalloc(lib, prob, o, S_T, status, stream)
+    torch.cuda.synchronize()
+    assert rc == kda.KDA_OK
+    assert int(status.item()) == kda.KDA_ERR_INVALID_ARGUMENT
+    assert bool((o == 7.0).all()) and bool((S_T == 7.0).all())
+    prob.cu_seqlens = good_cu
+    status.fill_(-1)
+    rc = call_noalloc(lib, prob, o, S_T, status, stream)
+    torch.cuda.synchronize()
+    assert rc == kda.KDA_OK
+    assert int(status.item()) == kda.KDA_OK
+    o_ref, S_ref = kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0,
+                               prob.cu_seqlens)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(S_T, S_ref)
 
 
 def test_noalloc_rejects_more_sequences_than_its_scratch_holds(kda):
