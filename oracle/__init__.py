@@ -24,6 +24,15 @@ Contents
     beta_i and the S_0 term; both are restored here, since unrolling the
     recurrence S_t = A_t S_{t-1} + beta_t k_t v_t^T produces them).
 
+``gated_rmsnorm``
+    The output epilogue of a KDA layer, per (token, head): a head-wise RMSNorm
+    over the value channels times a per-channel weight, then the sigmoid output
+    gate, y = sigmoid(g) * w * o / sqrt(mean_v(o^2) + eps) ("Kimi K3 模型结构（1）",
+    output section: per-head RMSNorm over the 128 channels, sigmoid gate on each
+    normalised channel; "Kimi K3" (gentlecold) section 3.2, y = W_o[Sigmoid(W_g x)
+    . RMSNorm(o~)]; "完全拆解", the KDA layer's output).  numpy, the definition
+    written out.
+
 ``verify_tokens`` / ``commit_tokens``
     Speculative-decode verification and commit over K cached draft tokens
     ("Kimi K3 深度拆解" section 9.2), written out as K (or n_accept[n]) calls of
@@ -173,6 +182,20 @@ def decode_step(q, k, v, log_alpha, beta, S):
     if rc != 0:
         raise ValueError("kda_oracle_decode_step rejected its arguments")
     return o, S
+
+
+def gated_rmsnorm(o, g, weight=None, eps=0.0):
+    """y = sigmoid(g) * weight * o / sqrt(mean over the last axis of o^2 + eps).
+
+    o, g: [..., dv] (any leading shape: tokens, heads); weight: [dv] or None
+    (ones); eps >= 0.  The mean runs over the value channels of one (token,
+    head) only.  Returns float64 of o's shape."""
+    o, g = _f64(o), _f64(g)
+    w = np.ones(o.shape[-1]) if weight is None else _f64(weight)
+    ms = np.mean(o * o, axis=-1, keepdims=True)          # mean square per (token, head)
+    with np.errstate(over="ignore"):
+        gate = 1.0 / (1.0 + np.exp(-g))                  # sigmoid
+    return o / np.sqrt(ms + eps) * w * gate
 
 
 def verify_tokens(q, k, v, log_alpha, beta, S):

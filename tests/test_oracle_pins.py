@@ -217,3 +217,60 @@ def test_verify_and_commit_compose_like_a_prefill():
             np.testing.assert_allclose(Sc[n:n + 1], Sa, rtol=1e-12, atol=1e-12)
         else:
             np.testing.assert_array_equal(Sc[n], S[n])
+
+
+# ---------------------------------------------------------------- output epilogue
+# y = sigmoid(g) * w * o / sqrt(mean_v(o^2) + eps), per (token, head) ("Kimi K3 模型
+# 结构（1）", output section: head-wise RMSNorm over the value channels and a sigmoid
+# gate on each normalised channel).  Each pin below is fixed by the definition
+# or by arithmetic done by hand, not by the oracle's own formula.
+
+def test_gated_rmsnorm_worked_example():
+    """o = (3, 4), g = (0, ln 3), w = (1, 2), eps = 1/2, worked by hand: the
+    mean square is (9 + 16) / 2 = 12.5, plus eps is 13; sigmoid(0) = 1/2 and
+    sigmoid(ln 3) = 3 / 4; so y = (3 * 1 * 1/2, 4 * 2 * 3/4) / sqrt(13)."""
+    y = oracle.gated_rmsnorm(np.array([3.0, 4.0]), np.array([0.0, np.log(3.0)]),
+                             np.array([1.0, 2.0]), eps=0.5)
+    assert np.allclose(y, np.array([1.5, 6.0]) / np.sqrt(13.0), rtol=1e-15, atol=0)
+
+
+def test_gated_rmsnorm_saturated_gate_gives_unit_rms_per_head():
+    """A gate far above zero passes everything (sigmoid = 1 in fp64), and with
+    w = 1, eps = 0 every (token, head) row then has mean square exactly 1 --
+    per head, even when the heads' scales differ by orders of magnitude (a norm
+    over the wrong axis fails this)."""
+    rng = np.random.default_rng(31)
+    o = rng.standard_normal((5, 3, 16)) * np.array([1e-3, 1.0, 1e3])[None, :, None]
+    y = oracle.gated_rmsnorm(o, np.full(o.shape, 60.0), None, eps=0.0)
+    assert np.allclose(np.mean(y * y, axis=-1), 1.0, rtol=1e-13, atol=0)
+    assert np.allclose(np.sign(y), np.sign(o))
+
+
+def test_gated_rmsnorm_scale_invariant_without_eps():
+    """With eps = 0 the output does not depend on the scale of o (the RMS norm
+    divides it out); with eps > 0 a tiny o is no longer blown up to unit RMS."""
+    rng = np.random.default_rng(32)
+    o = rng.standard_normal((4, 2, 8))
+    g = rng.standard_normal((4, 2, 8))
+    w = rng.uniform(0.5, 2.0, 8)
+    y1 = oracle.gated_rmsnorm(o, g, w, eps=0.0)
+    y2 = oracle.gated_rmsnorm(7.25 * o, g, w, eps=0.0)
+    assert np.allclose(y1, y2, rtol=1e-13, atol=0)
+    y3 = oracle.gated_rmsnorm(1e-6 * o, g, w, eps=1.0)
+    assert np.abs(y3).max() < 1e-5
+
+
+def test_gated_rmsnorm_gate_is_the_logistic_function():
+    """Dividing out the normalised value leaves exactly the gate, which must be
+    the logistic function of g (scipy's expit, an independent routine); g = 0
+    halves the plain RMS norm."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(33)
+    o = rng.standard_normal((6, 2, 8)) + 3.0            # no zero entries
+    g = rng.uniform(-8.0, 8.0, o.shape)
+    w = rng.uniform(0.5, 2.0, 8)
+    y = oracle.gated_rmsnorm(o, g, w, eps=0.25)
+    plain = oracle.gated_rmsnorm(o, np.full(o.shape, 60.0), w, eps=0.25)
+    assert np.allclose(y / plain, special.expit(g), rtol=1e-13, atol=0)
+    half = oracle.gated_rmsnorm(o, np.zeros(o.shape), w, eps=0.25)
+    assert np.allclose(half, 0.5 * plain, rtol=1e-15, atol=0)
