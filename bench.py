@@ -8,7 +8,10 @@ metric state-GB/s = 2 * state bytes / step time -- and a ``draft`` object:
 speculative decode on the same state, verify 8 draft tokens then commit them
 (kda_verify_tokens + kda_commit_tokens), metric draft tokens/s -- and a
 ``segment_parallel`` object: the long prefill of 12 heads (B=1, T=131072) with
-kda_fwd_cp against the plain kda_fwd.
+kda_fwd_cp against the plain kda_fwd -- and ``epilogue``, ``long`` and
+``varlen`` objects: the layer's output epilogue fused against a separate pass,
+the long prefill with carry-in (T=131072) and the varlen batch (16 packed
+sequences, then 256 decode steps on the returned states).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload prefill|decode|long|long_tp8|varlen]
@@ -404,6 +407,7 @@ def run_ours(args, world, rank):
             line["decode"] = decode_sub(kda, args, stream, pk, cpu)
             line["draft"] = draft_sub(kda, args, stream, pk, line["decode"]["us_per_step"])
             line["segment_parallel"] = cp_sub(kda, args, stream, pk)
+            line["epilogue"] = epilogue_sub(kda, args, stream, pk)
             line["long"] = long_sub(kda, args, stream, pk, cpu)
             line["varlen"] = varlen_sub(kda, args, stream, pk, cpu)
     else:
@@ -563,6 +567,48 @@ def prefill_roofline(w, ms, pk):
                    "frac": round(tf / pk["bf16"], 4), "flops_per_launch": prefill_flops(w),
                    "flop_count": "6Td^2+3TCd+TC^2 per head (pages' formula)"}
     return r
+
+
+def epilogue_sub(kda, args, stream, pk):
+    """The layer's output epilogue (head-wise RMSNorm times a sigmoid gate) on
+    the prefill and decode workloads, fused into the kernel against a separate
+    pass, same box: the A/B behind KDA_EPILOGUE_AUTO's choice."""
+    out = {"metric": "us per call", "unit": "us"}
+    w = make_workload("prefill", seed=args.seed, device="cuda")
+    p = w["prob"]
+    gen = torch.Generator(device="cuda").manual_seed(args.seed + 7)
+    g = (2 * torch.randn(p.v.shape, generator=gen, device="cuda")).to(p.v.dtype)
+    nw = torch.rand(w["d"], generator=gen, device="cuda") + 0.5
+    y = torch.empty_like(p.v)
+    ST = torch.empty((p.n_seq, w["H"], w["d"], w["d"]), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.kda_fwd_workspace_bytes(p.n_seq), dtype=torch.uint8, device="cuda")
+    for mode in ("fused", "separate"):
+        ms = time_calls(lambda: kda.kda_fwd_gated(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0,
+                                                  g=g, norm_weight=nw, y=y, S_T=ST,
+                                                  workspace=ws, epilogue=mode, stream=stream),
+                        10, stream)
+        out[f"prefill_{mode}_us"] = round(ms * 1e3, 2)
+    out["prefill_plain_us"] = round(time_calls(
+        lambda: kda.kda_fwd(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0, o=y, S_T=ST, workspace=ws,
+                            stream=stream), 10, stream) * 1e3, 2)
+    del w, p, g, y, ST
+    wd = make_workload("decode", seed=args.seed, device="cuda")
+    x = wd["tokens"][0]
+    gd = (2 * torch.randn(x["v"].shape, generator=gen, device="cuda")).to(x["v"].dtype)
+    yd = torch.empty_like(x["v"])
+    for mode in ("fused", "separate"):
+        ms = time_calls(lambda: kda.kda_decode_step_gated(
+            x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], wd["S"], g=gd, norm_weight=nw,
+            y=yd, epilogue=mode, stream=stream), 100, stream)
+        out[f"decode_{mode}_us"] = round(ms * 1e3, 2)
+    out["decode_plain_us"] = round(time_calls(
+        lambda: kda.kda_decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], wd["S"],
+                                    o=yd, stream=stream), 100, stream) * 1e3, 2)
+    out["workloads"] = "prefill B=1 H=96 T=8192 d=128 bf16; decode step N=64 H=96 d=128"
+    out["auto_choice"] = {"prefill": "separate", "decode": "fused"}
+    del wd
+    torch.cuda.empty_cache()
+    return out
 
 
 def long_sub(kda, args, stream, pk, cpu=False):

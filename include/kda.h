@@ -234,6 +234,62 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
                              void *o, void *stream);
 
 /*
+ * Output epilogue of a KDA layer, fused or as a pass of its own.
+ *
+ * After the recurrence, each head's output goes through a head-wise RMSNorm
+ * over its d_v value channels and a sigmoid output gate, before the output
+ * projection ("Kimi K3 模型结构（1）", output section: the norm runs per head
+ * over the 128 channels and the sigmoid gate acts on every normalised channel;
+ * "Kimi K3模型架构详解" section 3.2: y_t = W_o[Sigmoid(W_g x_t) . RMSNorm(o~_t)];
+ * "完全拆解", the KDA layer).  Per (token, head):
+ *
+ *     y_v = sigmoid(g_v) * w_v * o_v / sqrt(mean_v'(o_v'^2) + eps)
+ *
+ * g holds the gate logits W_g x (the projection stays with the caller), w the
+ * norm's per-channel weight, shared by all heads (NULL: ones), eps >= 0 the
+ * norm's epsilon (with eps = 0 an all-zero o row gives NaN).  g and y have o's
+ * layout and dtype.  The pages give neither eps nor where w lives; the
+ * caller passes both.
+ *
+ * `mode` chooses where the epilogue runs: KDA_EPILOGUE_FUSED inside the
+ * kernel's output stores (o never reaches HBM), KDA_EPILOGUE_SEPARATE as a
+ * second pass (the kernel writes o into y, then kda_gated_rmsnorm runs on y
+ * in place), KDA_EPILOGUE_AUTO the one measured faster on GB300: separate for
+ * the prefill (its output stores sit on the latency-bound carry chain, where
+ * the fused work costs more than the separate bandwidth-bound pass), fused for
+ * the decode step.  Both give the same y up to rounding order.
+ *
+ * kda_fwd_gated: kda_fwd whose output is y instead of o.  g: [Ttot, H, d_v],
+ * 16-byte aligned.  FUSED needs the tensor-core engine (KDA_ERR_UNSUPPORTED
+ * otherwise).  Other arguments, engines, errors and device status as
+ * kda_fwd_engine.
+ * kda_decode_step_gated: kda_decode_step with the epilogue (g [N, H, d_v],
+ * y [N, H, d_v]).
+ * kda_gated_rmsnorm: the epilogue alone over `rows` rows of d_v channels
+ * (rows = tokens x heads); o, g, y 16-byte aligned; y may alias o.
+ */
+typedef enum {
+    KDA_EPILOGUE_AUTO = 0,
+    KDA_EPILOGUE_FUSED = 1,
+    KDA_EPILOGUE_SEPARATE = 2
+} kda_epilogue_t;
+kda_status_t kda_fwd_gated(const void *q, const void *k, const void *v,
+                           const float *log_alpha, const float *beta, const float *S0,
+                           const int32_t *cu_seqlens, int B, int T, int H, int d_k, int d_v,
+                           int N, kda_dtype_t dtype, const void *g, const float *norm_weight,
+                           float eps, void *y, float *S_T, void *workspace,
+                           size_t workspace_bytes, void *stream, kda_engine_t engine,
+                           kda_epilogue_t mode);
+kda_status_t kda_decode_step_gated(const void *q, const void *k, const void *v,
+                                   const float *log_alpha, const float *beta, float *S,
+                                   int N, int H, int d_k, int d_v, kda_dtype_t dtype,
+                                   const void *g, const float *norm_weight, float eps,
+                                   void *y, void *stream, kda_epilogue_t mode);
+kda_status_t kda_gated_rmsnorm(const void *o, const void *g, const float *norm_weight,
+                               float eps, int64_t rows, int d_v, kda_dtype_t dtype, void *y,
+                               void *stream);
+
+/*
  * Speculative-decode verification and commit ("Kimi K3 深度拆解" section 9.2:
  * the draft tokens' projected inputs are kept instead of a copy of the state
  * per draft position; after verification the accepted tokens are replayed on

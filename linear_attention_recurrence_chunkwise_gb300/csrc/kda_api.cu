@@ -147,6 +147,59 @@ kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status_t kda_gated_rmsnorm(const void *o, const void *g, const float *norm_weight,
+                               float eps, int64_t rows, int d_v, kda_dtype_t dtype, void *y,
+                               void *stream) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (rows < 0 || d_v <= 0 || !(eps >= 0.f) || eps > 3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
+    if (d_v != 64 && d_v != 128) return KDA_ERR_UNSUPPORTED;
+    if (rows == 0) return KDA_OK;
+    if (!o || !g || !y || !aligned16(o) || !aligned16(g) || !aligned16(y) ||
+        (norm_weight && !aligned(norm_weight, 4)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (fault_injected()) return KDA_ERR_CUDA;
+    const cudaError_t e = kda::launch_gated_rmsnorm(o, g, norm_weight, eps, rows, d_v, dtype, y,
+                                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_fwd_gated(const void *q, const void *k, const void *v, const float *log_alpha,
+                           const float *beta, const float *S0, const int32_t *cu_seqlens,
+                           int B, int T, int H, int d_k, int d_v, int N, kda_dtype_t dtype,
+                           const void *g, const float *norm_weight, float eps, void *y,
+                           float *S_T, void *workspace, size_t workspace_bytes, void *stream,
+                           kda_engine_t engine, kda_epilogue_t mode) {
+    if (mode != KDA_EPILOGUE_AUTO && mode != KDA_EPILOGUE_FUSED && mode != KDA_EPILOGUE_SEPARATE)
+        return KDA_ERR_INVALID_ARGUMENT;
+    kda::FwdParams p;
+    bool use_tc = false;
+    const kda_status_t st = check_fwd(q, k, v, log_alpha, beta, S0, cu_seqlens, B, T, H, d_k,
+                                      d_v, N, dtype, y, S_T, workspace, engine, p, use_tc);
+    if (st != KDA_OK) return st;
+    if (!(eps >= 0.f) || eps > 3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
+    if (p.Ttot > 0 && (!g || !aligned16(g))) return KDA_ERR_INVALID_ARGUMENT;
+    if (norm_weight && !aligned(norm_weight, 4)) return KDA_ERR_INVALID_ARGUMENT;
+    if (mode == KDA_EPILOGUE_FUSED && !use_tc) return KDA_ERR_UNSUPPORTED;
+    if (workspace_bytes < kda_fwd_workspace_bytes(N)) return KDA_ERR_WORKSPACE;
+    if (fault_injected()) return KDA_ERR_CUDA;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (kda::launch_schedule(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (N == 0) return KDA_OK;
+    cudaError_t e;
+    if (mode == KDA_EPILOGUE_FUSED) {  // in the tensor-core kernel's output stores
+        p.gate = g;
+        p.norm_w = norm_weight;
+        p.eps = eps;
+        e = kda::launch_prefill_tc(p, s);
+    } else {  // o into y, then the epilogue in place (measured faster: AUTO)
+        e = use_tc ? kda::launch_prefill_tc(p, s) : kda::launch_prefill_simt(p, dtype, s);
+        if (e == cudaSuccess)
+            e = kda::launch_gated_rmsnorm(y, g, norm_weight, eps, p.Ttot * H, d_v, dtype, y, s);
+    }
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 size_t kda_fwd_cp_workspace_bytes(int N, int H, int d_k, int d_v, int segments) {
     if (segments < 1 || H <= 0 || !supported_dims(d_k, d_v)) return 0;
     const size_t base = kda_fwd_workspace_bytes(N);
@@ -234,6 +287,39 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v,
     if (fault_injected()) return KDA_ERR_CUDA;
     const cudaError_t e = kda::launch_decode(q, k, v, log_alpha, beta, S, N, H, d_k, dtype, o,
                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_decode_step_gated(const void *q, const void *k, const void *v,
+                                   const float *log_alpha, const float *beta, float *S, int N,
+                                   int H, int d_k, int d_v, kda_dtype_t dtype, const void *g,
+                                   const float *norm_weight, float eps, void *y, void *stream,
+                                   kda_epilogue_t mode) {
+    if (mode != KDA_EPILOGUE_AUTO && mode != KDA_EPILOGUE_FUSED && mode != KDA_EPILOGUE_SEPARATE)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (N < 0 || H <= 0 || d_k <= 0 || d_v <= 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!(eps >= 0.f) || eps > 3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
+    if (!supported_dims(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)N * H > INT32_MAX) return KDA_ERR_INVALID_ARGUMENT;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !S || !y || !g) return KDA_ERR_INVALID_ARGUMENT;
+    const unsigned elem = dtype == KDA_BF16 ? 2u : 4u;
+    if (!aligned(q, elem) || !aligned(k, elem) || !aligned(v, elem) || !aligned(y, elem) ||
+        !aligned(g, elem) || !aligned(log_alpha, 4) || !aligned(beta, 4) || !aligned16(S) ||
+        (norm_weight && !aligned(norm_weight, 4)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (fault_injected()) return KDA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (mode == KDA_EPILOGUE_SEPARATE) {
+        e = kda::launch_decode(q, k, v, log_alpha, beta, S, N, H, d_k, dtype, y, s);
+        if (e == cudaSuccess)
+            e = kda::launch_gated_rmsnorm(y, g, norm_weight, eps, (int64_t)N * H, d_v, dtype, y, s);
+    } else {  // fused (measured faster: AUTO)
+        e = kda::launch_decode(q, k, v, log_alpha, beta, S, N, H, d_k, dtype, y, s, g,
+                               norm_weight, eps);
+    }
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -41,6 +41,10 @@ struct FwdParams {
                                 // kTaskVZero tasks for the tensor-core engine)
     int32_t *status;            // workspace status word
     const int32_t *order;       // workspace launch order, nullptr for fixed length
+    const void *gate;           // fused output epilogue (tensor-core engine): gate
+                                // logits [Ttot][H][d_v] in the io dtype, or nullptr
+    const float *norm_w;        // its per-channel weight [d_v], or nullptr (ones)
+    float eps;                  // its epsilon
     int64_t Ttot;
     int T;                      // tokens per sequence when cu_seqlens is null
     int H, N, dk, dv;
@@ -109,6 +113,21 @@ __device__ __forceinline__ bool in_bounds(int32_t *status, size_t idx, size_t n)
 #endif
 }
 
+// Output epilogue of a KDA layer (head-wise RMSNorm times a sigmoid gate):
+// y_v = sigmoid(g_v) w_v o_v / sqrt(mean_v(o_v^2) + eps) per (token, head).
+// The logistic function for fp32 outputs: 1 / (1 + 2^(-x log2 e)) with the
+// fast exponential and an IEEE reciprocal (relative error ~1e-7).
+__device__ __forceinline__ float sigmoid_f32(float x) {
+    return __frcp_rn(1.f + __expf(-x));
+}
+// For bf16 outputs: (1 + tanh(x / 2)) / 2 with the hardware tanh (one MUFU
+// operation, absolute error about 2^-11, below the bf16 rounding of y).
+__device__ __forceinline__ float sigmoid_bf16out(float x) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+    return fmaf(0.5f, t, 0.5f);
+}
+
 // Workspace of the segment-parallel forward (byte offsets; [0, 4) is the status
 // word): task tables of pass A (N (2P - 1) tasks) and pass D (N (P - 1)), the
 // zero V source, and the state sets ([H][d][d] fp32 each) S_a (end of segment
@@ -134,6 +153,12 @@ cudaError_t launch_commit(const void *q, const void *k, const void *v, const flo
                           int H, int d, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_decode(const void *q, const void *k, const void *v,
                           const float *log_alpha, const float *beta, float *S, int N,
-                          int H, int d, kda_dtype_t dt, void *o, cudaStream_t s);
+                          int H, int d, kda_dtype_t dt, void *o, cudaStream_t s,
+                          const void *gate = nullptr, const float *norm_w = nullptr,
+                          float eps = 0.f);
+// y = gated RMSNorm of o over rows of d channels (y may alias o).
+cudaError_t launch_gated_rmsnorm(const void *o, const void *gate, const float *norm_w,
+                                 float eps, int64_t rows, int d, kda_dtype_t dt, void *y,
+                                 cudaStream_t s);
 
 }  // namespace kda

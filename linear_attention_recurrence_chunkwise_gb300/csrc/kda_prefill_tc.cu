@@ -47,7 +47,15 @@
 // the bf16 stores of T''s diagonal blocks from the solve's first step to its
 // idle warps in the second, which pays only on a busy GPU.
 //
-// Every wait is bounded in time; on a timeout the kernel records
+// kGated fuses the layer's output epilogue into the output stores: once the
+// carry warps have staged a chunk's bf16 o tile, two threads per token read
+// its row back, reduce its mean square over the 128 value channels (one
+// shuffle joins the halves), read the gate logits from global memory and
+// overwrite the row with y = sigmoid(g) w o / sqrt(mean(o^2) + eps) before
+// the TMA store, so the unnormalised o never reaches HBM ("Kimi K3 模型结构（1）"
+// output section: head-wise RMSNorm and sigmoid gate).
+//
+// Every mbarrier wait is bounded in time; on a timeout the kernel records
 // KDA_ERR_TIMEOUT, runs its remaining steps without waiting, drains its own
 // copies and MMAs, frees tensor memory and exits.
 #include <cuda.h>
@@ -55,6 +63,7 @@
 #include <cuda_bf16.h>
 
 #include <atomic>
+#include <cstddef>
 
 #include "kda_internal.h"
 #include "kda_sm100.cuh"
@@ -104,10 +113,16 @@ struct __align__(1024) TcSmem {
     float as[C * LDA];  // solve matrix / inverse blocks (fp32)
     uint64_t full[2], ready[2], gfull, tpfull;
     uint64_t bar_r, bar_u, bar_o, bar_s, bar_fin, tailfree[2];
+    alignas(16) float wn[D];  // epilogue: the norm weight (ones when none is given), read as float4
     uint32_t tmem_base;
     int abort;
     int domain;
 };
+
+// members read or written with 16-byte vector accesses
+static_assert(offsetof(TcSmem, wn) % 16 == 0 && offsetof(TcSmem, as) % 16 == 0 &&
+                  offsetof(TcStage, gam) % 16 == 0 && offsetof(TcStage, bet) % 16 == 0,
+              "16-byte vector accesses need 16-byte aligned members");
 
 // Wait for a phase; on timeout (or once any thread has timed out) return
 // without waiting so that every thread still reaches every barrier.
@@ -203,6 +218,7 @@ struct SerialStage {
     float red_o[C * Serial<D>::kParts * D];
 };
 
+template <bool kGated>
 __device__ __forceinline__ void serial_head(const FwdParams *pp, uint8_t *smem_raw,
                                          int64_t start, int len, int h, const StateRef &sref) {
     const FwdParams &p = *pp;
@@ -262,13 +278,43 @@ __device__ __forceinline__ void serial_head(const FwdParams *pp, uint8_t *smem_r
                                          ss.bet, D, nt, ss.red_r, ss.red_o, o, 0, 0, 0,
                                          p.status, 1);
         __syncthreads();
-        for (int idx = tid; idx < (no_out ? 0 : nt * D); idx += kThreads) {
-            const int r = idx / D, vv = idx % D;
-            float ov = 0.f;
+        if constexpr (kGated) {
+            // one warp per token: the output epilogue over its 128 channels
+            const int warp = tid >> 5, lane = tid & 31;
+            const __nv_bfloat16 *gt = static_cast<const __nv_bfloat16 *>(p.gate);
+            for (int r = warp; r < nt; r += kThreads / 32) {
+                float ov[4], ssq = 0.f;
 #pragma unroll
-            for (int j = 0; j < P; ++j) ov += ss.red_o[(r * P + j) * D + vv];
-            const size_t oi = row0 + (size_t)r * p.H * D + vv;
-            if (in_bounds(p.status, oi, n_tok)) o[oi] = __float2bfloat16_rn(ov);
+                for (int e = 0; e < 4; ++e) {
+                    const int vv = lane + 32 * e;
+                    ov[e] = 0.f;
+#pragma unroll
+                    for (int j = 0; j < P; ++j) ov[e] += ss.red_o[(r * P + j) * D + vv];
+                    ssq = fmaf(ov[e], ov[e], ssq);
+                }
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, m);
+                const float rs = rsqrtf(ssq * (1.f / D) + p.eps);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int vv = lane + 32 * e;
+                    const size_t oi = row0 + (size_t)r * p.H * D + vv;
+                    if (in_bounds(p.status, oi, n_tok)) {
+                        const float wv = p.norm_w ? p.norm_w[vv] : 1.f;
+                        o[oi] = __float2bfloat16_rn(
+                            ov[e] * rs * wv * sigmoid_bf16out(__bfloat162float(gt[oi])));
+                    }
+                }
+            }
+        } else {
+            for (int idx = tid; idx < (no_out ? 0 : nt * D); idx += kThreads) {
+                const int r = idx / D, vv = idx % D;
+                float ov = 0.f;
+#pragma unroll
+                for (int j = 0; j < P; ++j) ov += ss.red_o[(r * P + j) * D + vv];
+                const size_t oi = row0 + (size_t)r * p.H * D + vv;
+                if (in_bounds(p.status, oi, n_tok)) o[oi] = __float2bfloat16_rn(ov);
+            }
         }
     }
     if (stepper && sref.S_T) {
@@ -280,7 +326,7 @@ __device__ __forceinline__ void serial_head(const FwdParams *pp, uint8_t *smem_r
 
 // kTasks: task-table mode (segment-parallel forward); the plain instantiation
 // compiles none of its per-task choices.
-template <bool kTasks, bool kFullGrid>
+template <bool kTasks, bool kFullGrid, bool kGated>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -288,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_o,
                       const __grid_constant__ CUtensorMap tm_g,
                       const __grid_constant__ CUtensorMap tm_vz) {
+    static_assert(!(kTasks && kGated), "the fused epilogue serves plain calls only");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Align by offsetting the shared-memory pointer itself (not through an
     // integer round trip), so the compiler keeps every access in the shared
@@ -341,6 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&sm.tpfull), 1);
         fence_mbar_init();
     }
+    if constexpr (kGated)
+        if (tid < D) sm.wn[tid] = p.norm_w ? p.norm_w[tid] : 1.f;
     if (warp == kPrepWarp0) {
         tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
         tmem_relinquish();
@@ -663,9 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O^T of chunk n (lane v, column r) -> staged tile [r][v] in sm.ut (two
         // 64-channel slabs, 128-byte swizzle) -> global: one TMA store per slab
         // for a full chunk; a masked copy for the last, partial chunk.
-        auto store_output = [&](int n) {
-            const int64_t t0 = start + (int64_t)n * C;
-            const int valid = min(C, len - n * C);
+        // stage_output: O^T of chunk n (lane v, column r) -> staged bf16 tile,
+        // which frees the O accumulator; finish_output: the epilogue (kGated)
+        // and the store.  store_output does both.
+        auto stage_output = [&](int n) {
             uint8_t *stage = sm.ut + (v >> 6) * 8192;
             const int vc = v & 63;
             // this column's byte offset in a row r of the swizzled tile depends
@@ -684,6 +734,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __float2bfloat16_rn(__uint_as_float(x[j]));
                 }
             }
+        };
+        auto finish_output = [&](int n) {
+            const int64_t t0 = start + (int64_t)n * C;
+            const int valid = min(C, len - n * C);
+            if constexpr (kGated) {
+                // output epilogue over the staged bf16 tile (the caller has
+                // synchronised the carry warps after staging), one row per two
+                // threads: thread et takes token r = et / 2, channels
+                // 64 (et % 2) .. + 63 (one 128-byte row of slab et % 2)
+                const int r = et >> 1, half = et & 1;
+                uint8_t *row = sm.ut + half * 8192 + (r >> 3) * 1024 + (r & 7) * 128;
+                const bool live = r < valid;
+                uint4 gq[8];
+                const uint4 *gsrc = reinterpret_cast<const uint4 *>(
+                    static_cast<const __nv_bfloat16 *>(p.gate) +
+                    ((size_t)(t0 + (live ? r : 0)) * p.H + h) * D + 64 * half);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    gq[j] = live && in_bounds(p.status, ((size_t)(t0 + r) * p.H + h) * D + 64 * half + 8 * j + 7, n_tok)
+                                ? gsrc[j] : make_uint4(0, 0, 0, 0);
+                uint4 oq[8];
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    oq[j] = *reinterpret_cast<const uint4 *>(row + ((j ^ (r & 7)) << 4));
+                    float f[8];
+                    unpack8(oq[j], f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);  // the row's other half
+                const float rs = rsqrtf(ss * (1.f / D) + p.eps);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float f[8], gf[8];
+                    unpack8(oq[j], f);
+                    unpack8(gq[j], gf);
+                    const float4 w0 = *reinterpret_cast<const float4 *>(&sm.wn[64 * half + 8 * j]);
+                    const float4 w1 = *reinterpret_cast<const float4 *>(&sm.wn[64 * half + 8 * j + 4]);
+                    const float wj[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = f[e] * (rs * wj[e]) * sigmoid_bf16out(gf[e]);
+                    *reinterpret_cast<uint4 *>(row + ((j ^ (r & 7)) << 4)) = pack8(f);
+                }
+            }
+            // every thread's writes to the tile are done and visible to the
+            // async proxy before one thread hands it to the TMA store
             tc_fence_before();
             fence_proxy_async_smem();
             named_bar_sync(kBarCarry, kCarryThreads);
@@ -707,10 +804,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         };
+        auto store_output = [&](int n) {
+            stage_output(n);
+            if constexpr (kGated) named_bar_sync(kBarCarry, kCarryThreads);
+            finish_output(n);
+        };
 
         for (int n = 0; n < nchunks; ++n) {
             const int s = n & 1;
             TcStage &S = sm.st[s];
+            if constexpr (kGated) {
+                // the gate rows of chunk n into L2 (one 128-byte line per
+                // thread): its epilogue reads them one chunk from now
+                const int r = et >> 1;
+                if (r < min(C, len - n * C))
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                        static_cast<const __nv_bfloat16 *>(p.gate) +
+                        ((size_t)(start + (int64_t)n * C + r) * p.H + h) * D + 64 * (et & 1)));
+            }
             // a4: W^T = Kh^T T'^T, U~^T = V^T T'^T (M = 128, N = 64, K = 64) once
             // the chunk-local warps have T'
             if (issuer) {
@@ -764,18 +875,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(smem_u32(&sm.bar_u));
             }
             __syncwarp();
-            if (n >= 1) store_output(n - 1);  // frees the O accumulator
-            if (issuer) {  // O^T = S^T Qh^T
-                tc_fence_after();
-                const uint32_t id_o = idesc_bf16(128, 64, false, false);
-                const uint64_t bq0 = desc_sw128(smem_u32(S.kq) + 8192, 16, 1024);
+            auto issue_o = [&] {  // O^T = S^T Qh^T
+                if (issuer) {
+                    tc_fence_after();
+                    const uint32_t id_o = idesc_bf16(128, 64, false, false);
+                    const uint64_t bq0 = desc_sw128(smem_u32(S.kq) + 8192, 16, 1024);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mma_bf16_tmem_a(tmem + kColO, tmem + kColSb + 8 * k,
-                                    bq0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2), id_o, k > 0);
-                mma_commit(smem_u32(&sm.bar_o));
+                    for (int k = 0; k < 8; ++k)
+                        mma_bf16_tmem_a(tmem + kColO, tmem + kColSb + 8 * k,
+                                        bq0 + (uint64_t)((k >> 2) * 1024 + (k & 3) * 2), id_o,
+                                        k > 0);
+                    mma_commit(smem_u32(&sm.bar_o));
+                }
+                __syncwarp();
+            };
+            if constexpr (kGated) {
+                // the staged tile frees the O accumulator; the epilogue and the
+                // store of chunk n - 1 then run while the U and O products do
+                if (n >= 1) {
+                    stage_output(n - 1);
+                    tc_fence_before();
+                    named_bar_sync(kBarCarry, kCarryThreads);
+                }
+                issue_o();
+                if (n >= 1) finish_output(n - 1);
+            } else {
+                if (n >= 1) store_output(n - 1);  // frees the O accumulator
+                issue_o();
             }
-            __syncwarp();
             wait_phase_warp(sm.bar_u, n & 1, abort);
             if (issuer) bulk_wait_group_read0();  // the previous output tile has left sm.ut
             named_bar_sync(kBarCarry, kCarryThreads);
@@ -893,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (sm.domain && !sm.abort) serial_head(&p, smem_raw, start, len, h, sref);
+    if (sm.domain && !sm.abort) serial_head<kGated>(&p, smem_raw, start, len, h, sref);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -984,8 +1111,13 @@ cudaError_t launch_prefill_tc(const FwdParams &p, cudaStream_t s) {
     // on one head per SM for 96-304 blocks)
     const size_t blocks = (size_t)p.N * p.H;
     const bool full = blocks * 8 > (size_t)sm_count() * 7;
-    auto kern = p.tasks ? (full ? prefill_tc_kernel<true, true> : prefill_tc_kernel<true, false>)
-                        : (full ? prefill_tc_kernel<false, true> : prefill_tc_kernel<false, false>);
+    if (p.gate && p.tasks) return cudaErrorInvalidValue;
+    auto kern = p.tasks  ? (full ? prefill_tc_kernel<true, true, false>
+                                 : prefill_tc_kernel<true, false, false>)
+                : p.gate ? (full ? prefill_tc_kernel<false, true, true>
+                                 : prefill_tc_kernel<false, false, true>)
+                         : (full ? prefill_tc_kernel<false, true, false>
+                                 : prefill_tc_kernel<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

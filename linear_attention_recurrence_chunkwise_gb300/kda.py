@@ -27,11 +27,13 @@ KDA_ERR_BOUNDS = 7
 
 KDA_F32, KDA_BF16 = 0, 1
 ENGINES = {"auto": 0, "tensorcore": 1, "cudacore": 2}
+EPILOGUES = {"auto": 0, "fused": 1, "separate": 2}
 
 # every symbol include/kda.h declares
 EXPORTED = ["kda_fwd_workspace_bytes", "kda_fwd", "kda_fwd_engine", "kda_fwd_noalloc",
             "kda_fwd_cp", "kda_fwd_cp_workspace_bytes", "kda_fwd_cp_segments",
             "kda_decode_step", "kda_verify_tokens", "kda_commit_tokens",
+            "kda_fwd_gated", "kda_decode_step_gated", "kda_gated_rmsnorm",
             "kda_read_device_status", "kda_state_bytes", "kda_status_string"]
 KDA_NOALLOC_MAX_SEQS = 16384
 KDA_MAX_DRAFT_TOKENS = 16
@@ -86,6 +88,14 @@ def load_library(path: str) -> ctypes.CDLL:
     lib.kda_verify_tokens.argtypes = [vp, vp, vp, fp, fp, fp, ci, ci, ci, ci, ci, ci, vp, vp]
     lib.kda_commit_tokens.restype = ci
     lib.kda_commit_tokens.argtypes = [vp, vp, vp, fp, fp, fp, vp, ci, ci, ci, ci, ci, ci, vp]
+    cf = ctypes.c_float
+    lib.kda_fwd_gated.restype = ci
+    lib.kda_fwd_gated.argtypes = fwd_args[:14] + [vp, fp, cf] + fwd_args[14:] + [ci, ci]
+    lib.kda_decode_step_gated.restype = ci
+    lib.kda_decode_step_gated.argtypes = [vp, vp, vp, fp, fp, fp, ci, ci, ci, ci, ci, vp, fp, cf,
+                                          vp, vp, ci]
+    lib.kda_gated_rmsnorm.restype = ci
+    lib.kda_gated_rmsnorm.argtypes = [vp, vp, fp, cf, ctypes.c_int64, ci, ci, vp, vp]
     lib.kda_read_device_status.restype = ci
     lib.kda_read_device_status.argtypes = [vp, sz, vp]
     lib.kda_state_bytes.restype = sz
@@ -217,6 +227,60 @@ def kda_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, o=None, S_T=N
     return o, S_T
 
 
+def _check_gate(g, norm_weight, like, dev):
+    """The gate logits share o's shape and dtype; the norm weight is fp32 [d_v]."""
+    _check(g, "g", like.dtype, dev)
+    _check_shape(g, "g", like.shape)
+    if norm_weight is not None:
+        _check(norm_weight, "norm_weight", torch.float32, dev)
+        _check_shape(norm_weight, "norm_weight", (like.shape[-1],))
+
+
+def kda_fwd_gated(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *, g, norm_weight=None,
+                  eps: float = 1e-6, y=None, S_T=None, workspace=None,
+                  return_state: bool = True, engine: str = "auto", epilogue: str = "auto",
+                  stream=None, lib=None):
+    """kda_fwd followed by the layer's output epilogue, y = sigmoid(g) * w * o /
+    sqrt(mean(o^2) + eps) per (token, head).  g: gate logits shaped like v;
+    norm_weight: fp32 [d_v] or None; epilogue: 'auto', 'fused' (in the
+    tensor-core kernel's output stores) or 'separate' (a second pass).
+    Returns (y, S_T)."""
+    B, T, H, d_k, d_v, N, y, S_T = _fwd_args(q, k, v, log_alpha, beta, S0, cu_seqlens, y,
+                                             S_T, return_state)
+    _check_gate(g, norm_weight, y, q.device)
+    lib = lib or load()
+    if workspace is None:
+        workspace = torch.empty(int(lib.kda_fwd_workspace_bytes(N)), dtype=torch.uint8,
+                                device=q.device)
+    _check(workspace, "workspace", None, q.device)
+    rc = lib.kda_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                           _ptr(cu_seqlens), B, T, H, d_k, d_v, N, _dtype_code(q.dtype),
+                           _ptr(g), _ptr(norm_weight), float(eps), _ptr(y), _ptr(S_T),
+                           _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream(stream), ENGINES[engine], EPILOGUES[epilogue])
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_fwd_gated")
+    return y, S_T
+
+
+def kda_gated_rmsnorm(o, g, norm_weight=None, eps: float = 1e-6, *, y=None, stream=None):
+    """The output epilogue alone over the last axis: y = sigmoid(g) * w * o /
+    sqrt(mean(o^2) + eps).  y may be o itself (in place).  Returns y."""
+    _check(o, "o", o.dtype, o.device)
+    _check_gate(g, norm_weight, o, o.device)
+    if y is None:
+        y = torch.empty_like(o)
+    _check(y, "y", o.dtype, o.device)
+    _check_shape(y, "y", o.shape)
+    d_v = o.shape[-1]
+    rows = o.numel() // d_v if d_v else 0
+    rc = load().kda_gated_rmsnorm(_ptr(o), _ptr(g), _ptr(norm_weight), float(eps), rows, d_v,
+                                  _dtype_code(o.dtype), _ptr(y), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_gated_rmsnorm")
+    return y
+
+
 def kda_fwd_cp_workspace_bytes(N: int, H: int, d_k: int, d_v: int, segments: int) -> int:
     return int(load().kda_fwd_cp_workspace_bytes(N, H, d_k, d_v, segments))
 
@@ -304,6 +368,39 @@ def kda_decode_step(q, k, v, log_alpha, beta, S, *, o=None, stream=None):
     if rc != KDA_OK:
         raise KdaError(rc, "kda_decode_step")
     return o
+
+
+def kda_decode_step_gated(q, k, v, log_alpha, beta, S, *, g, norm_weight=None,
+                          eps: float = 1e-6, y=None, epilogue: str = "auto", stream=None):
+    """kda_decode_step with the output epilogue: returns y [N, H, d_v] =
+    sigmoid(g) * w * o / sqrt(mean(o^2) + eps); S is updated in place.
+    epilogue: 'auto', 'fused' or 'separate'."""
+    dev, dt = q.device, q.dtype
+    _check(q, "q", dt), _check(k, "k", dt, dev), _check(v, "v", dt, dev)
+    _check(log_alpha, "log_alpha", torch.float32, dev)
+    _check(beta, "beta", torch.float32, dev)
+    _check(S, "S", torch.float32, dev)
+    if q.dim() != 3:
+        raise ValueError("decode inputs are [N, H, d]")
+    N, H, d_k = q.shape
+    d_v = v.shape[-1]
+    if k.shape != q.shape or log_alpha.shape != q.shape or v.shape[:-1] != q.shape[:-1] \
+            or beta.shape != q.shape[:-1]:
+        raise ValueError("q, k, v, log_alpha, beta shapes disagree")
+    if S.shape != (N, H, d_v, d_k):
+        raise ValueError(f"S must be [N, H, d_v, d_k] = {(N, H, d_v, d_k)}")
+    if y is None:
+        y = torch.empty((N, H, d_v), dtype=dt, device=dev)
+    _check(y, "y", dt, dev)
+    _check_shape(y, "y", (N, H, d_v))
+    _check_gate(g, norm_weight, y, dev)
+    rc = load().kda_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                      _ptr(S), N, H, d_k, d_v, _dtype_code(dt), _ptr(g),
+                                      _ptr(norm_weight), float(eps), _ptr(y), _stream(stream),
+                                      EPILOGUES[epilogue])
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step_gated")
+    return y
 
 
 def _check_draft(q, k, v, log_alpha, beta, S):

@@ -44,3 +44,15 @@ def oracle_on_heads(prob, heads):
     S0 = None if prob.S0 is None else prob.S0.index_select(1, idx)
     cu = None if prob.cu_seqlens is None else prob.cu_seqlens.cpu().numpy()
     return oracle.fwd(q, k, v, g, b, S0, cu)
+
+
+_ORACLE_CACHE = {}
+
+
+def cached_oracle(key, prob, heads):
+    """The oracle's (o, S_T) on `heads` of a workload, computed once per test
+    session: every engine and every test of the same seeded workload compares
+    against the same fp64 run."""
+    if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE[key] = oracle_on_heads(prob, heads)
+    return _ORACLE_CACHE[key]

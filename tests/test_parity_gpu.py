@@ -15,7 +15,7 @@ import torch
 import oracle
 from linear_attention_recurrence_chunkwise_gb300 import build as kbuild
 from linear_attention_recurrence_chunkwise_gb300 import inputs as I
-from tests.gpu_util import oracle_on_heads, rel_err, tol_o, tol_s
+from tests.gpu_util import cached_oracle, oracle_on_heads, rel_err, tol_o, tol_s
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -477,17 +477,6 @@ def test_workload_tiny_fp32(kda, engine):
     print(f"[parity] tiny {engine}: o {eo:.2e} S {es:.2e}")
     assert eo < 1e-4
     assert es < 1e-4
-
-
-_ORACLE_CACHE = {}
-
-
-def cached_oracle(key, prob, heads):
-    """The oracle's (o, S_T) on `heads` of a workload, computed once per test
-    session: every engine compares against the same fp64 run."""
-    if key not in _ORACLE_CACHE:
-        _ORACLE_CACHE[key] = oracle_on_heads(prob, heads)
-    return _ORACLE_CACHE[key]
 
 
 @pytest.mark.parametrize("engine", ENGINES)
