@@ -12,7 +12,8 @@
 //   pass A  segment 0 from the real S0 (outputs and end state), and for every
 //           later segment j two state-only runs: S~_j (from S0 = 0) and M_j
 //           (v = 0 and S0 = I, so the end state is M_j I = M_j);
-//   scan    S_in(1) = end of segment 0; S_in(j+1) = M_j S_in(j) + S~_j;
+//   scan    S_in(1) = end of segment 0; S_in(j+1) = M_j S_in(j) + S~_j (fp32
+//           accuracy from three tf32 tensor-core products per tile);
 //   pass D  every later segment again from its S_in, writing its outputs; the
 //           last one writes S_T.
 // Both passes are the ordinary prefill kernels in task-table mode (one task per
@@ -94,25 +95,53 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// x rounded to the nearest tf32 value (ties away from zero), as its fp32 bit
+// pattern, and the remainder: x = hi + lo
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    hi = (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
+    lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
+// d (16 x 8, fp32) += a (16 x 8) b (8 x 8) with tf32 operands (mma.sync m16n8k8)
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // S_in of every later segment: X <- X M + S~ in fp32.  Row v of X M is row v
-// of X times M, so the rows are independent: a block takes kScanRows rows of
-// one (sequence, head) through all its segments, 16 threads per row, each
-// D / 16 consecutive columns.  M_{j+1} lands in shared memory (cp.async, two
-// buffers) while step j computes, and the thread's S~ values are loaded before
-// its product, so a step waits on no global load.
+// of X times M, so the rows are independent: a block takes kScanRows = 16 rows
+// of one (sequence, head) through all its segments.  The product is an m = 16
+// tensor-core tile: warp w owns output columns D / 8 w .. + D / 8 (one or two
+// m16n8 tiles), takes the k = 8 slices of X (A) and M (B) from shared memory
+// and splits each operand into a tf32 high part and the remainder, so that
+// high x high + high x low + low x high gives the product to fp32 accuracy
+// (the low x low term is below it).  The accumulators start from S~.  M_{j+1}
+// lands in shared memory (cp.async, two buffers) while step j computes; X and
+// M rows are padded (4 and 8 floats) so that the fragment loads of a warp hit
+// 32 different banks.
 constexpr int kScanRows = 16;
+template <int D>
+constexpr size_t scan_smem_bytes() {
+    return (2 * (size_t)D * (D + 8) + (size_t)kScanRows * (D + 4)) * sizeof(float);
+}
 template <int D>
 __global__ void __launch_bounds__(kScanThreads) cp_scan_kernel(int N, int P, int H,
                                                                 CpLayout L, uint8_t *ws) {
     int32_t *status = reinterpret_cast<int32_t *>(ws);
     if (*status == KDA_ERR_INVALID_ARGUMENT) return;
     extern __shared__ __align__(16) float cp_smem[];
-    float *Mbuf = cp_smem;           // two M_j [a][c] buffers
-    float *X = Mbuf + 2 * D * D;     // this block's rows of X [r][a]
-    constexpr int kBlocks = D / kScanRows, kCols = D / 16;
+    constexpr int kLdM = D + 8, kLdX = D + 4;
+    constexpr int kTiles = D / 64;  // m16n8 output tiles per warp (8 warps)
+    float *Mbuf = cp_smem;                 // two M_j [a][c] buffers, rows of kLdM
+    float *X = Mbuf + 2 * D * kLdM;        // this block's rows of X [r][a], rows of kLdX
+    constexpr int kBlocks = D / kScanRows;
     const int nh = blockIdx.x / kBlocks, v0 = kScanRows * (blockIdx.x % kBlocks);
     const int n = nh / H, h = nh % H, tid = threadIdx.x;
-    const int r = tid / 16, c0 = kCols * (tid % 16);
+    const int lane = tid & 31, warp = tid >> 5, g = lane >> 2, t4 = lane & 3;
     const size_t blk = (size_t)H * D * D, hoff = (size_t)h * D * D + (size_t)v0 * D;
     const float *sa = reinterpret_cast<const float *>(ws + L.s_a) + n * blk + hoff;
     const float *st = reinterpret_cast<const float *>(ws + L.s_t);
@@ -128,46 +157,78 @@ __global__ void __launch_bounds__(kScanThreads) cp_scan_kernel(int N, int P, int
     // M_j into buffer (j - 1) % 2; every thread copies the same pieces each time
     auto stage_m = [&](int j) {
         const float *mj = mt + seg(j) + (size_t)h * D * D;
-        float *dst = Mbuf + ((j - 1) & 1) * D * D;
-        for (int i = tid; i < D * D / 4; i += kScanThreads) cp_async16(dst + 4 * i, mj + 4 * i);
+        float *dst = Mbuf + ((j - 1) & 1) * D * kLdM;
+        for (int i = tid; i < D * D / 4; i += kScanThreads) {
+            const int a = i / (D / 4), c = 4 * (i % (D / 4));
+            cp_async16(dst + a * kLdM + c, mj + a * D + c);
+        }
         cp_async_commit();
     };
-    for (int i = tid; i < kScanRows * D / 4; i += kScanThreads)
-        reinterpret_cast<float4 *>(X)[i] = reinterpret_cast<const float4 *>(sa)[i];
+    for (int i = tid; i < kScanRows * D / 4; i += kScanThreads) {
+        const int r = i / (D / 4), c = 4 * (i % (D / 4));
+        *reinterpret_cast<float4 *>(X + r * kLdX + c) =
+            *reinterpret_cast<const float4 *>(sa + r * D + c);
+    }
     if (P > 2) stage_m(1);
     for (int j = 1; j < P; ++j) {
         __syncthreads();  // X complete; the last product has read its M buffer
-        for (int i = tid; i < kScanRows * D / 4; i += kScanThreads)
-            reinterpret_cast<float4 *>(sin + seg(j) + hoff)[i] = reinterpret_cast<const float4 *>(X)[i];
+        for (int i = tid; i < kScanRows * D / 4; i += kScanThreads) {
+            const int r = i / (D / 4), c = 4 * (i % (D / 4));
+            *reinterpret_cast<float4 *>(sin + seg(j) + hoff + r * D + c) =
+                *reinterpret_cast<const float4 *>(X + r * kLdX + c);
+        }
         if (j == P - 1) break;
-        float add[kCols];  // this thread's S~_j entries
-        const float *stj = st + seg(j) + hoff + (size_t)r * D + c0;
+        // an empty segment's map is exactly (I, 0): X passes through unchanged
+        // (bit for bit, which the tensor-core product would not give)
+        const SegTask *td = reinterpret_cast<const SegTask *>(ws + L.tasks_d);
+        const bool empty = td[(size_t)n * (P - 1) + (j - 1)].len == 0;
+        // accumulators start from this warp's entries of S~_j: tile nt covers
+        // columns c0 .. c0 + 7; lane (g, t4) holds rows g, g + 8, columns
+        // c0 + 2 t4, + 1
+        float acc[kTiles][3][4];
+        const float *stj = st + seg(j) + hoff;
 #pragma unroll
-        for (int k = 0; k < kCols; k += 4) {
-            const float4 x4 = *reinterpret_cast<const float4 *>(stj + k);
-            add[k] = x4.x, add[k + 1] = x4.y, add[k + 2] = x4.z, add[k + 3] = x4.w;
+        for (int nt = 0; nt < kTiles; ++nt) {
+            const int col = (D / 8) * warp + 8 * nt + 2 * t4;
+            const float2 s0 = *reinterpret_cast<const float2 *>(stj + (size_t)g * D + col);
+            const float2 s1 = *reinterpret_cast<const float2 *>(stj + (size_t)(g + 8) * D + col);
+            acc[nt][2][0] = s0.x, acc[nt][2][1] = s0.y, acc[nt][2][2] = s1.x, acc[nt][2][3] = s1.y;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][0][e] = acc[nt][1][e] = 0.f;
         }
         cp_async_wait_all();
         __syncthreads();  // M_j in place
         if (j + 1 < P - 1) stage_m(j + 1);
-        const float *M = Mbuf + ((j - 1) & 1) * D * D;
-        float acc[kCols];
+        if (empty) continue;  // (the next step's first barrier follows)
+        const float *M = Mbuf + ((j - 1) & 1) * D * kLdM;
+#pragma unroll 4
+        for (int k0 = 0; k0 < D; k0 += 8) {
+            uint32_t ah[4], al[4];  // A = X[r][k0 + k]: (g, t4), (g + 8, t4), (g, t4 + 4), (g + 8, t4 + 4)
+            split_tf32(X[g * kLdX + k0 + t4], ah[0], al[0]);
+            split_tf32(X[(g + 8) * kLdX + k0 + t4], ah[1], al[1]);
+            split_tf32(X[g * kLdX + k0 + t4 + 4], ah[2], al[2]);
+            split_tf32(X[(g + 8) * kLdX + k0 + t4 + 4], ah[3], al[3]);
 #pragma unroll
-        for (int k = 0; k < kCols; ++k) acc[k] = add[k];
-        for (int a = 0; a < D; ++a) {
-            const float x = X[r * D + a];
-#pragma unroll
-            for (int k = 0; k < kCols; k += 4) {
-                const float4 m = *reinterpret_cast<const float4 *>(&M[a * D + c0 + k]);
-                acc[k] = fmaf(x, m.x, acc[k]);
-                acc[k + 1] = fmaf(x, m.y, acc[k + 1]);
-                acc[k + 2] = fmaf(x, m.z, acc[k + 2]);
-                acc[k + 3] = fmaf(x, m.w, acc[k + 3]);
+            for (int nt = 0; nt < kTiles; ++nt) {
+                const int c = (D / 8) * warp + 8 * nt + g;  // B = M[k0 + k][c]: k = t4, t4 + 4
+                uint32_t bh0, bl0, bh1, bl1;
+                split_tf32(M[(k0 + t4) * kLdM + c], bh0, bl0);
+                split_tf32(M[(k0 + t4 + 4) * kLdM + c], bh1, bl1);
+                mma_tf32(acc[nt][0], al, bh0, bh1);
+                mma_tf32(acc[nt][1], ah, bl0, bl1);
+                mma_tf32(acc[nt][2], ah, bh0, bh1);
             }
         }
         __syncthreads();  // every product has read X
 #pragma unroll
-        for (int k = 0; k < kCols; ++k) X[r * D + c0 + k] = acc[k];
+        for (int nt = 0; nt < kTiles; ++nt) {
+            const int col = (D / 8) * warp + 8 * nt + 2 * t4;
+            float r[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) r[e] = (acc[nt][0][e] + acc[nt][1][e]) + acc[nt][2][e];
+            *reinterpret_cast<float2 *>(X + g * kLdX + col) = make_float2(r[0], r[1]);
+            *reinterpret_cast<float2 *>(X + (g + 8) * kLdX + col) = make_float2(r[2], r[3]);
+        }
     }
     cp_async_wait_all();  // nothing in flight at exit
 }
@@ -220,15 +281,19 @@ cudaError_t launch_fwd_cp(const FwdParams &base, kda_dtype_t dt, bool use_tc, in
         return use_tc ? launch_prefill_tc(p, s) : launch_prefill_simt(p, dt, s);
     };
     if ((e = run(L.tasks_a, N * (2 * P - 1))) != cudaSuccess) return e;
-    const size_t smem = (2 * (size_t)d * d + (size_t)kScanRows * d) * sizeof(float);
     const unsigned grid = (unsigned)((size_t)N * H * (d / kScanRows));
     if (d == 128) {
+        constexpr size_t smem = scan_smem_bytes<128>();  // 146 KB
         e = cudaFuncSetAttribute(cp_scan_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         cp_scan_kernel<128><<<grid, kScanThreads, smem, s>>>(N, P, H, L, ws);
     } else {
-        cp_scan_kernel<64><<<grid, kScanThreads, smem, s>>>(N, P, H, L, ws);  // 36 KB
+        constexpr size_t smem = scan_smem_bytes<64>();  // 40 KB
+        e = cudaFuncSetAttribute(cp_scan_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        cp_scan_kernel<64><<<grid, kScanThreads, smem, s>>>(N, P, H, L, ws);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return run(L.tasks_d, N * (P - 1));
