@@ -5,7 +5,10 @@ Each translation unit under ``csrc/`` compiles in parallel to an object in
 shared CUDA runtime (so the library and PyTorch share one runtime).  Only
 stale objects are rebuilt.  ``build(bounds_check=True)`` makes the
 bounds-checked variant ``libkda_bounds.so`` (objects in ``_build_bounds/``),
-whose kernels check every computed global index and report KDA_ERR_BOUNDS.
+whose kernels check every computed global index and report KDA_ERR_BOUNDS;
+``build(timeout_probe=True)`` makes the test-only ``libkda_timeout.so``, in
+which one wait of the tensor-core prefill runs out after 2 ms (the tests of
+the timeout path use it).
 Run ``python -m linear_attention_recurrence_chunkwise_gb300.build``.
 """
 from __future__ import annotations
@@ -25,6 +28,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkda.so")
 BUILD_BOUNDS = os.path.join(PKG, "_build_bounds")
 LIB_BOUNDS = os.path.join(PKG, "libkda_bounds.so")
+BUILD_TIMEOUT = os.path.join(PKG, "_build_timeout")
+LIB_TIMEOUT = os.path.join(PKG, "libkda_timeout.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -33,13 +38,17 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else (shutil.which("nvcc") or "nvcc")
 
 
-def _flags(verbose_ptxas: bool, bounds_check: bool = False):
+def _flags(verbose_ptxas: bool, bounds_check: bool = False, timeout_probe: bool = False):
     f = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                 "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
     if bounds_check:
         f += ["-DKDA_BOUNDS_CHECK=1"]
+    if timeout_probe:
+        # test-only: a 2 ms wait limit and one mbarrier arrive left out, so a
+        # wait of the tensor-core prefill runs out of time (the timeout path)
+        f += ["-DKDA_WAIT_LIMIT_NS=2000000ull", "-DKDA_TEST_SKIP_ARRIVE=1"]
     return f
 
 
@@ -50,8 +59,9 @@ def _deps_mtime() -> float:
 
 
 def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None,
-          bounds_check: bool = False) -> str:
-    build_dir, lib_path = (BUILD_BOUNDS, LIB_BOUNDS) if bounds_check else (BUILD, LIB)
+          bounds_check: bool = False, timeout_probe: bool = False) -> str:
+    build_dir, lib_path = (BUILD_BOUNDS, LIB_BOUNDS) if bounds_check else \
+        (BUILD_TIMEOUT, LIB_TIMEOUT) if timeout_probe else (BUILD, LIB)
     os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_t = _deps_mtime()
@@ -67,7 +77,7 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
     def compile_one(item):
         s, obj = item
         tmp = obj + f".tmp{os.getpid()}"
-        cmd = [nvcc(), "-c", s, "-o", tmp] + _flags(verbose_ptxas, bounds_check)
+        cmd = [nvcc(), "-c", s, "-o", tmp] + _flags(verbose_ptxas, bounds_check, timeout_probe)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(s)}:\n{r.stderr}")

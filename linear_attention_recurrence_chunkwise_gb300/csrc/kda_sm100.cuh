@@ -10,8 +10,12 @@ namespace kda {
 namespace sm100 {
 
 // A wait that has not completed after this long gives up (the kernel then
-// records KDA_ERR_TIMEOUT and winds down instead of spinning forever).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// records KDA_ERR_TIMEOUT and winds down instead of spinning forever).  2 s;
+// the test-only build of the timeout path sets a few milliseconds.
+#ifndef KDA_WAIT_LIMIT_NS
+#define KDA_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = KDA_WAIT_LIMIT_NS;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
