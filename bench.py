@@ -210,12 +210,18 @@ def line_config(w, world):
     return c
 
 
-def time_calls(fn, reps, stream, warm=2):
-    """Mean device time of one call of fn (CUDA events on `stream`)."""
+def time_calls(fn, reps, stream, warm=2, warm_s=0.3):
+    """Mean device time of one call of fn (CUDA events on `stream`), after at
+    least `warm` calls and `warm_s` seconds of untimed calls (the clocks ramp
+    up from idle after the CPU-only phases of the run)."""
+    t_end = time.time() + warm_s
     with torch.cuda.stream(stream):
-        for _ in range(warm):
-            fn()
-    stream.synchronize()
+        while warm > 0:
+            for _ in range(warm):
+                fn()
+            stream.synchronize()
+            if time.time() >= t_end:
+                break
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         a.record(stream)
@@ -620,7 +626,7 @@ def long_sub(kda, args, stream, pk, cpu=False):
     ST = torch.empty_like(p.S0)
     ws = torch.empty(kda.kda_fwd_workspace_bytes(p.n_seq), dtype=torch.uint8, device="cuda")
     ms = time_calls(lambda: kda.kda_fwd(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0, o=o, S_T=ST,
-                                        workspace=ws, stream=stream), 5, stream)
+                                        workspace=ws, stream=stream), 10, stream)
     out = {"metric": "tokens/s", "value": round(w["Ttot"] / (ms / 1e3), 1), "unit": "tokens/s",
            "workload": w["label"], "ms_per_call": round(ms, 3),
            "roofline": prefill_roofline(w, ms, pk)}
@@ -642,7 +648,7 @@ def varlen_sub(kda, args, stream, pk, cpu=False):
     ws = torch.empty(kda.kda_fwd_workspace_bytes(p.n_seq), dtype=torch.uint8, device="cuda")
     ms = time_calls(lambda: kda.kda_fwd(p.q, p.k, p.v, p.log_alpha, p.beta, p.S0,
                                         p.cu_seqlens, o=o, S_T=ST, workspace=ws,
-                                        stream=stream), 5, stream)
+                                        stream=stream), 10, stream)
     pv = I.PRESETS["varlen"]
     N, H, d = p.n_seq, w["H"], w["d"]
     toks = [I.decode_token(N, H, d, d, pv["dtype"], pv["la"], args.seed + 1, s, "cuda")
