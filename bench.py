@@ -179,6 +179,13 @@ def nbytes(*ts):
 # ------------------------------------------------------------------ workloads
 
 def make_workload(name, seed, device):
+    w = _make_workload(name, seed, device)
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()  # generated on the current stream; timed on another
+    return w
+
+
+def _make_workload(name, seed, device):
     if name == "decode":
         p = I.PRESETS["decode"]
         S = I.decode_state(p["N"], p["H"], p["d"], p["d"], p["s0_std"], seed, device)
@@ -214,6 +221,7 @@ def time_calls(fn, reps, stream, warm=2, warm_s=0.3):
     """Mean device time of one call of fn (CUDA events on `stream`), after at
     least `warm` calls and `warm_s` seconds of untimed calls (the clocks ramp
     up from idle after the CPU-only phases of the run)."""
+    torch.cuda.synchronize()  # inputs made on another stream are complete
     t_end = time.time() + warm_s
     with torch.cuda.stream(stream):
         while warm > 0:
@@ -414,6 +422,7 @@ def run_ours(args, world, rank):
             line["draft"] = draft_sub(kda, args, stream, pk, line["decode"]["us_per_step"])
             line["segment_parallel"] = cp_sub(kda, args, stream, pk)
             line["epilogue"] = epilogue_sub(kda, args, stream, pk)
+            line["wide_gates"] = wide_gates_sub(kda, args, stream, pk)
             line["long"] = long_sub(kda, args, stream, pk, cpu)
             line["varlen"] = varlen_sub(kda, args, stream, pk, cpu)
     else:
@@ -455,6 +464,7 @@ def decode_sub(kda, args, stream, pk, cpu=False):
     # state a step reads can still sit in L2 from the step before
     S2 = I.decode_state(w["N"], w["H"], w["d"], w["d"], I.PRESETS["decode"]["s0_std"],
                         args.seed + 1, "cuda")
+    torch.cuda.synchronize()
     ms2, p50_2 = run([S, S2])
     del S2
     alg = decode_alg_bytes(w)
@@ -482,6 +492,7 @@ def draft_sub(kda, args, stream, pk, decode_us):
     N, K, H, d = p["N"], p["K"], p["H"], p["d"]
     S = I.decode_state(N, H, d, d, p["s0_std"], args.seed, "cuda")
     x = I.draft_tokens(N, K, H, d, d, p["dtype"], p["la"], args.seed + 1, "cuda")
+    torch.cuda.synchronize()
     ins = (x["q"], x["k"], x["v"], x["log_alpha"], x["beta"])
     o = torch.empty_like(x["v"])
     acc = torch.full((N,), K, dtype=torch.int32, device="cuda")
@@ -617,6 +628,33 @@ def epilogue_sub(kda, args, stream, pk):
     return out
 
 
+def wide_gates_sub(kda, args, stream, pk):
+    """K3-strength gates (per-token log-decay in U(-5, -0.5): every 64-token
+    chunk leaves the chunk form's range) on the prefill shape, B=1, H=96,
+    T=8192: the tensor-core engine with the blocked path against the plain one
+    (which recomputes such heads token by token), and the blocked-path
+    engine's cost on in-range gates."""
+    out = {"metric": "ms per call", "unit": "ms",
+           "workload": "prefill B=1 H=96 T=8192 d=128 bf16, log alpha in U(-5, -0.5)"}
+    for la, tag in (((-5.0, -0.5), "wide"), ((-0.5, -0.001), "in_range")):
+        prob = I.prefill_problem(1, 8192, 96, 128, 128, "bf16", la, None, args.seed, "cuda")
+        torch.cuda.synchronize()
+        o = torch.empty_like(prob.v)
+        ST = torch.empty((1, 96, 128, 128), dtype=torch.float32, device="cuda")
+        ws = torch.empty(kda.kda_fwd_workspace_bytes(1), dtype=torch.uint8, device="cuda")
+        engines = ("tensorcore_wide", "tensorcore") if tag == "wide" else ("tensorcore_wide",)
+        for eng in engines:
+            ms = time_calls(lambda: kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha,
+                                                prob.beta, None, o=o, S_T=ST, workspace=ws,
+                                                engine=eng, stream=stream), 5, stream)
+            out[f"{tag}_{eng}_ms"] = round(ms, 4)
+        del prob, o, ST
+    out["note"] = ("tensorcore: heads with such chunks are recomputed token by token; "
+                   "tensorcore_wide: such chunks take the blocked path on the tensor cores")
+    torch.cuda.empty_cache()
+    return out
+
+
 def long_sub(kda, args, stream, pk, cpu=False):
     """The long prefill with carry-in: B=1, H=96, T=131072, S0 ~ N(0, 0.02),
     long-memory gates (one kda_fwd per call)."""
@@ -653,6 +691,7 @@ def varlen_sub(kda, args, stream, pk, cpu=False):
     N, H, d = p.n_seq, w["H"], w["d"]
     toks = [I.decode_token(N, H, d, d, pv["dtype"], pv["la"], args.seed + 1, s, "cuda")
             for s in range(pv["decode_steps"])]
+    torch.cuda.synchronize()
     od = torch.empty_like(toks[0]["v"])
     S = ST.clone()
     ctr = [0]

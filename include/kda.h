@@ -75,7 +75,15 @@ typedef enum {
 typedef enum {
     KDA_ENGINE_AUTO = 0,        /* tensor-core kernel where supported, else CUDA-core kernel */
     KDA_ENGINE_TENSORCORE = 1,  /* tcgen05/TMEM/TMA kernel: bf16, d = 128 only */
-    KDA_ENGINE_CUDACORE = 2     /* fp32 CUDA-core chunkwise kernel: any supported dtype/d */
+    KDA_ENGINE_CUDACORE = 2,    /* fp32 CUDA-core chunkwise kernel: any supported dtype/d */
+    KDA_ENGINE_TENSORCORE_WIDE = 3  /* the tensor-core kernel with the blocked path for
+                                       chunks outside the chunk form's log-decay range
+                                       (see kda_fwd, gate domain): for gates like K3's
+                                       (per-token log-decay down to -5); a few percent
+                                       slower than KDA_ENGINE_TENSORCORE on gates that
+                                       stay in range.  Plain kda_fwd / kda_fwd_engine /
+                                       kda_fwd_gated calls (separate epilogue) only;
+                                       kda_fwd_cp treats it as KDA_ENGINE_TENSORCORE */
 } kda_engine_t;
 
 /* Bytes of workspace kda_fwd needs for N sequences (status word and the
@@ -109,11 +117,15 @@ size_t kda_fwd_workspace_bytes(int N);
  * Gate domain: any finite log_alpha <= 0.  The chunk form scales keys by
  * exp(-G), G the in-chunk cumulative log-decay, which overflows fp32 once |G|
  * passes 80 -- reachable under K3's per-token bound of -5 ("Kimi K3 的 KDA"
- * section 6: -320 over 64 tokens).  Such chunks are computed token by token
+ * section 6: -320 over 64 tokens).  KDA_ENGINE_TENSORCORE_WIDE keeps such a
+ * chunk on the tensor cores when each of its four 16-token blocks stays within
+ * 80 (always, under K3's bound): A and M are built block by block with the
+ * decay referenced to each block's first token ("Kimi K3模型架构详解" section
+ * 3.4), and the state is handed on as Diag(gamma) S + K~^T U with K~ the keys
+ * decayed to the chunk end.  Any other such chunk is computed token by token
  * with the recurrence itself on CUDA cores, in fp32: by the CUDA-core engine
- * chunk by chunk, by the tensor-core engine for the whole (sequence, head)
+ * chunk by chunk, by the tensor-core engines for the whole (sequence, head)
  * that contains one (from S0, after its chunk pass; S_T may still alias S0).
- * The results are exact to fp32 rounding either way; only the time differs.
  *
  * Device status (kda_read_device_status): KDA_ERR_INVALID_ARGUMENT when the
  * device-side cu_seqlens is not non-decreasing or does not end at Ttot; no

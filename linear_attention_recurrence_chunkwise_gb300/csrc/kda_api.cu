@@ -69,7 +69,7 @@ kda_status_t check_fwd(const void *q, const void *k, const void *v, const float 
                        bool &use_tc) {
     if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_INVALID_ARGUMENT;
     if (engine != KDA_ENGINE_AUTO && engine != KDA_ENGINE_TENSORCORE &&
-        engine != KDA_ENGINE_CUDACORE)
+        engine != KDA_ENGINE_CUDACORE && engine != KDA_ENGINE_TENSORCORE_WIDE)
         return KDA_ERR_INVALID_ARGUMENT;
     if (B < 0 || T < 0 || N < 0 || H <= 0 || d_k <= 0 || d_v <= 0)
         return KDA_ERR_INVALID_ARGUMENT;
@@ -93,8 +93,9 @@ kda_status_t check_fwd(const void *q, const void *k, const void *v, const float 
     if (!aligned16(workspace)) return KDA_ERR_INVALID_ARGUMENT;
 
     const bool tc_ok = kda::prefill_tc_supported(dtype, d_k, d_v) && Ttot <= INT32_MAX;
-    if (engine == KDA_ENGINE_TENSORCORE && !tc_ok) return KDA_ERR_UNSUPPORTED;
-    use_tc = engine == KDA_ENGINE_TENSORCORE || (engine == KDA_ENGINE_AUTO && tc_ok);
+    const bool tc_engine = engine == KDA_ENGINE_TENSORCORE || engine == KDA_ENGINE_TENSORCORE_WIDE;
+    if (tc_engine && !tc_ok) return KDA_ERR_UNSUPPORTED;
+    use_tc = tc_engine || (engine == KDA_ENGINE_AUTO && tc_ok);
 
     p = kda::FwdParams{};
     p.tasks = nullptr;
@@ -118,6 +119,7 @@ kda_status_t check_fwd(const void *q, const void *k, const void *v, const float 
     p.N = N;
     p.dk = d_k;
     p.dv = d_v;
+    p.blocked = engine == KDA_ENGINE_TENSORCORE_WIDE;
     return KDA_OK;
 }
 
@@ -179,7 +181,7 @@ kda_status_t kda_fwd_gated(const void *q, const void *k, const void *v, const fl
     if (!(eps >= 0.f) || eps > 3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
     if (p.Ttot > 0 && (!g || !aligned16(g))) return KDA_ERR_INVALID_ARGUMENT;
     if (norm_weight && !aligned(norm_weight, 4)) return KDA_ERR_INVALID_ARGUMENT;
-    if (mode == KDA_EPILOGUE_FUSED && !use_tc) return KDA_ERR_UNSUPPORTED;
+    if (mode == KDA_EPILOGUE_FUSED && (!use_tc || p.blocked)) return KDA_ERR_UNSUPPORTED;
     if (workspace_bytes < kda_fwd_workspace_bytes(N)) return KDA_ERR_WORKSPACE;
     if (fault_injected()) return KDA_ERR_CUDA;
 

@@ -45,6 +45,8 @@ struct FwdParams {
                                 // logits [Ttot][H][d_v] in the io dtype, or nullptr
     const float *norm_w;        // its per-channel weight [d_v], or nullptr (ones)
     float eps;                  // its epsilon
+    int blocked;                // tensor-core engine: the variant with the blocked path
+                                // for chunks outside the chunk form's log-decay range
     int64_t Ttot;
     int T;                      // tokens per sequence when cu_seqlens is null
     int H, N, dk, dv;

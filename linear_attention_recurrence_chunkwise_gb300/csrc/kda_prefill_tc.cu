@@ -102,7 +102,8 @@ struct __align__(1024) TcStage {
     uint8_t m[8192];    // output mask [r][j]
     float gam[D];       // gamma per key channel
     float bet[C];       // beta per token (0 past the end)
-    uint8_t pad[256];
+    int wide;           // the chunk took the blocked path (kb holds K~, not Kb)
+    uint8_t pad[252];
 };
 
 struct __align__(1024) TcSmem {
@@ -117,9 +118,11 @@ struct __align__(1024) TcSmem {
     uint32_t tmem_base;
     int abort;
     int domain;
+    int wide_chunk[2];  // scan -> chunk-local warps: chunk m (slot m % 2) takes the blocked path
 };
 
 // members read or written with 16-byte vector accesses
+static_assert(sizeof(TcStage) == 74752, "stage layout");
 static_assert(offsetof(TcSmem, wn) % 16 == 0 && offsetof(TcSmem, as) % 16 == 0 &&
                   offsetof(TcStage, gam) % 16 == 0 && offsetof(TcStage, bet) % 16 == 0,
               "16-byte vector accesses need 16-byte aligned members");
@@ -202,6 +205,23 @@ __device__ __forceinline__ void solve_ut(TcSmem &sm, const float *bet, int pt) {
 __device__ __forceinline__ void pack16(const uint32_t (&u)[16], uint32_t (&w)[8]) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) w[j] = pack_bf16(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1]));
+}
+
+// d (16 x 8, fp32) += a (16 x 16) b (16 x 8), bf16 operands (warp-level tensor cores)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of bf16 element (row, c) in rows of 128 channels (256 bytes)
+// whose 16-byte chunks are XOR-swizzled by row % 8: the m16n8k16 fragment
+// loads of a warp then hit 32 different banks.
+__device__ __forceinline__ uint32_t xrow_offset(int row, int c) {
+    return row * 256 + ((((c >> 3) ^ row) & 7) | ((c >> 3) & 8)) * 16 + (c & 7) * 2;
 }
 
 // Token-serial pass over a whole (sequence, head), from S0: the fallback for a
@@ -324,9 +344,172 @@ __device__ __forceinline__ void serial_head(const FwdParams *pp, uint8_t *smem_r
     }
 }
 
+// a3-a5 of a chunk on the blocked path (see the kernel): called by the 256
+// threads of the chunk-local warps, which reach every named barrier inside.
+// Out of line, so that the common path's code and registers do not change.
+__device__ __noinline__ void blocked_chunk(TcSmem &sm, TcStage &S, uint32_t gaddr, int n,
+                                           int valid, volatile int *abort) {
+    const int pt = threadIdx.x, lane = pt & 31, pw = pt >> 5;
+    const int s = n & 1;
+    const int fl = (lane >> 2) & 1;
+    const int c0 = 16 * pw;
+    const int slab = c0 >> 6, col = c0 & 63;
+    float g[2][16];  // G2 of this thread's tokens and channels, parked in tensor memory
+    tmem_ld32(gaddr, reinterpret_cast<uint32_t(&)[32]>(g));
+                // a3-a5 for a chunk whose in-chunk log-decay leaves the chunk form's
+                // range (K3's per-token bound of -5 reaches -320 over 64 tokens): A
+                // and M block by block, 16 tokens per block, block I taking its decay
+                // reference at its first token 16 I, so that every scaled operand
+                // stays inside fp32 / bf16 range (the scan checked each block):
+                //   A[r][j] = beta_r sum_c (k_rc 2^(G2_rc - G2_16I,c)) (k_jc 2^(G2_16I,c - G2_jc)),
+                //   M[r][j] = sum_c (q_rc 2^(G2_rc - G2_16I,c)) (k_jc 2^(G2_16I,c - G2_jc)),
+                // for r in block I and j <= r ("Kimi K3 的 KDA" section 6 and "Kimi K3模型
+                // 架构详解" section 3.4: with the decay bounded, sub-tiles with their own
+                // reference points keep every causal tile a dense product).  The
+                // products run on the warp-level tensor cores (bf16 m16n8k16): X =
+                // [Kh_I; Qh_I] (32 rows) is staged in sm.tp, Kb_I (tokens 0 .. 16 I + 15)
+                // in the slot's kb area.  Then the chunk-start operands as on the other
+                // path, except K~ = K 2^(G2_63 - G2) in place of Kb: the carry hands the
+                // state on as S <- Diag(gamma) S + K~^T U (scaling S before the product)
+                // instead of Diag(gamma) (S + Kb^T U), which would overflow here.
+                // no R product here: complete bar_r's phase of this chunk by hand, so
+                // that the next chunk's wait on it keeps its parity
+                if (pt == 0) {
+        mbar_arrive(smem_u32(&sm.bar_r));
+        S.wide = 1;  // for the carry, which clears it once it has read it
+    }
+                if (n >= 1) wait_phase(sm.ready[s ^ 1], ((n - 1) >> 1) & 1, abort);  // sm.tp is free
+                named_bar_sync(kBarPrep, kPrepThreads);  // beta of the chunk is written
+                if (pt == 0) sm.wide_chunk[s] = 0;       // (every thread has read it)
+                uint8_t *X = sm.tp, *Y = S.kb;
+                const int g8 = lane >> 2, t4 = lane & 3;
+    #pragma unroll 1
+                for (int I = 0; I < 4; ++I) {
+                    float ref[16];  // G2 of token 16 I (lane 8 I, slot 0) on this warp's channels
+    #pragma unroll
+                    for (int e = 0; e < 16; ++e) ref[e] = __shfl_sync(0xffffffffu, g[0][e], 8 * I);
+    #pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int t = 2 * lane + (i ^ fl);
+                        if (t < 16 * I + 16) {
+                            const bool live = t < valid, in_block = t >= 16 * I;
+    #pragma unroll
+                            for (int k = 0; k < 2; ++k) {
+                                const uint32_t off = slab * 16384 + sw128_offset(t, col + 8 * k);
+                                float kf[8], qf[8], kbf[8], kh[8], qh[8];
+                                if (live) {
+                                    unpack8(*reinterpret_cast<const uint4 *>(S.kq + off), kf);
+                                    unpack8(*reinterpret_cast<const uint4 *>(S.kq + off + 8192), qf);
+                                } else {
+    #pragma unroll
+                                    for (int e = 0; e < 8; ++e) kf[e] = qf[e] = 0.f;
+                                }
+    #pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const float gr = g[i][8 * k + e], rf = ref[8 * k + e];
+                                    kbf[e] = kf[e] * ex2_approx(rf - gr);
+                                    const float up = in_block ? ex2_approx(gr - rf) : 0.f;
+                                    kh[e] = kf[e] * up;
+                                    qh[e] = qf[e] * up;
+                                }
+                                *reinterpret_cast<uint4 *>(Y + xrow_offset(t, c0 + 8 * k)) = pack8(kbf);
+                                if (in_block) {
+                                    *reinterpret_cast<uint4 *>(X + xrow_offset(t - 16 * I, c0 + 8 * k)) =
+                                        pack8(kh);
+                                    *reinterpret_cast<uint4 *>(X + xrow_offset(16 + t - 16 * I, c0 + 8 * k)) =
+                                        pack8(qh);
+                                }
+                            }
+                        }
+                    }
+                    named_bar_sync(kBarPrep, kPrepThreads);  // X and Y of block I are staged
+                    // tiles (mt, nt): mt 0 = the K rows (A), 1 = the Q rows (M);
+                    // columns j = 8 nt .. 8 nt + 7, nt < 2 (I + 1)
+                    const int ntiles = 2 * (I + 1);
+                    for (int idx = pw; idx < 2 * ntiles; idx += kPrepWarps) {
+                        const int mt = idx / ntiles, nt = idx % ntiles;
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    #pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const int ca = 16 * kk + 2 * t4;
+                            uint32_t a[4];
+                            a[0] = *reinterpret_cast<const uint32_t *>(X + xrow_offset(16 * mt + g8, ca));
+                            a[1] = *reinterpret_cast<const uint32_t *>(X + xrow_offset(16 * mt + g8 + 8, ca));
+                            a[2] = *reinterpret_cast<const uint32_t *>(X + xrow_offset(16 * mt + g8, ca + 8));
+                            a[3] = *reinterpret_cast<const uint32_t *>(X + xrow_offset(16 * mt + g8 + 8, ca + 8));
+                            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(Y + xrow_offset(8 * nt + g8, ca));
+                            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(Y + xrow_offset(8 * nt + g8, ca + 8));
+                            mma_bf16_16816(acc, a, b0, b1);
+                        }
+                        // rows r = 16 I + g8 (acc 0, 1) and r + 8 (acc 2, 3); columns j, j + 1
+                        const int j = 8 * nt + 2 * t4;
+    #pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int r = 16 * I + g8 + 8 * hh;
+                            const float v0 = acc[2 * hh], v1 = acc[2 * hh + 1];
+                            if (mt == 0) {  // fp32, beta-scaled; only j < r is ever read
+                                const float br = S.bet[r];
+                                *reinterpret_cast<float2 *>(&sm.as[r * LDA + j]) = make_float2(br * v0, br * v1);
+                            } else {        // bf16 operand, diagonal included
+                                *reinterpret_cast<uint32_t *>(S.m + sw128_offset(r, j)) =
+                                    pack_bf16(j <= r ? v0 : 0.f, j + 1 <= r ? v1 : 0.f);
+                            }
+                        }
+                    }
+                    // M is zero right of the block's columns: rows of block I, 16-byte
+                    // pieces 2 (I + 1) .. 7
+                    const int np = 6 - 2 * I;
+                    for (int q = pt; q < 16 * np; q += kPrepThreads) {
+                        const int r = 16 * I + q / np, piece = 2 * (I + 1) + q % np;
+                        *reinterpret_cast<uint4 *>(S.m + sw128_offset(r, 8 * piece)) = make_uint4(0, 0, 0, 0);
+                    }
+                    named_bar_sync(kBarPrep, kPrepThreads);  // X and Y are free again
+                }
+                // chunk-start operands over the landed tiles: Kh = K Gamma, Qh = Q Gamma,
+                // and K~ = K 2^(G2_63 - G2) into the kb area
+                float g63[16];
+    #pragma unroll
+                for (int e = 0; e < 16; ++e) g63[e] = __shfl_sync(0xffffffffu, g[0][e], 31);
+    #pragma unroll
+                for (int ik = 0; ik < 4; ++ik) {
+                    const int i = ik >> 1, k = ik & 1;
+                    const float *gr = g[i] + 8 * k;
+                    const int t = 2 * lane + (i ^ fl);
+                    const uint32_t off = slab * 16384 + sw128_offset(t, col + 8 * k);
+                    const uint32_t offv = slab * 8192 + sw128_offset(t, col + 8 * k);
+                    float kf[8], qf[8], kt[8], gfv[8];
+                    if (t < valid) {
+                        unpack8(*reinterpret_cast<const uint4 *>(S.kq + off), kf);
+                        unpack8(*reinterpret_cast<const uint4 *>(S.kq + off + 8192), qf);
+                    } else {
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e) kf[e] = qf[e] = 0.f;
+                        *reinterpret_cast<uint4 *>(S.v + offv) = make_uint4(0, 0, 0, 0);
+                    }
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        gfv[e] = ex2_approx(gr[e]);
+                        kt[e] = kf[e] * ex2_approx(g63[8 * k + e] - gr[e]);
+                        kf[e] *= gfv[e];
+                        qf[e] *= gfv[e];
+                    }
+                    *reinterpret_cast<uint4 *>(S.kq + off) = pack8(kf);
+                    *reinterpret_cast<uint4 *>(S.kq + off + 8192) = pack8(qf);
+                    *reinterpret_cast<uint4 *>(S.kb + offv) = pack8(kt);
+                    if (i == 0 && lane == 31) {  // gamma = Gamma of token 63
+                        float4 *gd = reinterpret_cast<float4 *>(S.gam + c0 + 8 * k);
+                        gd[0] = make_float4(gfv[0], gfv[1], gfv[2], gfv[3]);
+                        gd[1] = make_float4(gfv[4], gfv[5], gfv[6], gfv[7]);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                named_bar_sync(kBarPrep, kPrepThreads);
+}
+
 // kTasks: task-table mode (segment-parallel forward); the plain instantiation
 // compiles none of its per-task choices.
-template <bool kTasks, bool kFullGrid, bool kGated>
+template <bool kTasks, bool kFullGrid, bool kGated, bool kBlocked>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -335,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_g,
                       const __grid_constant__ CUtensorMap tm_vz) {
     static_assert(!(kTasks && kGated), "the fused epilogue serves plain calls only");
+    static_assert(!(kBlocked && (kTasks || kGated)), "the blocked path serves plain calls only");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Align by offsetting the shared-memory pointer itself (not through an
     // integer round trip), so the compiler keeps every access in the shared
@@ -373,6 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         sm.abort = 0;
         sm.domain = 0;
+        sm.wide_chunk[0] = sm.wide_chunk[1] = 0;
+        sm.st[0].wide = sm.st[1].wide = 0;
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.ready[s]), 1);
@@ -522,9 +708,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 g[1][e + 1] = s11;
                 amax = fmaxf(amax, fmaxf(fabsf(inc[e]), fabsf(inc[e + 1])));
             }
-            // a chunk outside the chunk form's range sends the whole (sequence,
-            // head) to the token-serial pass after teardown
-            if (!(amax <= kLog2DecayLimit)) *reinterpret_cast<volatile int *>(&sm.domain) = 1;
+            // a chunk outside the chunk form's range takes the blocked path
+            // (kBlocked: four 16-token blocks, each with its own decay
+            // reference) when every block stays inside the range; otherwise
+            // the whole (sequence, head) goes to the token-serial pass after
+            // teardown.  G2 only decreases along the chunk, so a block's range
+            // is G2 at its first token (lane 8 I, slot 0) minus G2 at its last
+            // (lane 8 I + 7, slot 0).
+            if constexpr (kBlocked) {
+                if (__any_sync(0xffffffffu, !(amax <= kLog2DecayLimit))) {
+                    float bmax = 0.f;
+#pragma unroll
+                    for (int I = 0; I < 4; ++I)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float top = __shfl_sync(0xffffffffu, g[0][e], 8 * I);
+                            const float bot = __shfl_sync(0xffffffffu, g[0][e], 8 * I + 7);
+                            bmax = fmaxf(bmax, top - bot);
+                        }
+                    if (!(bmax <= kLog2DecayLimit))
+                        *reinterpret_cast<volatile int *>(&sm.domain) = 1;
+                    else
+                        *reinterpret_cast<volatile int *>(&sm.wide_chunk[m & 1]) = 1;
+                }
+            } else if (!(amax <= kLog2DecayLimit)) {
+                *reinterpret_cast<volatile int *>(&sm.domain) = 1;
+            }
         };
         // Warps 4-7: gates of chunk m scanned and parked; once every scanning
         // thread has read the gate tile, it takes chunk m + 1.
@@ -564,11 +773,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bn = (pt < C && pt < valid1 && in_bounds(p.status, bi, n_beta)) ? p.beta[bi] : 0.f;
             }
 
+            // the scan of this chunk (one step earlier) chose the blocked path
+            bool wide = false;
+            if constexpr (kBlocked) wide = *reinterpret_cast<volatile int *>(&sm.wide_chunk[s]) != 0;
+
             wait_phase_warp(sm.full[s], (n >> 1) & 1, abort);
             // Kb, M and gamma of chunk n - 2 (same slot) are no longer read by the carry
             if (n >= 2) wait_phase_warp(sm.tailfree[s], ((n >> 1) - 1) & 1, abort);
             if (pt < C) S.bet[pt] = bet;
 
+          if (!wide) {
             // a2: scaled operands, written over the landed tiles (same swizzle)
 #pragma unroll
             for (int ik = 0; ik < 4; ++ik) {
@@ -662,6 +876,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (pt == 0 && n >= 1) wait_phase(sm.ready[s ^ 1], ((n - 1) >> 1) & 1, abort);
             tc_fence_before();
             named_bar_sync(kBarPrep, kPrepThreads);
+          } else if constexpr (kBlocked) {
+            blocked_chunk(sm, S, gpark + 32 * half, n, valid, abort);
+          }
 
             if (!scanner) {
                 // a4: T' = (I + A)^-1 diag(beta); the carry warps take it from here
@@ -881,6 +1098,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(smem_u32(&sm.bar_u));
             }
             __syncwarp();
+            // a chunk of the blocked path hands the state on as Diag(gamma) S + K~^T U:
+            // scale the fp32 state now (the U and O products read its bf16 copy;
+            // the S update below then adds K~^T U and scales by nothing)
+            bool wide = false;
+            if constexpr (kBlocked) wide = S.wide;
+            if (wide) {
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t x[32];
+                    tmem_ld32(tmem + lane_addr + kColS + 32 * cb, x);
+                    const float4 *gm = reinterpret_cast<const float4 *>(S.gam + 32 * cb);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 gq = gm[q];
+                        float a0 = __uint_as_float(x[4 * q + 0]), a1 = __uint_as_float(x[4 * q + 1]);
+                        float a2 = __uint_as_float(x[4 * q + 2]), a3 = __uint_as_float(x[4 * q + 3]);
+                        mul2(a0, a1, gq.x, gq.y);
+                        mul2(a2, a3, gq.z, gq.w);
+                        x[4 * q + 0] = __float_as_uint(a0);
+                        x[4 * q + 1] = __float_as_uint(a1);
+                        x[4 * q + 2] = __float_as_uint(a2);
+                        x[4 * q + 3] = __float_as_uint(a3);
+                    }
+                    tmem_st32(tmem + lane_addr + kColS + 32 * cb, x);
+                }
+            }
             auto issue_o = [&] {  // O^T = S^T Qh^T
                 if (issuer) {
                     tc_fence_after();
@@ -912,6 +1155,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_phase_warp(sm.bar_u, n & 1, abort);
             if (issuer) bulk_wait_group_read0();  // the previous output tile has left sm.ut
             named_bar_sync(kBarCarry, kCarryThreads);
+            // a blocked chunk's gamma has been applied (every thread has read it):
+            // ones for the S update below (ordered by its barrier)
+            if (wide) {
+                S.gam[et] = 1.f;
+                if (et == 0) S.wide = 0;
+            }
             tc_fence_after();
             // U^T (lane v, column j) -> bf16 pairs in tensor memory, over U^T itself:
             // the A operand of the two products that follow
@@ -953,6 +1202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_phase_warp(sm.bar_s, n & 1, abort);
             tc_fence_after();
             // S^T <- (S^T + U^T Kb) scaled by gamma along c: TMEM fp32 and bf16 copy
+            // (for a blocked chunk gamma holds ones by now: its state is scaled)
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t x[32];
@@ -1117,13 +1367,16 @@ cudaError_t launch_prefill_tc(const FwdParams &p, cudaStream_t s) {
     // on one head per SM for 96-304 blocks)
     const size_t blocks = (size_t)p.N * p.H;
     const bool full = blocks * 8 > (size_t)sm_count() * 7;
-    if (p.gate && p.tasks) return cudaErrorInvalidValue;
-    auto kern = p.tasks  ? (full ? prefill_tc_kernel<true, true, false>
-                                 : prefill_tc_kernel<true, false, false>)
-                : p.gate ? (full ? prefill_tc_kernel<false, true, true>
-                                 : prefill_tc_kernel<false, false, true>)
-                         : (full ? prefill_tc_kernel<false, true, false>
-                                 : prefill_tc_kernel<false, false, false>);
+    if ((p.gate || p.blocked) && p.tasks) return cudaErrorInvalidValue;
+    if (p.gate && p.blocked) return cudaErrorInvalidValue;
+    auto kern = p.tasks     ? (full ? prefill_tc_kernel<true, true, false, false>
+                                    : prefill_tc_kernel<true, false, false, false>)
+                : p.gate    ? (full ? prefill_tc_kernel<false, true, true, false>
+                                    : prefill_tc_kernel<false, false, true, false>)
+                : p.blocked ? (full ? prefill_tc_kernel<false, true, false, true>
+                                    : prefill_tc_kernel<false, false, false, true>)
+                            : (full ? prefill_tc_kernel<false, true, false, false>
+                                    : prefill_tc_kernel<false, false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

@@ -26,7 +26,7 @@ KDA_ERR_TIMEOUT = 6
 KDA_ERR_BOUNDS = 7
 
 KDA_F32, KDA_BF16 = 0, 1
-ENGINES = {"auto": 0, "tensorcore": 1, "cudacore": 2}
+ENGINES = {"auto": 0, "tensorcore": 1, "cudacore": 2, "tensorcore_wide": 3}
 EPILOGUES = {"auto": 0, "fused": 1, "separate": 2}
 
 # every symbol include/kda.h declares

@@ -33,7 +33,7 @@ def kda():
 
 
 def engine_ok(engine, dtype, d):
-    return engine != "tensorcore" or (dtype == "bf16" and d == 128)
+    return not engine.startswith("tensorcore") or (dtype == "bf16" and d == 128)
 
 
 def assert_engine_rejects(kda, call):
@@ -53,7 +53,7 @@ def run_fwd(kda, prob, engine, **kw):
 
 # --------------------------------------------------------------- prefill, small
 
-@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("engine", ENGINES + ["tensorcore_wide"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 333])
@@ -170,14 +170,15 @@ def test_zero_sizes(kda):
     assert o.numel() == 0 and ST.shape == (0, 2, 64, 64)
 
 
-@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("engine", ENGINES + ["tensorcore_wide"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("T", [1, 65, 200])
 def test_wide_gate_domain(kda, engine, dtype, d, T):
     """Per-token log-decay down to -5 (the K3 bound: -320 over a 64-token chunk,
-    far outside the chunk form's +-80) is exact: such chunks are taken token by
-    token, and the status word stays clear."""
+    far outside the chunk form's +-80) is exact: such chunks take the blocked
+    path (tensorcore_wide) or are taken token by token, and the status word
+    stays clear."""
     prob = I.prefill_problem(2, T, 3, d, d, dtype, (-5.0, -0.5), 0.05, seed=T + d + 11,
                              device=DEV)
     ws = torch.zeros(kda.kda_fwd_workspace_bytes(2), dtype=torch.uint8, device=DEV)
@@ -191,11 +192,13 @@ def test_wide_gate_domain(kda, engine, dtype, d, T):
     assert rel_err(ST, S_ref) < tol_s(dt)
 
 
-@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("engine", ENGINES + ["tensorcore_wide"])
 def test_wide_gate_mixed_chunks_varlen_in_place(kda, engine):
     """Strong and mild gates mixed across heads and across the chunks of one
     sequence, packed varlen with empty and ragged sequences, S_T written over
-    S0: the wide chunks take the token-serial path, the rest the chunk form."""
+    S0: the wide chunks take the blocked path (tensorcore_wide; a head with ten
+    tokens of near-total forgetting, beyond any 16-token block's range, still
+    goes token by token) or the token-serial path, the rest the chunk form."""
     lengths = [130, 0, 64, 257, 1]
     prob = I.prefill_problem(1, 0, 4, 128, 128, "bf16", (-0.5, -0.001), 0.05, seed=21,
                              device=DEV, lengths=lengths)
@@ -504,6 +507,38 @@ def test_workload_long_sampled_heads(kda, engine):
     assert eo < 2e-2
     assert es < 1e-2
     assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(ST).all())
+
+
+@pytest.mark.parametrize("engine", ["tensorcore_wide", "tensorcore"])
+def test_workload_wide_gates_all_heads(kda, engine):
+    """B=1, H=96, T=8192, d=128, bf16 with K3-strength gates, log alpha in
+    U(-5, -0.5): every chunk leaves the chunk form's range; o and S_T of every
+    head against the oracle."""
+    prob = I.prefill_problem(1, 8192, 96, 128, 128, "bf16", (-5.0, -0.5), None, seed=0,
+                             device=DEV)
+    ws = torch.zeros(kda.kda_fwd_workspace_bytes(1), dtype=torch.uint8, device=DEV)
+    o, ST = run_fwd(kda, prob, engine, workspace=ws)
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK
+    o_ref, S_ref = cached_oracle("wide_gates", prob, list(range(96)))
+    eo, es = rel_err(o, o_ref), rel_err(ST, S_ref)
+    print(f"[parity] wide gates {engine}, all 96 heads: o {eo:.2e} S {es:.2e}")
+    assert eo < 2e-2
+    assert es < 1e-2
+
+
+def test_bounds_checked_build_blocked_path(kda):
+    """The bounds-checked build through the blocked path: wide chunks, ragged
+    and empty sequences, no report, results against the oracle."""
+    lib = kda.load_library(kbuild.build(bounds_check=True))
+    prob = I.prefill_problem(1, 0, 2, 128, 128, "bf16", (-5.0, -0.5), 0.05, seed=8,
+                             device=DEV, lengths=[0, 130, 1, 64, 200])
+    ws = torch.zeros(int(lib.kda_fwd_workspace_bytes(5)), dtype=torch.uint8, device=DEV)
+    o, ST = kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0,
+                        prob.cu_seqlens, workspace=ws, engine="tensorcore_wide", lib=lib)
+    assert kda.kda_read_device_status(ws, lib=lib) == kda.KDA_OK
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1])
+    assert rel_err(o, o_ref) < 2e-2
+    assert rel_err(ST, S_ref) < 1e-2
 
 
 # ------------------------------------------------ segment-parallel forward
