@@ -115,6 +115,7 @@ struct __align__(1024) TcSmem {
     uint64_t full[2], ready[2], gfull, tpfull;
     uint64_t bar_r, bar_u, bar_o, bar_s, bar_fin, tailfree[2];
     alignas(16) float wn[D];  // epilogue: the norm weight (ones when none is given), read as float4
+    alignas(16) float bfac[6][D];  // blocked path: 2^(G2_16I - G2_16J) per key channel, J < I
     uint32_t tmem_base;
     int abort;
     int domain;
@@ -123,8 +124,8 @@ struct __align__(1024) TcSmem {
 
 // members read or written with 16-byte vector accesses
 static_assert(sizeof(TcStage) == 74752, "stage layout");
-static_assert(offsetof(TcSmem, wn) % 16 == 0 && offsetof(TcSmem, as) % 16 == 0 &&
-                  offsetof(TcStage, gam) % 16 == 0 && offsetof(TcStage, bet) % 16 == 0,
+static_assert(offsetof(TcSmem, wn) % 16 == 0 && offsetof(TcSmem, bfac) % 16 == 0 &&
+                  offsetof(TcSmem, as) % 16 == 0 && offsetof(TcStage, gam) % 16 == 0 && offsetof(TcStage, bet) % 16 == 0,
               "16-byte vector accesses need 16-byte aligned members");
 
 // Wait for a phase; on timeout (or once any thread has timed out) return
@@ -215,13 +216,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Byte offset of bf16 element (row, c) in rows of 128 channels (256 bytes)
-// whose 16-byte chunks are XOR-swizzled by row % 8: the m16n8k16 fragment
-// loads of a warp then hit 32 different banks.
-__device__ __forceinline__ uint32_t xrow_offset(int row, int c) {
-    return row * 256 + ((((c >> 3) ^ row) & 7) | ((c >> 3) & 8)) * 16 + (c & 7) * 2;
 }
 
 // Token-serial pass over a whole (sequence, head), from S0: the fallback for a
@@ -347,6 +341,70 @@ __device__ __forceinline__ void serial_head(const FwdParams *pp, uint8_t *smem_r
 // a3-a5 of a chunk on the blocked path (see the kernel): called by the 256
 // threads of the chunk-local warps, which reach every named barrier inside.
 // Out of line, so that the common path's code and registers do not change.
+//
+// For a chunk whose in-chunk log-decay leaves the chunk form's range (K3's
+// per-token bound of -5 reaches -320 over 64 tokens), A and M are built in
+// 16-token blocks, block I taking its decay reference at its first token 16 I
+// (the scan checked that each block stays inside the range):
+//   A[r][j] = beta_r sum_c Kh_rc Kb_jc,  M[r][j] = sum_c Qh_rc Kb_jc,  r in block I,
+//   Kh = k 2^(G2_r - G2_16I) <= 1,  Qh likewise,  Kb = k 2^(G2_16I - G2_j),
+// for j <= r ("Kimi K3 的 KDA" section 6 and "Kimi K3模型架构详解" section 3.4:
+// with the decay bounded, sub-tiles with their own reference points keep every
+// causal tile a dense product).  Kb of a token j of an earlier block J is its
+// own block's Kb times 2^(G2_16I - G2_16J) <= 1, a per-channel factor, so one
+// pass writes every operand once, each referenced to its own block: Kh and Qh
+// over the landed k / q tile, Kb into the slot's kb area.  The 20 16 x 16 tiles
+// of A and M (row block I, column block J <= I) then run at once on the
+// warp-level tensor cores (bf16 m16n8k16, K = 128), the B fragments of a tile
+// below the diagonal scaled by the factor table sm.bfac.  The fragment loads
+// read the 128-byte-swizzled tiles conflict-free (eight rows, eight 16-byte
+// columns).  Last, the chunk-start operands as on the other path, except K~ =
+// k 2^(G2_63 - G2) <= 1 in place of Kb: the carry hands the state on as
+// S <- Diag(gamma) S + K~^T U (scaling S before the product) instead of
+// Diag(gamma) (S + Kb^T U), which would overflow here.  They are computed in
+// the first pass and held in registers until the products have read the tiles.
+template <bool kScaled>
+__device__ __forceinline__ void blocked_tile(const TcSmem &sm, const TcStage &S, int mt, int I,
+                                             int J, int lane, float (&acc)[2][4]) {
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const uint8_t *xa = S.kq + (mt ? 8192 : 0);
+    const float *fac = sm.bfac[kScaled ? I * (I - 1) / 2 + J : 0];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const int c = 16 * kk + 2 * t4, cc = c & 63;  // channel of a[0] / b0, its slab column
+        const uint8_t *xs = xa + (kk >> 2) * 16384, *ys = S.kb + (kk >> 2) * 8192;
+        uint32_t a[4];
+        a[0] = *reinterpret_cast<const uint32_t *>(xs + sw128_offset(16 * I + g8, cc));
+        a[1] = *reinterpret_cast<const uint32_t *>(xs + sw128_offset(16 * I + g8 + 8, cc));
+        a[2] = *reinterpret_cast<const uint32_t *>(xs + sw128_offset(16 * I + g8, cc + 8));
+        a[3] = *reinterpret_cast<const uint32_t *>(xs + sw128_offset(16 * I + g8 + 8, cc + 8));
+        float2 f0, f1;
+        if constexpr (kScaled) {
+            f0 = *reinterpret_cast<const float2 *>(fac + c);
+            f1 = *reinterpret_cast<const float2 *>(fac + c + 8);
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int j = 16 * J + 8 * hh + g8;
+            uint32_t b0 = *reinterpret_cast<const uint32_t *>(ys + sw128_offset(j, cc));
+            uint32_t b1 = *reinterpret_cast<const uint32_t *>(ys + sw128_offset(j, cc + 8));
+            if constexpr (kScaled) {
+                b0 = pack_bf16(__uint_as_float(b0 << 16) * f0.x, __uint_as_float(b0 & 0xFFFF0000u) * f0.y);
+                b1 = pack_bf16(__uint_as_float(b1 << 16) * f1.x, __uint_as_float(b1 & 0xFFFF0000u) * f1.y);
+            }
+            mma_bf16_16816(acc[hh], a, b0, b1);
+        }
+    }
+}
+
+// tiles of the products, (matrix << 4) | (I << 2) | J with matrix 0 = A, 1 = M:
+// warp w takes entries w, w + 8 and w + 16: warps 0-3 the eight diagonal tiles
+// (no factors) and one below the diagonal each, warps 4-7 two below it each
+__constant__ uint8_t kBlockedTiles[20] = {
+    0x00, 0x05, 0x0A, 0x0F, 0x04, 0x08, 0x09, 0x0C,  // A: (0,0) (1,1) (2,2) (3,3) | (1,0) (2,0) (2,1) (3,0)
+    0x10, 0x15, 0x1A, 0x1F, 0x0D, 0x0E, 0x14, 0x18,  // M diagonal | A (3,1) (3,2), M (1,0) (2,0)
+    0x19, 0x1C, 0x1D, 0x1E};                         // M (2,1) (3,0) (3,1) (3,2)
+
 __device__ __noinline__ void blocked_chunk(TcSmem &sm, TcStage &S, uint32_t gaddr, int n,
                                            int valid, volatile int *abort) {
     const int pt = threadIdx.x, lane = pt & 31, pw = pt >> 5;
@@ -354,157 +412,164 @@ __device__ __noinline__ void blocked_chunk(TcSmem &sm, TcStage &S, uint32_t gadd
     const int fl = (lane >> 2) & 1;
     const int c0 = 16 * pw;
     const int slab = c0 >> 6, col = c0 & 63;
-    float g[2][16];  // G2 of this thread's tokens and channels, parked in tensor memory
-    tmem_ld32(gaddr, reinterpret_cast<uint32_t(&)[32]>(g));
-                // a3-a5 for a chunk whose in-chunk log-decay leaves the chunk form's
-                // range (K3's per-token bound of -5 reaches -320 over 64 tokens): A
-                // and M block by block, 16 tokens per block, block I taking its decay
-                // reference at its first token 16 I, so that every scaled operand
-                // stays inside fp32 / bf16 range (the scan checked each block):
-                //   A[r][j] = beta_r sum_c (k_rc 2^(G2_rc - G2_16I,c)) (k_jc 2^(G2_16I,c - G2_jc)),
-                //   M[r][j] = sum_c (q_rc 2^(G2_rc - G2_16I,c)) (k_jc 2^(G2_16I,c - G2_jc)),
-                // for r in block I and j <= r ("Kimi K3 的 KDA" section 6 and "Kimi K3模型
-                // 架构详解" section 3.4: with the decay bounded, sub-tiles with their own
-                // reference points keep every causal tile a dense product).  The
-                // products run on the warp-level tensor cores (bf16 m16n8k16): X =
-                // [Kh_I; Qh_I] (32 rows) is staged in sm.tp, Kb_I (tokens 0 .. 16 I + 15)
-                // in the slot's kb area.  Then the chunk-start operands as on the other
-                // path, except K~ = K 2^(G2_63 - G2) in place of Kb: the carry hands the
-                // state on as S <- Diag(gamma) S + K~^T U (scaling S before the product)
-                // instead of Diag(gamma) (S + Kb^T U), which would overflow here.
-                // no R product here: complete bar_r's phase of this chunk by hand, so
-                // that the next chunk's wait on it keeps its parity
-                if (pt == 0) {
+    const int I = lane >> 3;  // the block of this thread's tokens 2 lane, 2 lane + 1
+    // G2 of those tokens on channels c0 .. c0 + 15 is parked in tensor memory
+    // (columns: slot 0's 16 channels, then slot 1's) and read as it is needed
+    // no R product here: complete bar_r's phase of this chunk by hand, so that
+    // the next chunk's wait on it keeps its parity
+    if (pt == 0) {
         mbar_arrive(smem_u32(&sm.bar_r));
         S.wide = 1;  // for the carry, which clears it once it has read it
     }
-                if (n >= 1) wait_phase(sm.ready[s ^ 1], ((n - 1) >> 1) & 1, abort);  // sm.tp is free
-                named_bar_sync(kBarPrep, kPrepThreads);  // beta of the chunk is written
-                if (pt == 0) sm.wide_chunk[s] = 0;       // (every thread has read it)
-                uint8_t *X = sm.tp, *Y = S.kb;
-                const int g8 = lane >> 2, t4 = lane & 3;
-    #pragma unroll 1
-                for (int I = 0; I < 4; ++I) {
-                    float ref[16];  // G2 of token 16 I (lane 8 I, slot 0) on this warp's channels
-    #pragma unroll
-                    for (int e = 0; e < 16; ++e) ref[e] = __shfl_sync(0xffffffffu, g[0][e], 8 * I);
-    #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int t = 2 * lane + (i ^ fl);
-                        if (t < 16 * I + 16) {
-                            const bool live = t < valid, in_block = t >= 16 * I;
-    #pragma unroll
-                            for (int k = 0; k < 2; ++k) {
-                                const uint32_t off = slab * 16384 + sw128_offset(t, col + 8 * k);
-                                float kf[8], qf[8], kbf[8], kh[8], qh[8];
-                                if (live) {
-                                    unpack8(*reinterpret_cast<const uint4 *>(S.kq + off), kf);
-                                    unpack8(*reinterpret_cast<const uint4 *>(S.kq + off + 8192), qf);
-                                } else {
-    #pragma unroll
-                                    for (int e = 0; e < 8; ++e) kf[e] = qf[e] = 0.f;
-                                }
-    #pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    const float gr = g[i][8 * k + e], rf = ref[8 * k + e];
-                                    kbf[e] = kf[e] * ex2_approx(rf - gr);
-                                    const float up = in_block ? ex2_approx(gr - rf) : 0.f;
-                                    kh[e] = kf[e] * up;
-                                    qh[e] = qf[e] * up;
-                                }
-                                *reinterpret_cast<uint4 *>(Y + xrow_offset(t, c0 + 8 * k)) = pack8(kbf);
-                                if (in_block) {
-                                    *reinterpret_cast<uint4 *>(X + xrow_offset(t - 16 * I, c0 + 8 * k)) =
-                                        pack8(kh);
-                                    *reinterpret_cast<uint4 *>(X + xrow_offset(16 + t - 16 * I, c0 + 8 * k)) =
-                                        pack8(qh);
-                                }
-                            }
-                        }
-                    }
-                    named_bar_sync(kBarPrep, kPrepThreads);  // X and Y of block I are staged
-                    // tiles (mt, nt): mt 0 = the K rows (A), 1 = the Q rows (M);
-                    // columns j = 8 nt .. 8 nt + 7, nt < 2 (I + 1)
-                    const int ntiles = 2 * (I + 1);
-                    for (int idx = pw; idx < 2 * ntiles; idx += kPrepWarps) {
-                        const int mt = idx / ntiles, nt = idx % ntiles;
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const int ca = 16 * kk + 2 * t4;
-                            uint32_t a[4];
-                            a[0] = *reinterpret_cast<const uint32_t *>(X + xrow_offset(16 * mt + g8, ca));
-                            a[1] = *reinterpret_cast<const uint32_t *>(X + xrow_offset(16 * mt + g8 + 8, ca));
-                            a[2] = *reinterpret_cast<const uint32_t *>(X + xrow_offset(16 * mt + g8, ca + 8));
-                            a[3] = *reinterpret_cast<const uint32_t *>(X + xrow_offset(16 * mt + g8 + 8, ca + 8));
-                            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(Y + xrow_offset(8 * nt + g8, ca));
-                            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(Y + xrow_offset(8 * nt + g8, ca + 8));
-                            mma_bf16_16816(acc, a, b0, b1);
-                        }
-                        // rows r = 16 I + g8 (acc 0, 1) and r + 8 (acc 2, 3); columns j, j + 1
-                        const int j = 8 * nt + 2 * t4;
-    #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int r = 16 * I + g8 + 8 * hh;
-                            const float v0 = acc[2 * hh], v1 = acc[2 * hh + 1];
-                            if (mt == 0) {  // fp32, beta-scaled; only j < r is ever read
-                                const float br = S.bet[r];
-                                *reinterpret_cast<float2 *>(&sm.as[r * LDA + j]) = make_float2(br * v0, br * v1);
-                            } else {        // bf16 operand, diagonal included
-                                *reinterpret_cast<uint32_t *>(S.m + sw128_offset(r, j)) =
-                                    pack_bf16(j <= r ? v0 : 0.f, j + 1 <= r ? v1 : 0.f);
-                            }
-                        }
-                    }
-                    // M is zero right of the block's columns: rows of block I, 16-byte
-                    // pieces 2 (I + 1) .. 7
-                    const int np = 6 - 2 * I;
-                    for (int q = pt; q < 16 * np; q += kPrepThreads) {
-                        const int r = 16 * I + q / np, piece = 2 * (I + 1) + q % np;
-                        *reinterpret_cast<uint4 *>(S.m + sw128_offset(r, 8 * piece)) = make_uint4(0, 0, 0, 0);
-                    }
-                    named_bar_sync(kBarPrep, kPrepThreads);  // X and Y are free again
+    // G2 at the block's first token (lane 8 I, slot 0) and at token 63 (lane 31, slot 0)
+    {  // factor table: lane 8 I + J (J < I) writes 2^(G2_16I - G2_16J) for this warp's channels
+        const int J = lane & 7;
+        uint32_t g0[16];
+        tmem_ld16(gaddr, g0);
+        float fi[16], fj[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            fi[e] = __shfl_sync(0xffffffffu, __uint_as_float(g0[e]), lane & 24);
+            fj[e] = __shfl_sync(0xffffffffu, __uint_as_float(g0[e]), 8 * min(J, 3));
+        }
+        if (J < I) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) fj[e] = ex2_approx(fi[e] - fj[e]);
+            float4 *dst = reinterpret_cast<float4 *>(sm.bfac[I * (I - 1) / 2 + J] + c0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                dst[q] = make_float4(fj[4 * q], fj[4 * q + 1], fj[4 * q + 2], fj[4 * q + 3]);
+        }
+    }
+    // one pass over this thread's 2 tokens x 16 channels (8 channels at a
+    // time): the block-referenced Kh, Qh (over the landed k / q tile) and Kb
+    // (kb area), and the chunk-start Kh = k 2^G2, Qh and K~ as bf16 pairs,
+    // parked in tensor memory until the products have read the tiles -- Kh and
+    // Qh in this thread's 32 columns of the R accumulator (no R product on this
+    // path), K~ over G2 columns 0-15 once each 8-column piece has been read;
+    // column 8 k + 4 i (+ 16 for Qh) starts the pairs of slot i, channels c0 + 8 k ..
+    const uint32_t park = gaddr - (kColG - kColR);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        uint32_t gk[2][8];  // G2 of slot i, channels c0 + 8 k ..
+        tmem_ld8(gaddr + 8 * k, gk[0]);
+        tmem_ld8(gaddr + 16 + 8 * k, gk[1]);
+        float ref[8], g63[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            ref[e] = __shfl_sync(0xffffffffu, __uint_as_float(gk[0][e]), lane & 24);
+            g63[e] = __shfl_sync(0xffffffffu, __uint_as_float(gk[0][e]), 31);
+        }
+        uint32_t khs[8], qhs[8], kts[8];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int t = 2 * lane + (i ^ fl);
+            const uint32_t off = slab * 16384 + sw128_offset(t, col + 8 * k);
+            const uint32_t offv = slab * 8192 + sw128_offset(t, col + 8 * k);
+            float kf[8], qf[8], kh[8], qh[8], kb[8], ks[8], qs[8], kt[8];
+            if (t < valid) {
+                unpack8(*reinterpret_cast<const uint4 *>(S.kq + off), kf);
+                unpack8(*reinterpret_cast<const uint4 *>(S.kq + off + 8192), qf);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) kf[e] = qf[e] = 0.f;
+                *reinterpret_cast<uint4 *>(S.v + offv) = make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float gr = __uint_as_float(gk[i][e]);
+                const float up = ex2_approx(gr - ref[e]);
+                kh[e] = kf[e] * up;
+                qh[e] = qf[e] * up;
+                kb[e] = kf[e] * ex2_approx(ref[e] - gr);
+                kt[e] = kf[e] * ex2_approx(g63[e] - gr);
+                const float gam = ex2_approx(gr);  // Gamma
+                ks[e] = kf[e] * gam;
+                qs[e] = qf[e] * gam;
+                // gamma: token 63 closes the chunk, and lane 31 holds it in slot 0
+                if (i == 0 && lane == 31) S.gam[c0 + 8 * k + e] = gam;
+            }
+            *reinterpret_cast<uint4 *>(S.kq + off) = pack8(kh);
+            *reinterpret_cast<uint4 *>(S.kq + off + 8192) = pack8(qh);
+            *reinterpret_cast<uint4 *>(S.kb + offv) = pack8(kb);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                khs[4 * i + e] = pack_bf16(ks[2 * e], ks[2 * e + 1]);
+                qhs[4 * i + e] = pack_bf16(qs[2 * e], qs[2 * e + 1]);
+                kts[4 * i + e] = pack_bf16(kt[2 * e], kt[2 * e + 1]);
+            }
+        }
+        tmem_st8(park + 8 * k, khs);
+        tmem_st8(park + 16 + 8 * k, qhs);
+        tmem_st8(gaddr + 8 * k, kts);
+    }
+    // M is zero right of the block's columns: warp pw clears 16-byte piece pw
+    // (columns 8 pw .. 8 pw + 7) of its rows from piece 2 (I + 1) on
+    if (pw >= 2 * (I + 1)) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            *reinterpret_cast<uint4 *>(S.m + sw128_offset(2 * lane + i, 8 * pw)) = make_uint4(0, 0, 0, 0);
+    }
+    tmem_wait_st();
+    named_bar_sync(kBarPrep, kPrepThreads);  // operands, factors and beta are in place
+    if (pt == 0) sm.wide_chunk[s] = 0;       // (every thread has read it)
+
+    // the products: A (fp32, beta-scaled, where the solve reads it) and M
+    // (bf16, diagonal included)
+    const int g8 = lane >> 2, t4 = lane & 3;
+#pragma unroll 1
+    for (int u = pw; u < 20; u += kPrepWarps) {
+        const int code = kBlockedTiles[u];
+        const int mt = code >> 4, bi = (code >> 2) & 3, bj = code & 3;
+        float acc[2][4] = {};
+        if (bj < bi)
+            blocked_tile<true>(sm, S, mt, bi, bj, lane, acc);
+        else
+            blocked_tile<false>(sm, S, mt, bi, bj, lane, acc);
+        // rows r = 16 bi + g8 (acc 0, 1) and r + 8 (acc 2, 3); columns j, j + 1
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int j = 16 * bj + 8 * hh + 2 * t4;
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int r = 16 * bi + g8 + 8 * rr;
+                const float v0 = acc[hh][2 * rr], v1 = acc[hh][2 * rr + 1];
+                if (mt == 0) {  // only j < r is ever read
+                    const float br = S.bet[r];
+                    *reinterpret_cast<float2 *>(&sm.as[r * LDA + j]) = make_float2(br * v0, br * v1);
+                } else {
+                    *reinterpret_cast<uint32_t *>(S.m + sw128_offset(r, j)) =
+                        pack_bf16(j <= r ? v0 : 0.f, j + 1 <= r ? v1 : 0.f);
                 }
-                // chunk-start operands over the landed tiles: Kh = K Gamma, Qh = Q Gamma,
-                // and K~ = K 2^(G2_63 - G2) into the kb area
-                float g63[16];
-    #pragma unroll
-                for (int e = 0; e < 16; ++e) g63[e] = __shfl_sync(0xffffffffu, g[0][e], 31);
-    #pragma unroll
-                for (int ik = 0; ik < 4; ++ik) {
-                    const int i = ik >> 1, k = ik & 1;
-                    const float *gr = g[i] + 8 * k;
-                    const int t = 2 * lane + (i ^ fl);
-                    const uint32_t off = slab * 16384 + sw128_offset(t, col + 8 * k);
-                    const uint32_t offv = slab * 8192 + sw128_offset(t, col + 8 * k);
-                    float kf[8], qf[8], kt[8], gfv[8];
-                    if (t < valid) {
-                        unpack8(*reinterpret_cast<const uint4 *>(S.kq + off), kf);
-                        unpack8(*reinterpret_cast<const uint4 *>(S.kq + off + 8192), qf);
-                    } else {
-    #pragma unroll
-                        for (int e = 0; e < 8; ++e) kf[e] = qf[e] = 0.f;
-                        *reinterpret_cast<uint4 *>(S.v + offv) = make_uint4(0, 0, 0, 0);
-                    }
-    #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        gfv[e] = ex2_approx(gr[e]);
-                        kt[e] = kf[e] * ex2_approx(g63[8 * k + e] - gr[e]);
-                        kf[e] *= gfv[e];
-                        qf[e] *= gfv[e];
-                    }
-                    *reinterpret_cast<uint4 *>(S.kq + off) = pack8(kf);
-                    *reinterpret_cast<uint4 *>(S.kq + off + 8192) = pack8(qf);
-                    *reinterpret_cast<uint4 *>(S.kb + offv) = pack8(kt);
-                    if (i == 0 && lane == 31) {  // gamma = Gamma of token 63
-                        float4 *gd = reinterpret_cast<float4 *>(S.gam + c0 + 8 * k);
-                        gd[0] = make_float4(gfv[0], gfv[1], gfv[2], gfv[3]);
-                        gd[1] = make_float4(gfv[4], gfv[5], gfv[6], gfv[7]);
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                named_bar_sync(kBarPrep, kPrepThreads);
+            }
+        }
+    }
+    named_bar_sync(kBarPrep, kPrepThreads);  // the block-referenced tiles are read
+
+    // the chunk-start operands over them
+    {
+        uint32_t x[32], y[16];
+        tmem_ld32(park, x);
+        tmem_ld16(gaddr, y);
+#pragma unroll
+        for (int ik = 0; ik < 4; ++ik) {
+            const int i = ik >> 1, k = ik & 1;
+            const int t = 2 * lane + (i ^ fl);
+            const uint32_t off = slab * 16384 + sw128_offset(t, col + 8 * k);
+            const uint32_t offv = slab * 8192 + sw128_offset(t, col + 8 * k);
+            const int q = 8 * k + 4 * i;
+            *reinterpret_cast<uint4 *>(S.kq + off) = make_uint4(x[q], x[q + 1], x[q + 2], x[q + 3]);
+            *reinterpret_cast<uint4 *>(S.kq + off + 8192) =
+                make_uint4(x[16 + q], x[17 + q], x[18 + q], x[19 + q]);
+            *reinterpret_cast<uint4 *>(S.kb + offv) = make_uint4(y[q], y[q + 1], y[q + 2], y[q + 3]);
+        }
+    }
+    fence_proxy_async_smem();
+    // the previous chunk's W and U~ products (issued by the carry warps) have
+    // finished reading sm.tp, which the solve overwrites next
+    if (pt == 0 && n >= 1) wait_phase(sm.ready[s ^ 1], ((n - 1) >> 1) & 1, abort);
+    tc_fence_before();
+    named_bar_sync(kBarPrep, kPrepThreads);
 }
 
 // kTasks: task-table mode (segment-parallel forward); the plain instantiation
