@@ -92,10 +92,14 @@ kda_status_t check_fwd(const void *q, const void *k, const void *v, const float 
     if (!workspace) return KDA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KDA_ERR_INVALID_ARGUMENT;
 
+    // tensor cores: bf16 at d = 128 (the blocked path for wide gates only there),
+    // fp32 or bf16 at d = 64
     const bool tc_ok = kda::prefill_tc_supported(dtype, d_k, d_v) && Ttot <= INT32_MAX;
-    const bool tc_engine = engine == KDA_ENGINE_TENSORCORE || engine == KDA_ENGINE_TENSORCORE_WIDE;
-    if (tc_engine && !tc_ok) return KDA_ERR_UNSUPPORTED;
-    use_tc = tc_engine || (engine == KDA_ENGINE_AUTO && tc_ok);
+    const bool tc64_ok = d_k == 64 && d_v == 64 && Ttot <= INT32_MAX;
+    if (engine == KDA_ENGINE_TENSORCORE_WIDE && !tc_ok) return KDA_ERR_UNSUPPORTED;
+    if (engine == KDA_ENGINE_TENSORCORE && !(tc_ok || tc64_ok)) return KDA_ERR_UNSUPPORTED;
+    use_tc = engine == KDA_ENGINE_TENSORCORE || engine == KDA_ENGINE_TENSORCORE_WIDE ||
+             (engine == KDA_ENGINE_AUTO && tc_ok);
 
     p = kda::FwdParams{};
     p.tasks = nullptr;
@@ -144,7 +148,7 @@ kda_status_t kda_fwd_engine(const void *q, const void *k, const void *v,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (kda::launch_schedule(p, s) != cudaSuccess) return KDA_ERR_CUDA;
     if (N == 0) return KDA_OK;
-    const cudaError_t e = use_tc ? kda::launch_prefill_tc(p, s)
+    const cudaError_t e = use_tc ? kda::launch_prefill_tensorcore(p, dtype, s)
                                  : kda::launch_prefill_simt(p, dtype, s);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -181,7 +185,7 @@ kda_status_t kda_fwd_gated(const void *q, const void *k, const void *v, const fl
     if (!(eps >= 0.f) || eps > 3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
     if (p.Ttot > 0 && (!g || !aligned16(g))) return KDA_ERR_INVALID_ARGUMENT;
     if (norm_weight && !aligned(norm_weight, 4)) return KDA_ERR_INVALID_ARGUMENT;
-    if (mode == KDA_EPILOGUE_FUSED && (!use_tc || p.blocked)) return KDA_ERR_UNSUPPORTED;
+    if (mode == KDA_EPILOGUE_FUSED && (!use_tc || p.blocked || d_k != 128)) return KDA_ERR_UNSUPPORTED;
     if (workspace_bytes < kda_fwd_workspace_bytes(N)) return KDA_ERR_WORKSPACE;
     if (fault_injected()) return KDA_ERR_CUDA;
 
@@ -195,7 +199,7 @@ kda_status_t kda_fwd_gated(const void *q, const void *k, const void *v, const fl
         p.eps = eps;
         e = kda::launch_prefill_tc(p, s);
     } else {  // o into y, then the epilogue in place (measured faster: AUTO)
-        e = use_tc ? kda::launch_prefill_tc(p, s) : kda::launch_prefill_simt(p, dtype, s);
+        e = use_tc ? kda::launch_prefill_tensorcore(p, dtype, s) : kda::launch_prefill_simt(p, dtype, s);
         if (e == cudaSuccess)
             e = kda::launch_gated_rmsnorm(y, g, norm_weight, eps, p.Ttot * H, d_v, dtype, y, s);
     }

@@ -279,7 +279,7 @@ cudaError_t launch_fwd_cp(const FwdParams &base, kda_dtype_t dt, bool use_tc, in
         p.order = nullptr;
         p.vzero = ws + L.vzero;
         p.blocked = 0;  // task-table mode runs the plain tensor-core variant
-        return use_tc ? launch_prefill_tc(p, s) : launch_prefill_simt(p, dt, s);
+        return use_tc ? launch_prefill_tensorcore(p, dt, s) : launch_prefill_simt(p, dt, s);
     };
     if ((e = run(L.tasks_a, N * (2 * P - 1))) != cudaSuccess) return e;
     const unsigned grid = (unsigned)((size_t)N * H * (d / kScanRows));

@@ -147,6 +147,10 @@ cudaError_t launch_schedule(const FwdParams &p, cudaStream_t s);
 cudaError_t launch_prefill_simt(const FwdParams &p, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_prefill_tc(const FwdParams &p, cudaStream_t s);
 bool prefill_tc_supported(kda_dtype_t dt, int dk, int dv);
+// d_k = d_v = 64, fp32 or bf16 q/k/v, to fp32 accuracy (bf16 hi/lo operand pairs)
+cudaError_t launch_prefill_tc64(const FwdParams &p, kda_dtype_t dt, cudaStream_t s);
+// the tensor-core engine for the head size: d = 64 -> launch_prefill_tc64, else launch_prefill_tc
+cudaError_t launch_prefill_tensorcore(const FwdParams &p, kda_dtype_t dt, cudaStream_t s);
 cudaError_t launch_verify(const void *q, const void *k, const void *v, const float *log_alpha,
                           const float *beta, const float *S, int N, int K, int H, int d,
                           kda_dtype_t dt, void *o, cudaStream_t s);

@@ -454,11 +454,17 @@ __device__ __noinline__ void blocked_chunk(TcSmem &sm, TcStage &S, uint32_t gadd
         uint32_t gk[2][8];  // G2 of slot i, channels c0 + 8 k ..
         tmem_ld8(gaddr + 8 * k, gk[0]);
         tmem_ld8(gaddr + 16 + 8 * k, gk[1]);
-        float ref[8], g63[8];
+        // per channel: G2 at the block's first token (ref), 2^ref, and
+        // 2^(G2_63 - ref + 64) for K~ = (Kb 2^-64) 2^(G2_63 - ref + 64): two
+        // exact-range factors, since 2^(G2_63 - ref) alone can underflow while
+        // K~ = k 2^(G2_63 - G2) is still a normal number
+        float ref[8], pref[8], p63[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             ref[e] = __shfl_sync(0xffffffffu, __uint_as_float(gk[0][e]), lane & 24);
-            g63[e] = __shfl_sync(0xffffffffu, __uint_as_float(gk[0][e]), 31);
+            const float g63 = __shfl_sync(0xffffffffu, __uint_as_float(gk[0][e]), 31);
+            pref[e] = ex2_approx(ref[e]);
+            p63[e] = ex2_approx(g63 - ref[e] + 64.f);
         }
         uint32_t khs[8], qhs[8], kts[8];
 #pragma unroll
@@ -482,8 +488,9 @@ __device__ __noinline__ void blocked_chunk(TcSmem &sm, TcStage &S, uint32_t gadd
                 kh[e] = kf[e] * up;
                 qh[e] = qf[e] * up;
                 kb[e] = kf[e] * ex2_approx(ref[e] - gr);
-                kt[e] = kf[e] * ex2_approx(g63[e] - gr);
-                const float gam = ex2_approx(gr);  // Gamma
+                kt[e] = kb[e] * 0x1p-64f * p63[e];
+                // Gamma = 2^G2 (it underflows only where 2^ref does, below fp32's range)
+                const float gam = up * pref[e];
                 ks[e] = kf[e] * gam;
                 qs[e] = qf[e] * gam;
                 // gamma: token 63 closes the chunk, and lane 31 holds it in slot 0

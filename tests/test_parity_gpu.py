@@ -33,7 +33,13 @@ def kda():
 
 
 def engine_ok(engine, dtype, d):
-    return not engine.startswith("tensorcore") or (dtype == "bf16" and d == 128)
+    """The tensor-core engine takes bf16 at d = 128 and fp32 or bf16 at d = 64;
+    its variant with the blocked path for wide gates only bf16 at d = 128."""
+    if engine == "tensorcore_wide":
+        return dtype == "bf16" and d == 128
+    if engine == "tensorcore":
+        return d == 64 or dtype == "bf16"
+    return True
 
 
 def assert_engine_rejects(kda, call):
@@ -82,6 +88,32 @@ def test_prefill_varlen_small(kda, engine):
     for i, L in enumerate(lengths):
         if L == 0:
             assert torch.equal(ST[i], prob.S0[i])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_prefill_d64_tensorcore_varlen_in_place(kda, dtype):
+    """d = 64 on the tensor cores: packed sequences with empty, one-token and
+    ragged ones, S_T written over S0, one head with gates past the chunk form's
+    range (recomputed token by token); fp32 inputs at the fp32 tolerance."""
+    lengths = [0, 1, 64, 130, 7, 0, 257, 63]
+    prob = I.prefill_problem(1, 0, 3, 64, 64, dtype, (-0.5, -0.001), 0.05, seed=41,
+                             device=DEV, lengths=lengths)
+    la = prob.log_alpha.cpu()
+    la[266:266 + 100, 1] = -3.0                # head 1 of the 257-token sequence: wide
+    prob.log_alpha.copy_(la.to(DEV))
+    o_ref, S_ref = oracle_on_heads(prob, [0, 1, 2])
+    S = prob.S0.clone()
+    ws = torch.zeros(kda.kda_fwd_workspace_bytes(len(lengths)), dtype=torch.uint8, device=DEV)
+    o, _ = kda.kda_fwd(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, S, prob.cu_seqlens,
+                       S_T=S, workspace=ws, engine="tensorcore")
+    torch.cuda.synchronize()
+    assert kda.kda_read_device_status(ws) == kda.KDA_OK
+    dt = prob.q.dtype
+    assert rel_err(o, o_ref) < tol_o(dt)
+    assert rel_err(S, S_ref) < tol_s(dt)
+    for i, L in enumerate(lengths):
+        if L == 0:
+            assert torch.equal(S[i], prob.S0[i])
 
 
 @pytest.mark.parametrize("engine", ENGINES)
