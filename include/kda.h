@@ -73,8 +73,11 @@ typedef enum {
 } kda_dtype_t;
 
 typedef enum {
-    KDA_ENGINE_AUTO = 0,        /* tensor-core kernel where supported, else CUDA-core kernel */
-    KDA_ENGINE_TENSORCORE = 1,  /* tcgen05/TMEM/TMA kernel: bf16, d = 128 only */
+    KDA_ENGINE_AUTO = 0,        /* the tensor-core engine for bf16 at d = 128 and fp32 at
+                                   d = 64, the CUDA-core engine otherwise (measured fastest) */
+    KDA_ENGINE_TENSORCORE = 1,  /* tcgen05 kernels: bf16 at d = 128 (TMA, warp-specialised);
+                                   fp32 or bf16 at d = 64, to fp32 accuracy (every operand a
+                                   bf16 hi/lo pair, three products per K slice) */
     KDA_ENGINE_CUDACORE = 2,    /* fp32 CUDA-core chunkwise kernel: any supported dtype/d */
     KDA_ENGINE_TENSORCORE_WIDE = 3  /* the tensor-core kernel with the blocked path for
                                        chunks outside the chunk form's log-decay range
