@@ -101,7 +101,11 @@ def test_fwd_argument_errors(kda):
     assert fwd_call(lib, ws=None) == E_WS
     assert fwd_call(lib, wsb=8) == E_WS
     assert fwd_call(lib, engine=9) == E_INV
-    assert fwd_call(lib, engine=1, dt=0) == E_UNS                      # tensor cores: bf16 only
+    # tensor cores: bf16 at d = 128, fp32 or bf16 at d = 64; the blocked-path
+    # variant bf16 at d = 128 only
+    assert fwd_call(lib, engine=1, dt=0, dk=128, dv=128) == E_UNS
+    assert fwd_call(lib, engine=3, dt=0, dk=128, dv=128) == E_UNS
+    assert fwd_call(lib, engine=3, dt=1) == E_UNS
 
 
 def cp_call(lib, segments=2, **kw):
@@ -135,7 +139,7 @@ def test_cp_argument_errors(kda):
     assert cp_call(lib, segments=70000) == E_INV
     assert cp_call(lib, q=None) == E_INV
     assert cp_call(lib, dk=96, dv=96) == E_UNS
-    assert cp_call(lib, engine=1, dt=0) == E_UNS
+    assert cp_call(lib, engine=1, dt=0, dk=128, dv=128) == E_UNS      # fp32 at d = 128: CUDA cores
     assert cp_call(lib, ws=None) == E_WS
     need = kda.kda_fwd_cp_workspace_bytes(1, 2, 64, 64, 4)
     assert cp_call(lib, segments=4, wsb=need - 1) == E_WS
