@@ -312,6 +312,31 @@ def test_bounds_checked_build(kda, engine):
         assert rel_err(ST, S_ref) < 1e-2
 
 
+def test_bounds_checked_build_d64_tensorcore(kda):
+    """The bounds-checked build through the d = 64 tensor-core engine: fp32
+    fixed-length and ragged packed sequences with empty ones, a wide-gate head
+    (token-serial pass), and kda_fwd_cp's task tables -- no report, results
+    against the oracle at the fp32 tolerance."""
+    lib = kda.load_library(kbuild.build(bounds_check=True))
+    cases = [I.prefill_problem(2, 65, 2, 64, 64, "f32", (-0.5, -0.001), 0.05, seed=12,
+                               device=DEV),
+             I.prefill_problem(1, 0, 2, 64, 64, "f32", (-0.5, -0.001), 0.05, seed=13,
+                               device=DEV, lengths=[0, 130, 1, 64, 0, 7]),
+             I.prefill_problem(1, 0, 2, 64, 64, "f32", (-5.0, -0.5), 0.05, seed=14,
+                               device=DEV, lengths=[70, 0, 3])]
+    for prob in cases:
+        n = prob.S0.shape[0]
+        ws = torch.zeros(int(lib.kda_fwd_cp_workspace_bytes(n, 2, 64, 64, 3)),
+                         dtype=torch.uint8, device=DEV)
+        o_ref, S_ref = oracle_on_heads(prob, [0, 1])
+        for call in (kda.kda_fwd, lambda *a, **k: kda.kda_fwd_cp(*a, segments=3, **k)):
+            o, ST = call(prob.q, prob.k, prob.v, prob.log_alpha, prob.beta, prob.S0,
+                         prob.cu_seqlens, workspace=ws, engine="tensorcore", lib=lib)
+            assert kda.kda_read_device_status(ws, lib=lib) == kda.KDA_OK
+            assert rel_err(o, o_ref) < 1e-4
+            assert rel_err(ST, S_ref) < 1e-4
+
+
 def test_cuda_graph_capture(kda):
     """kda_fwd, kda_fwd_cp and kda_decode_step enqueue kernels only (no
     allocation, no synchronisation), so each can be captured in a CUDA graph;
