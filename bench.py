@@ -46,6 +46,7 @@ _CSRC = "linear_attention_recurrence_chunkwise_gb300/csrc/"
 KERNEL_SOURCES = {  # every source file a kernel is compiled from
     "prefill_tc": (_CSRC + "kda_prefill_tc.cu", _CSRC + "kda_solve.cuh", _CSRC + "kda_sm100.cuh",
                    _CSRC + "kda_serial.cuh"),
+    "prefill_tc64": (_CSRC + "kda_prefill_tc64.cu", _CSRC + "kda_sm100.cuh"),
     "prefill_simt": (_CSRC + "kda_prefill_simt.cu", _CSRC + "kda_serial.cuh"),
     "decode": (_CSRC + "kda_decode.cu",),
     "multitoken": (_CSRC + "kda_multitoken.cu",),
@@ -373,8 +374,11 @@ def run_ours(args, world, rank):
         unit = "tokens/s"
         alg = prefill_alg_bytes(w)
         flops = prefill_flops(w)
-        kernel_key = "prefill_tc" if (w["prob"].q.dtype == torch.bfloat16 and w["d"] == 128) \
-            else "prefill_simt"
+        # the engine kda_fwd's AUTO choice runs: tensor cores for bf16 at d = 128
+        # and for any dtype at d = 64, CUDA cores otherwise
+        bf16 = w["prob"].q.dtype == torch.bfloat16
+        kernel_key = "prefill_tc" if (bf16 and w["d"] == 128) else \
+            "prefill_tc64" if w["d"] == 64 else "prefill_simt"
     else:
         value = 2 * nbytes(w["S"]) * world / (ms_step / 1e3) / 1e9
         unit = "GB/s"

@@ -73,8 +73,8 @@ typedef enum {
 } kda_dtype_t;
 
 typedef enum {
-    KDA_ENGINE_AUTO = 0,        /* the tensor-core engine for bf16 at d = 128 and fp32 at
-                                   d = 64, the CUDA-core engine otherwise (measured fastest) */
+    KDA_ENGINE_AUTO = 0,        /* the tensor-core engine where it runs (bf16 at d = 128,
+                                   any dtype at d = 64), else the CUDA-core engine */
     KDA_ENGINE_TENSORCORE = 1,  /* tcgen05 kernels: bf16 at d = 128 (TMA, warp-specialised);
                                    fp32 or bf16 at d = 64, to fp32 accuracy (every operand a
                                    bf16 hi/lo pair, three products per K slice) */

@@ -98,10 +98,10 @@ kda_status_t check_fwd(const void *q, const void *k, const void *v, const float 
     const bool tc64_ok = d_k == 64 && d_v == 64 && Ttot <= INT32_MAX;
     if (engine == KDA_ENGINE_TENSORCORE_WIDE && !tc_ok) return KDA_ERR_UNSUPPORTED;
     if (engine == KDA_ENGINE_TENSORCORE && !(tc_ok || tc64_ok)) return KDA_ERR_UNSUPPORTED;
-    // AUTO: the faster engine as measured -- at d = 64 the tensor cores for fp32
-    // inputs (1.5-1.9x the CUDA-core engine), the CUDA cores for bf16 (1.3x)
+    // AUTO: the tensor cores wherever they run (at d = 64 they take 0.6 of the
+    // CUDA-core engine's time for fp32 inputs and 0.55 for bf16, measured)
     use_tc = engine == KDA_ENGINE_TENSORCORE || engine == KDA_ENGINE_TENSORCORE_WIDE ||
-             (engine == KDA_ENGINE_AUTO && (tc_ok || (tc64_ok && dtype == KDA_F32)));
+             (engine == KDA_ENGINE_AUTO && (tc_ok || tc64_ok));
 
     p = kda::FwdParams{};
     p.tasks = nullptr;

@@ -61,9 +61,12 @@ struct __align__(1024) Tc64Smem {
     uint8_t tp[16384];  // T' [r][j] K-major: hi | lo
     uint8_t wn[16384];  // -W as [c][r] (MN-major B of U): hi | lo
     uint8_t mm[16384];  // M [r][j] K-major: hi | lo
+    uint8_t raw[4 * C * 256];  // the next chunk's rows as they are in memory (cp.async):
+                               // log_alpha, k, q, v, 64 rows each of 64 elements
     float a[C * LDA];   // beta-scaled A (fp32); staging of the token-by-token pass
     float gam[D];
     float bet[C];
+    float rbet[C];      // the next chunk's beta
     uint64_t bar_mma, bar_fin;
     uint32_t tmem_base;
     int abort;
@@ -77,6 +80,20 @@ __device__ __forceinline__ void wait_bounded(uint64_t &bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(smem_u32(&bar), parity))
         if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+}
+
+// Global -> shared copies that complete asynchronously (cp.async; waited for
+// with cp_async_wait_all before a barrier).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // byte offset of element (row, col) of a 64-column tile part (128-byte rows)
@@ -325,21 +342,55 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
     const uint32_t id_mk = idesc_bf16(128, 64, true, false);   // MN-major A
     const uint32_t id_km = idesc_bf16(128, 64, false, true);   // MN-major B
 
+    // chunk m's rows of log_alpha, k, q, v and its beta -> sm.raw / sm.rbet (all
+    // threads, 16-byte copies; rows past the sequence end are not copied)
+    constexpr int kRow = D * (int)sizeof(T);  // bytes of one k / q / v row
+    float *raw_la = reinterpret_cast<float *>(sm.raw);
+    const T *raw_k = reinterpret_cast<const T *>(sm.raw + C * 256);
+    const T *raw_q = reinterpret_cast<const T *>(sm.raw + 2 * C * 256);
+    const T *raw_v = reinterpret_cast<const T *>(sm.raw + 3 * C * 256);
+    auto prefetch = [&](int m) {
+        const int64_t tm = start + (int64_t)m * C;
+        const int vm = min(C, len - m * C);
+        for (int i = tid; i < vm * 16; i += kThreads) {  // log_alpha: 16 pieces per row
+            const int t = i >> 4, c4 = (i & 15) * 4;
+            const size_t g = ((size_t)(tm + t) * p.H + h) * D + c4;
+            if (in_bounds(p.status, g + 3, n_tok)) cp_async16(raw_la + t * D + c4, p.log_alpha + g);
+        }
+        constexpr int kPieces = kRow / 16;
+        for (int i = tid; i < 3 * vm * kPieces; i += kThreads) {
+            const int w = i / (vm * kPieces), r = i % (vm * kPieces);
+            const int t = r / kPieces, e = (r % kPieces) * (16 / (int)sizeof(T));
+            if (w == 2 && vzero) continue;
+            const T *src = w == 0 ? k : w == 1 ? q : v;
+            const size_t g = ((size_t)(tm + t) * p.H + h) * D + e;
+            if (in_bounds(p.status, g + 16 / sizeof(T) - 1, n_tok))
+                cp_async16(sm.raw + (w + 1) * C * 256 + t * kRow + e * sizeof(T), src + g);
+        }
+        if (tid < vm) {
+            const size_t bi = (size_t)(tm + tid) * p.H + h;
+            if (in_bounds(p.status, bi, n_beta)) cp_async4(&sm.rbet[tid], p.beta + bi);
+        }
+    };
+    prefetch(0);
+    cp_async_wait_all();
+    __syncthreads();
+
     for (int n = 0; n < nchunks; ++n) {
         const int64_t t0 = start + (int64_t)n * C;
         const int valid = min(C, len - n * C);
         // ---------------------------------------------- a1, a2: gates and operands
-        // thread c < 64: channel c of k, q and the gates; thread 64 + v: channel v
-        // of V and beta of token v
+        // from the staged rows: thread c < 64 takes channel c of k, q and the
+        // gates, thread 64 + v channel v of V and beta of token v
         if (tid < D) {
             const int c = tid;
             float G = 0.f;
 #pragma unroll 4
             for (int t = 0; t < C; ++t) {
-                const size_t i = ((size_t)(t0 + t) * p.H + h) * D + c;
-                const bool live = t < valid && in_bounds(p.status, i, n_tok);
-                G += live ? p.log_alpha[i] : 0.f;
-                const float kf = live ? ld(k, i) : 0.f, qf = live ? ld(q, i) : 0.f;
+                const bool live = t < valid;
+                G += live ? raw_la[t * D + c] : 0.f;
+                const float kf = live ? ld(raw_k, t * D + c) : 0.f;
+                const float qf = live ? ld(raw_q, t * D + c) : 0.f;
                 const float gf = expf(G), gi = expf(-G);
                 const float kh = kf * gf;
                 put(sm.xq, 16384, t, c, kh);
@@ -353,15 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
             const int vv = tid - D;
 #pragma unroll 4
             for (int t = 0; t < C; ++t) {
-                const size_t i = ((size_t)(t0 + t) * p.H + h) * D + vv;
-                const bool live = t < valid && !vzero && in_bounds(p.status, i, n_tok);
-                put(sm.kv + 8192, 16384, t, vv, live ? ld(v, i) : 0.f);
+                const bool live = t < valid && !vzero;
+                put(sm.kv + 8192, 16384, t, vv, live ? ld(raw_v, t * D + vv) : 0.f);
             }
-            const size_t bi = (size_t)(t0 + vv) * p.H + h;
-            sm.bet[vv] = vv < valid && in_bounds(p.status, bi, n_beta) ? p.beta[bi] : 0.f;
+            sm.bet[vv] = vv < valid ? sm.rbet[vv] : 0.f;
         }
         publish_smem();
         if (*reinterpret_cast<volatile int *>(&sm.domain)) break;  // (read by all after the barrier)
+        if (n + 1 < nchunks) prefetch(n + 1);  // the staged rows have been read
 
         // ---------------------------------------------- a3, a5: R = [Kh; Qh] Kb^T
         if (tid == 0) {
@@ -512,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
             }
             tmem_wait_st();
         }
+        cp_async_wait_all();  // the next chunk's rows have landed
         tc_fence_before();
         __syncthreads();
     }
