@@ -33,6 +33,17 @@ Contents
     . RMSNorm(o~)]; "完全拆解", the KDA layer's output).  numpy, the definition
     written out.
 
+``short_conv`` / ``prologue``
+    The input prologue of a KDA layer: a depthwise causal convolution of
+    kernel 4 along the sequence (ShortConv), Swish, and for q and k an L2
+    normalisation over the d channels of one (token, head)
+    ("Kimi K3 模型结构（1）", parameterisation section: depthwise causal, kernel
+    size 4, each token mixed with the previous 3, and the last 3 projected inputs
+    of q, k, v cached for decode; "Kimi Delta Attention 完全拆解", the KDA
+    layer's forward: q, k = L2Norm(Swish(ShortConv(W x))), v =
+    Swish(ShortConv(W_v x)); "Kimi K3" (gentlecold) section 3.3).  numpy,
+    token by token, the definition written out.
+
 ``verify_tokens`` / ``commit_tokens``
     Speculative-decode verification and commit over K cached draft tokens
     ("Kimi K3 深度拆解" section 9.2), written out as K (or n_accept[n]) calls of
@@ -196,6 +207,62 @@ def gated_rmsnorm(o, g, weight=None, eps=0.0):
     with np.errstate(over="ignore"):
         gate = 1.0 / (1.0 + np.exp(-g))                  # sigmoid
     return o / np.sqrt(ms + eps) * w * gate
+
+
+def short_conv(x, w, conv0=None, cu_seqlens=None, l2norm=False, eps=0.0):
+    """ShortConv(4) + Swish (+ L2Norm) of one stream, token by token.
+
+    x: [B, T, H, d] (fixed length) or [Ttot, H, d] with cu_seqlens [N+1];
+    w: [H, d, 4] depthwise taps, tap 3 on the current token and taps 0-2 on the
+    three before it, oldest first; conv0: [N, 3, H, d] the three inputs before
+    each sequence, oldest first, or None (zeros).  Per sequence and channel:
+      c_t = sum_{i=0..3} w[i] x_{t-3+i}   (x_{-3..-1} from conv0)
+      y_t = c_t * sigmoid(c_t)            (Swish)
+    and with l2norm, y_t / sqrt(sum_d y_t^2 + eps) over the d channels of one
+    (token, head) (zero where that sum is zero).  Returns (y float64 of x's
+    shape, conv_T [N, 3, H, d]: the last three inputs of each sequence, oldest
+    first -- with conv0's tail where the sequence has fewer than three)."""
+    x, w = _f64(x), _f64(w)
+    packed = cu_seqlens is not None
+    xs = x if packed else x.reshape((-1,) + x.shape[2:])
+    if packed:
+        cu = [int(c) for c in np.asarray(cu_seqlens).reshape(-1)]
+    else:
+        T = x.shape[1]
+        cu = [b * T for b in range(x.shape[0] + 1)]
+    N = len(cu) - 1
+    H, d = xs.shape[1], xs.shape[2]
+    hist0 = np.zeros((N, 3, H, d)) if conv0 is None else _f64(conv0)
+    y = np.zeros(xs.shape, dtype=np.float64)
+    conv_T = np.zeros((N, 3, H, d), dtype=np.float64)
+    for n in range(N):
+        win = [hist0[n, 0], hist0[n, 1], hist0[n, 2]]   # the three inputs before token t
+        for t in range(cu[n], cu[n + 1]):
+            cur = xs[t]
+            c = w[:, :, 0] * win[0] + w[:, :, 1] * win[1] + w[:, :, 2] * win[2] + w[:, :, 3] * cur
+            with np.errstate(over="ignore"):
+                yt = c / (1.0 + np.exp(-c))              # c * sigmoid(c)
+            if l2norm:
+                ss = np.sum(yt * yt, axis=-1, keepdims=True) + eps
+                yt = np.where(ss > 0, yt / np.sqrt(np.where(ss > 0, ss, 1.0)), 0.0)
+            y[t] = yt
+            win = [win[1], win[2], cur]
+        conv_T[n] = np.stack(win)
+    return (y if packed else y.reshape(x.shape)), conv_T
+
+
+def prologue(xq, xk, xv, wq, wk, wv, conv0=None, cu_seqlens=None, eps=0.0):
+    """The input prologue of a KDA layer for the three streams: q and k through
+    ShortConv(4), Swish and L2Norm, v through ShortConv(4) and Swish (see
+    short_conv).  conv0: [N, 3, 3, H, d] (stream q, k, v; three inputs, oldest
+    first) or None.  Returns (q, k, v, conv_T [N, 3, 3, H, d])."""
+    outs, states = [], []
+    for i, (x, w, norm) in enumerate(((xq, wq, True), (xk, wk, True), (xv, wv, False))):
+        y, st = short_conv(x, w, None if conv0 is None else _f64(conv0)[:, i], cu_seqlens,
+                           l2norm=norm, eps=eps)
+        outs.append(y)
+        states.append(st)
+    return outs[0], outs[1], outs[2], np.stack(states, axis=1)
 
 
 def verify_tokens(q, k, v, log_alpha, beta, S):

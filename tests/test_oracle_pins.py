@@ -274,3 +274,103 @@ def test_gated_rmsnorm_gate_is_the_logistic_function():
     assert np.allclose(y / plain, special.expit(g), rtol=1e-13, atol=0)
     half = oracle.gated_rmsnorm(o, np.zeros(o.shape), w, eps=0.25)
     assert np.allclose(half, 0.5 * plain, rtol=1e-15, atol=0)
+
+
+# ------------------------------------------------------- input prologue (ShortConv(4), Swish, L2Norm)
+
+def _swish_expit(c):
+    special = pytest.importorskip("scipy.special")
+    return c * special.expit(c)
+
+
+def test_short_conv_identity_taps_give_swish():
+    """Taps (0, 0, 0, 1) put the whole weight on the current token: the output
+    is Swish(x) = x * sigmoid(x) (scipy's expit), whatever the history."""
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((2, 9, 3, 8)) * 3
+    w = np.zeros((3, 8, 4))
+    w[:, :, 3] = 1.0
+    conv0 = rng.standard_normal((2, 3, 3, 8))
+    y, _ = oracle.short_conv(x, w, conv0)
+    assert np.allclose(y, _swish_expit(x), rtol=1e-14, atol=1e-15)
+
+
+def test_short_conv_delay_tap_is_causal_three_steps_back():
+    """Taps (1, 0, 0, 0) read the input three tokens back: zeros (no history)
+    for the first three tokens, then Swish(x_{t-3}); changing a later token
+    never changes an earlier output (causality)."""
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((1, 10, 2, 4))
+    w = np.zeros((2, 4, 4))
+    w[:, :, 0] = 1.0
+    y, _ = oracle.short_conv(x, w)
+    assert np.all(y[:, :3] == 0.0)
+    assert np.allclose(y[:, 3:], _swish_expit(x[:, :-3]), rtol=1e-14, atol=1e-15)
+    x2 = x.copy()
+    x2[:, 6:] += 5.0
+    y2, _ = oracle.short_conv(x2, w)
+    assert np.array_equal(y2[:, :9], y[:, :9])   # token 6 reaches outputs 9 on
+
+
+def test_short_conv_matches_numpy_convolution_with_history():
+    """General taps and a nonzero history against numpy's convolve (an
+    independent routine): the valid part of history ++ x convolved with the
+    reversed taps is the pre-Swish sum c_t = sum_i w_i x_{t-3+i}."""
+    rng = np.random.default_rng(43)
+    T, H, d = 12, 2, 5
+    x = rng.standard_normal((1, T, H, d))
+    w = rng.standard_normal((H, d, 4))
+    conv0 = rng.standard_normal((1, 3, H, d))
+    y, _ = oracle.short_conv(x, w, conv0)
+    c = np.zeros((T, H, d))
+    for h in range(H):
+        for ch in range(d):
+            seq = np.concatenate([conv0[0, :, h, ch], x[0, :, h, ch]])
+            c[:, h, ch] = np.convolve(seq, w[h, ch, ::-1], mode="valid")
+    assert np.allclose(y[0], _swish_expit(c), rtol=1e-12, atol=1e-14)
+
+
+def test_prologue_l2norm_unit_rows_for_q_and_k_only():
+    """With eps = 0, every (token, head) row of q and k has norm 1 (a norm over
+    the wrong axis fails this with heads of very different scales); v is not
+    normalised."""
+    rng = np.random.default_rng(44)
+    scale = np.array([1e-2, 1.0, 1e2])[None, None, :, None]
+    xq, xk, xv = (rng.standard_normal((2, 7, 3, 16)) * scale for _ in range(3))
+    wq, wk, wv = (rng.standard_normal((3, 16, 4)) for _ in range(3))
+    q, k, v, _ = oracle.prologue(xq, xk, xv, wq, wk, wv, eps=0.0)
+    assert np.allclose(np.linalg.norm(q, axis=-1), 1.0, rtol=1e-13)
+    assert np.allclose(np.linalg.norm(k, axis=-1), 1.0, rtol=1e-13)
+    v_plain, _ = oracle.short_conv(xv, wv)
+    assert np.array_equal(v, v_plain)
+
+
+def test_prologue_state_hand_off_and_varlen_isolation():
+    """Running a sequence in two pieces, the second from the first's final conv
+    state, equals one run (pieces of 2 tokens, shorter than the window,
+    included); packed sequences equal their runs alone; the final state is the
+    last three inputs of each stream."""
+    rng = np.random.default_rng(45)
+    H, d = 2, 6
+    lengths = [2, 7, 0, 1, 5]
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    Tt = int(cu[-1])
+    xs = [rng.standard_normal((Tt, H, d)) for _ in range(3)]
+    ws = [rng.standard_normal((H, d, 4)) for _ in range(3)]
+    conv0 = rng.standard_normal((len(lengths), 3, 3, H, d))
+    q, k, v, st = oracle.prologue(*xs, *ws, conv0, cu, eps=1e-6)
+    for n, L in enumerate(lengths):
+        a, b = int(cu[n]), int(cu[n + 1])
+        one = [x[a:b][None] for x in xs]
+        q1, k1, v1, st1 = oracle.prologue(*one, *ws, conv0[n:n + 1], eps=1e-6)
+        assert np.array_equal(q1[0], q[a:b]) and np.array_equal(v1[0], v[a:b])
+        assert np.array_equal(st1[0], st[n])
+        hist = np.concatenate([conv0[n, 0], xs[0][a:b]])     # stream q: history ++ inputs
+        assert np.array_equal(st[n, 0], hist[-3:])
+        for cut in range(0, L + 1):
+            p1 = [x[:, :cut] for x in one]
+            p2 = [x[:, cut:] for x in one]
+            qa, ka, va, sa = oracle.prologue(*p1, *ws, conv0[n:n + 1], eps=1e-6)
+            qb, kb, vb, sb = oracle.prologue(*p2, *ws, sa, eps=1e-6)
+            assert np.allclose(np.concatenate([qa, qb], 1), q1, rtol=0, atol=0)
+            assert np.array_equal(sb, st1)
