@@ -426,6 +426,7 @@ def run_ours(args, world, rank):
             line["draft"] = draft_sub(kda, args, stream, pk, line["decode"]["us_per_step"])
             line["segment_parallel"] = cp_sub(kda, args, stream, pk)
             line["epilogue"] = epilogue_sub(kda, args, stream, pk)
+            line["prologue"] = prologue_sub(kda, args, stream, pk)
             line["wide_gates"] = wide_gates_sub(kda, args, stream, pk)
             line["long"] = long_sub(kda, args, stream, pk, cpu)
             line["varlen"] = varlen_sub(kda, args, stream, pk, cpu)
@@ -628,6 +629,48 @@ def epilogue_sub(kda, args, stream, pk):
     out["workloads"] = "prefill B=1 H=96 T=8192 d=128 bf16; decode step N=64 H=96 d=128"
     out["auto_choice"] = {"prefill": "separate", "decode": "fused"}
     del wd
+    torch.cuda.empty_cache()
+    return out
+
+
+def prologue_sub(kda, args, stream, pk):
+    """The layer's input prologue (ShortConv(4), Swish, L2Norm of q and k) on
+    the prefill shape (B=1, T=8192, H=96, d=128, bf16; a pass of its own that
+    reads the three projected streams and writes q, k, v) and one decode token
+    for 64 sessions x 96 heads (the conv state moved on in place)."""
+    out = {"metric": "GB/s", "unit": "GB/s"}
+    T, H, d, N = 8192, 96, 128, 64
+    gen = torch.Generator(device="cuda").manual_seed(args.seed + 11)
+    xs = [torch.randn((1, T, H, d), generator=gen, device="cuda").to(torch.bfloat16)
+          for _ in range(3)]
+    ws = [0.5 * torch.randn((H, d, 4), generator=gen, device="cuda") for _ in range(3)]
+    c0 = torch.randn((1, 3, 3, H, d), generator=gen, device="cuda")
+    ys = [torch.empty_like(xs[0]) for _ in range(3)]
+    cT = torch.empty_like(c0)
+    wsp = torch.empty(kda.kda_fwd_workspace_bytes(1), dtype=torch.uint8, device="cuda")
+    ms = time_calls(lambda: kda.kda_short_conv(*xs, *ws, c0, q=ys[0], k=ys[1], v=ys[2],
+                                               conv_T=cT, workspace=wsp, stream=stream),
+                    10, stream)
+    alg = 3 * 2 * xs[0].numel() * 2 + 3 * H * d * 4 * 4 + 2 * c0.numel() * 4
+    out["prefill"] = {"workload": "prologue of B=1 T=8192 H=96 d=128 bf16 (q, k, v streams)",
+                      "us_per_call": round(ms * 1e3, 2), "value": round(alg / (ms / 1e3) / 1e9, 1),
+                      "roofline": hbm_roof(alg, ms, pk)}
+    del xs, ys
+    xd = [torch.randn((N, H, d), generator=gen, device="cuda").to(torch.bfloat16)
+          for _ in range(3)]
+    yd = [torch.empty_like(xd[0]) for _ in range(3)]
+    conv = torch.randn((N, 3, 3, H, d), generator=gen, device="cuda")
+    ms = time_calls(lambda: kda.kda_short_conv_step(*xd, *ws, conv, q=yd[0], k=yd[1], v=yd[2],
+                                                    stream=stream), 100, stream)
+    alg = 3 * 2 * xd[0].numel() * 2 + 3 * H * d * 4 * 4 + 2 * conv.numel() * 4
+    out["decode_step"] = {"workload": "prologue of one token, N=64 sessions H=96 d=128 bf16, "
+                                      "conv state [64,3,3,96,128] fp32 in place",
+                          "us_per_call": round(ms * 1e3, 2),
+                          "value": round(alg / (ms / 1e3) / 1e9, 1),
+                          "roofline": hbm_roof(alg, ms, pk),
+                          "note": "the 28 MB conv state fits in L2, so repeated steps may "
+                                  "re-read it from L2"}
+    del xd, yd, conv
     torch.cuda.empty_cache()
     return out
 

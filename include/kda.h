@@ -305,6 +305,52 @@ kda_status_t kda_gated_rmsnorm(const void *o, const void *g, const float *norm_w
                                void *stream);
 
 /*
+ * Input prologue of a KDA layer ("Kimi Delta Attention 完全拆解", the KDA
+ * layer's forward: q, k = L2Norm(Swish(ShortConv(W x))), v =
+ * Swish(ShortConv(W_v x)); "Kimi K3 模型结构（1）", parameterisation section:
+ * ShortConv is a depthwise causal convolution of kernel 4 along the sequence,
+ * and decode keeps the last three projected inputs of q, k and v as the
+ * layer's only state besides S).  Per stream, channel and token t:
+ *
+ *   c_t = w[0] x_{t-3} + w[1] x_{t-2} + w[2] x_{t-1} + w[3] x_t
+ *   y_t = c_t * sigmoid(c_t)                                    (Swish)
+ *   q_t, k_t = y_t / sqrt(sum over the d channels of y_t^2 + eps)  (per token, head;
+ *              0 where that sum is 0);  v_t = y_t
+ *
+ * with x_{-3}, x_{-2}, x_{-1} of each sequence taken from the conv state.
+ * Layout:
+ *   xq, xk, xv  [Ttot, H, d] dtype: the projected inputs W x (16-byte aligned)
+ *   wq, wk, wv  [H, d, 4] fp32 depthwise taps, w[3] on the current token
+ *   conv        [N, 3, 3, H, d] fp32: per sequence (session) the three most
+ *               recent inputs of stream q, k, v, oldest first
+ *   q, k, v     [Ttot, H, d] dtype outputs
+ *   d = 64 or 128; eps >= 0 finite.
+ *
+ * kda_short_conv: whole sequences (fixed length T, or packed with cu_seqlens as
+ * in kda_fwd).  conv0 is the state before each sequence (NULL: zeros); conv_T
+ * (NULL to skip) receives the state after it -- its last three inputs, with
+ * conv0's tail for a sequence shorter than three -- and may alias conv0.  A
+ * sequence run in pieces, each from the previous piece's conv_T, gives the
+ * same outputs as one run.  workspace: at least kda_fwd_workspace_bytes(N)
+ * bytes (the status word; a bad device-side cu_seqlens is reported as in
+ * kda_fwd and nothing is written).
+ * kda_short_conv_step: one token per session (xq, xk, xv, q, k, v [N, H, d]);
+ * the state conv is read and moved on by one token in place.  No workspace.
+ * Errors: KDA_ERR_INVALID_ARGUMENT for bad sizes, pointers or alignment,
+ * KDA_ERR_UNSUPPORTED for other d, KDA_ERR_WORKSPACE for a short workspace.
+ */
+kda_status_t kda_short_conv(const void *xq, const void *xk, const void *xv, const float *wq,
+                            const float *wk, const float *wv, const float *conv0,
+                            const int32_t *cu_seqlens, int B, int T, int H, int d, int N,
+                            kda_dtype_t dtype, float eps, void *q, void *k, void *v,
+                            float *conv_T, void *workspace, size_t workspace_bytes,
+                            void *stream);
+kda_status_t kda_short_conv_step(const void *xq, const void *xk, const void *xv,
+                                 const float *wq, const float *wk, const float *wv, float *conv,
+                                 int N, int H, int d, kda_dtype_t dtype, float eps, void *q,
+                                 void *k, void *v, void *stream);
+
+/*
  * Speculative-decode verification and commit ("Kimi K3 深度拆解" section 9.2:
  * the draft tokens' projected inputs are kept instead of a copy of the state
  * per draft position; after verification the accepted tokens are replayed on

@@ -171,6 +171,78 @@ kda_status_t kda_gated_rmsnorm(const void *o, const void *g, const float *norm_w
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status_t kda_short_conv(const void *xq, const void *xk, const void *xv, const float *wq,
+                            const float *wk, const float *wv, const float *conv0,
+                            const int32_t *cu_seqlens, int B, int T, int H, int d, int N,
+                            kda_dtype_t dtype, float eps, void *q, void *k, void *v,
+                            float *conv_T, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (B < 0 || T < 0 || N < 0 || H <= 0 || d <= 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!(eps >= 0.f) || eps > 3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
+    if (d != 64 && d != 128) return KDA_ERR_UNSUPPORTED;
+    if (cu_seqlens) {
+        if (B != 1 || ((uintptr_t)cu_seqlens & 3u) != 0) return KDA_ERR_INVALID_ARGUMENT;
+    } else if (N != B) {
+        return KDA_ERR_INVALID_ARGUMENT;
+    }
+    const int64_t Ttot = (int64_t)B * T;
+    if ((int64_t)N * H > INT32_MAX / 9) return KDA_ERR_INVALID_ARGUMENT;
+    const void *x[3] = {xq, xk, xv};
+    const float *w[3] = {wq, wk, wv};
+    void *y[3] = {q, k, v};
+    for (int i = 0; i < 3; ++i) {
+        if (Ttot > 0 && (!x[i] || !y[i] || !aligned16(x[i]) || !aligned16(y[i])))
+            return KDA_ERR_INVALID_ARGUMENT;
+        if (!w[i] || !aligned16(w[i])) return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if ((conv0 && !aligned16(conv0)) || (conv_T && !aligned16(conv_T)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (!workspace) return KDA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return KDA_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < kda_fwd_workspace_bytes(N)) return KDA_ERR_WORKSPACE;
+    if (fault_injected()) return KDA_ERR_CUDA;
+    // the status word and the device-side check of cu_seqlens, as in kda_fwd
+    kda::FwdParams p{};
+    p.cu_seqlens = cu_seqlens;
+    p.N = N;
+    p.Ttot = Ttot;
+    p.status = static_cast<int32_t *>(workspace);
+    p.order = cu_seqlens ? reinterpret_cast<const int32_t *>(
+                               static_cast<char *>(workspace) + kda::kWsOrderOffset)
+                         : nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (kda::launch_schedule(p, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (N == 0) return KDA_OK;
+    const cudaError_t e = kda::launch_short_conv(x, w, conv0, cu_seqlens, Ttot, T, H, d, N, dtype,
+                                                 eps, y, conv_T, p.status, false, s);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_short_conv_step(const void *xq, const void *xk, const void *xv,
+                                 const float *wq, const float *wk, const float *wv, float *conv,
+                                 int N, int H, int d, kda_dtype_t dtype, float eps, void *q,
+                                 void *k, void *v, void *stream) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (N < 0 || H <= 0 || d <= 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!(eps >= 0.f) || eps > 3.0e38f) return KDA_ERR_INVALID_ARGUMENT;
+    if (d != 64 && d != 128) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)N * H > INT32_MAX / 9) return KDA_ERR_INVALID_ARGUMENT;
+    if (N == 0) return KDA_OK;
+    const void *x[3] = {xq, xk, xv};
+    const float *w[3] = {wq, wk, wv};
+    void *y[3] = {q, k, v};
+    for (int i = 0; i < 3; ++i)
+        if (!x[i] || !y[i] || !w[i] || !aligned16(x[i]) || !aligned16(y[i]) || !aligned16(w[i]))
+            return KDA_ERR_INVALID_ARGUMENT;
+    if (!conv || !aligned16(conv)) return KDA_ERR_INVALID_ARGUMENT;
+    if (fault_injected()) return KDA_ERR_CUDA;
+    const cudaError_t e = kda::launch_short_conv(x, w, nullptr, nullptr, N, 1, H, d, N, dtype, eps,
+                                                 y, conv, nullptr, true,
+                                                 static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status_t kda_fwd_gated(const void *q, const void *k, const void *v, const float *log_alpha,
                            const float *beta, const float *S0, const int32_t *cu_seqlens,
                            int B, int T, int H, int d_k, int d_v, int N, kda_dtype_t dtype,

@@ -162,6 +162,13 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v,
                           int H, int d, kda_dtype_t dt, void *o, cudaStream_t s,
                           const void *gate = nullptr, const float *norm_w = nullptr,
                           float eps = 0.f);
+// Input prologue (ShortConv(4), Swish, L2Norm of q and k) of the three streams x[0..2]
+// into y[0..2]: over whole sequences with the conv state conv0 -> conv_T (step =
+// false), or one token per session with the state conv_T updated in place (step).
+cudaError_t launch_short_conv(const void *const x[3], const float *const w[3], const float *conv0,
+                              const int32_t *cu_seqlens, int64_t Ttot, int T, int H, int d, int N,
+                              kda_dtype_t dt, float eps, void *const y[3], float *conv_T,
+                              int32_t *status, bool step, cudaStream_t s);
 // y = gated RMSNorm of o over rows of d channels (y may alias o).
 cudaError_t launch_gated_rmsnorm(const void *o, const void *gate, const float *norm_w,
                                  float eps, int64_t rows, int d, kda_dtype_t dt, void *y,

@@ -34,6 +34,7 @@ EXPORTED = ["kda_fwd_workspace_bytes", "kda_fwd", "kda_fwd_engine", "kda_fwd_noa
             "kda_fwd_cp", "kda_fwd_cp_workspace_bytes", "kda_fwd_cp_segments",
             "kda_decode_step", "kda_verify_tokens", "kda_commit_tokens",
             "kda_fwd_gated", "kda_decode_step_gated", "kda_gated_rmsnorm",
+            "kda_short_conv", "kda_short_conv_step",
             "kda_read_device_status", "kda_state_bytes", "kda_status_string"]
 KDA_NOALLOC_MAX_SEQS = 16384
 KDA_MAX_DRAFT_TOKENS = 16
@@ -96,6 +97,12 @@ def load_library(path: str) -> ctypes.CDLL:
                                           vp, vp, ci]
     lib.kda_gated_rmsnorm.restype = ci
     lib.kda_gated_rmsnorm.argtypes = [vp, vp, fp, cf, ctypes.c_int64, ci, ci, vp, vp]
+    lib.kda_short_conv.restype = ci
+    lib.kda_short_conv.argtypes = [vp, vp, vp, fp, fp, fp, fp, vp, ci, ci, ci, ci, ci, ci, cf,
+                                   vp, vp, vp, fp, vp, sz, vp]
+    lib.kda_short_conv_step.restype = ci
+    lib.kda_short_conv_step.argtypes = [vp, vp, vp, fp, fp, fp, fp, ci, ci, ci, ci, cf, vp, vp,
+                                        vp, vp]
     lib.kda_read_device_status.restype = ci
     lib.kda_read_device_status.argtypes = [vp, sz, vp]
     lib.kda_state_bytes.restype = sz
@@ -279,6 +286,91 @@ def kda_gated_rmsnorm(o, g, norm_weight=None, eps: float = 1e-6, *, y=None, stre
     if rc != KDA_OK:
         raise KdaError(rc, "kda_gated_rmsnorm")
     return y
+
+
+def _prologue_checks(xq, xk, xv, wq, wk, wv):
+    dev, dt = xq.device, xq.dtype
+    _dtype_code(dt)
+    for t, name in ((xq, "xq"), (xk, "xk"), (xv, "xv")):
+        _check(t, name, dt, dev)
+        _check_shape(t, name, xq.shape)
+    H, d = xq.shape[-2], xq.shape[-1]
+    for t, name in ((wq, "wq"), (wk, "wk"), (wv, "wv")):
+        _check(t, name, torch.float32, dev)
+        _check_shape(t, name, (H, d, 4))
+    return dev, dt, H, d
+
+
+def kda_short_conv(xq, xk, xv, wq, wk, wv, conv0=None, cu_seqlens=None, *, eps: float = 1e-6,
+                   q=None, k=None, v=None, conv_T=None, return_state: bool = True,
+                   workspace=None, stream=None, lib=None):
+    """The layer's input prologue over whole sequences: q, k =
+    L2Norm(Swish(ShortConv(xq / xk))), v = Swish(ShortConv(xv)).  x: [B, T, H, d]
+    or packed [Ttot, H, d] with cu_seqlens; w: [H, d, 4] fp32 taps (w[..., 3] on
+    the current token); conv0 / conv_T: [N, 3, 3, H, d] fp32 conv states (conv_T
+    may be conv0).  Returns (q, k, v, conv_T)."""
+    dev, dt, H, d = _prologue_checks(xq, xk, xv, wq, wk, wv)
+    _check(conv0, "conv0", torch.float32, dev)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    if cu_seqlens is not None:
+        if xq.dim() != 3 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+            raise ValueError("with cu_seqlens, x must be packed [Ttot, H, d] and cu_seqlens [N + 1]")
+        B, T, N = 1, xq.shape[0], cu_seqlens.numel() - 1
+    elif xq.dim() == 4:
+        B, T = xq.shape[0], xq.shape[1]
+        N = B
+    elif xq.dim() == 3:
+        B, T, N = 1, xq.shape[0], 1
+    else:
+        raise ValueError("x must be [B, T, H, d] or [Ttot, H, d]")
+    _check_shape(conv0, "conv0", (N, 3, 3, H, d))
+    outs = []
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        if t is None:
+            t = torch.empty(xq.shape, dtype=dt, device=dev)
+        _check(t, name, dt, dev)
+        _check_shape(t, name, xq.shape)
+        outs.append(t)
+    if conv_T is None and return_state:
+        conv_T = torch.empty((N, 3, 3, H, d), dtype=torch.float32, device=dev)
+    _check(conv_T, "conv_T", torch.float32, dev)
+    _check_shape(conv_T, "conv_T", (N, 3, 3, H, d))
+    lib = lib or load()
+    if workspace is None:
+        workspace = torch.empty(int(lib.kda_fwd_workspace_bytes(N)), dtype=torch.uint8, device=dev)
+    rc = lib.kda_short_conv(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(wq), _ptr(wk), _ptr(wv),
+                            _ptr(conv0), _ptr(cu_seqlens), B, T, H, d, N, _dtype_code(dt),
+                            float(eps), _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]),
+                            _ptr(conv_T), _ptr(workspace), workspace.numel(), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_short_conv")
+    return outs[0], outs[1], outs[2], conv_T
+
+
+def kda_short_conv_step(xq, xk, xv, wq, wk, wv, conv, *, eps: float = 1e-6, q=None, k=None,
+                        v=None, stream=None, lib=None):
+    """The prologue for one token per session: x [N, H, d]; conv [N, 3, 3, H, d]
+    fp32 is moved on by one token in place.  Returns (q, k, v)."""
+    dev, dt, H, d = _prologue_checks(xq, xk, xv, wq, wk, wv)
+    if xq.dim() != 3:
+        raise ValueError("x must be [N, H, d]")
+    N = xq.shape[0]
+    _check(conv, "conv", torch.float32, dev)
+    _check_shape(conv, "conv", (N, 3, 3, H, d))
+    outs = []
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        if t is None:
+            t = torch.empty(xq.shape, dtype=dt, device=dev)
+        _check(t, name, dt, dev)
+        _check_shape(t, name, xq.shape)
+        outs.append(t)
+    rc = (lib or load()).kda_short_conv_step(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(wq), _ptr(wk),
+                                             _ptr(wv), _ptr(conv), N, H, d, _dtype_code(dt),
+                                             float(eps), _ptr(outs[0]), _ptr(outs[1]),
+                                             _ptr(outs[2]), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_short_conv_step")
+    return outs[0], outs[1], outs[2]
 
 
 def kda_fwd_cp_workspace_bytes(N: int, H: int, d_k: int, d_v: int, segments: int) -> int:

@@ -199,6 +199,49 @@ def test_draft_token_argument_errors(kda):
     assert commit(N=0, S=None) == 0
 
 
+def test_short_conv_argument_errors(kda):
+    """The prologue entry points validate sizes, pointers, alignment, eps and
+    the workspace on the host, before any launch."""
+    lib = kda.load()
+    E_INV, E_UNS, E_WS = 1, 2, 3
+
+    def conv(**kw):
+        a = dict(x=P[0], w=P[1], c0=None, cu=None, B=1, T=64, H=2, d=64, N=1, dt=0, eps=1e-6,
+                 y=P[2], cT=P[3], ws=P[4], wsb=4096)
+        a.update(kw)
+        return lib.kda_short_conv(a["x"], a["x"], a["x"], a["w"], a["w"], a["w"], a["c0"],
+                                  a["cu"], a["B"], a["T"], a["H"], a["d"], a["N"], a["dt"],
+                                  a["eps"], a["y"], a["y"], a["y"], a["cT"], a["ws"], a["wsb"],
+                                  None)
+
+    assert conv(dt=5) == E_INV
+    assert conv(d=96) == E_UNS
+    assert conv(H=0) == E_INV
+    assert conv(N=2) == E_INV                                  # N != B without cu_seqlens
+    assert conv(cu=P[8], B=2, N=2) == E_INV                    # varlen needs B = 1
+    assert conv(eps=-1.0) == E_INV
+    assert conv(eps=float("nan")) == E_INV
+    assert conv(x=None) == E_INV
+    assert conv(x=ctypes.c_void_p(0x10008)) == E_INV           # misaligned
+    assert conv(w=None) == E_INV
+    assert conv(c0=ctypes.c_void_p(0x10004)) == E_INV
+    assert conv(ws=None) == E_WS
+    assert conv(wsb=8) == E_WS
+
+    def step(**kw):
+        a = dict(x=P[0], w=P[1], c=P[2], N=4, H=2, d=128, dt=1, eps=0.0, y=P[3])
+        a.update(kw)
+        return lib.kda_short_conv_step(a["x"], a["x"], a["x"], a["w"], a["w"], a["w"], a["c"],
+                                       a["N"], a["H"], a["d"], a["dt"], a["eps"], a["y"],
+                                       a["y"], a["y"], None)
+
+    assert step(d=32) == E_UNS
+    assert step(N=-1) == E_INV
+    assert step(c=None) == E_INV
+    assert step(y=ctypes.c_void_p(0x10002)) == E_INV
+    assert step(N=0) == 0                                      # nothing to do
+
+
 def test_failure_injection_reports_cuda_error(kda, monkeypatch):
     """The host-only injection hook turns a valid call into KDA_ERR_CUDA
     without enqueueing anything."""
