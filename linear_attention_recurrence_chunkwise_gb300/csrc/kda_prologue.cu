@@ -9,9 +9,8 @@
 //   y_t = c_t sigmoid(c_t),   q, k: y_t / sqrt(sum_d y_t^2 + eps) per (token, head).
 //
 // A memory-bound pass: one warp per (stream, head, run of 64 packed tokens),
-// lane l holding channels d/32 l .. d/32 (l + 1) - 1 of the row (one 16-, 8- or
-// 4-byte load, two rows in flight), the three previous inputs in registers as
-// the window slides,
+// lane l holding channels d/32 l .. d/32 (l + 1) - 1 of each row, the three
+// previous inputs in registers as the window slides,
 // the L2 norm's sum by a warp butterfly.  Consecutive warps take consecutive
 // heads of the same tokens, so the rows they read are neighbours in memory.
 // A run that crosses into another sequence reloads its window there; windows
@@ -26,7 +25,6 @@ namespace kda {
 namespace {
 
 constexpr int kRun = 64;    // tokens per warp
-constexpr int kGroup = 2;   // rows loaded together
 constexpr int kWarps = 8;   // warps per block
 
 struct ConvParams {
@@ -134,12 +132,35 @@ __device__ __forceinline__ int64_t seq_start(const ConvParams &p, int n) {
     return p.cu ? (int64_t)p.cu[n] : (int64_t)n * p.T;
 }
 
+template <int kBytes>
+__device__ __forceinline__ void cp_async(void *dst, const void *src) {
+    if constexpr (kBytes == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src), "n"(kBytes) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int n>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory"); }
+
+// Rows are staged in shared memory by cp.async, eight at a time and double
+// buffered: the next eight rows are in flight while the current ones are
+// computed, without holding registers (rows loaded into registers, two or four
+// at a time, kept the pass at 0.5 of the copy bandwidth: too few bytes in
+// flight per SM).  Each lane copies, and reads back, only its own piece of a
+// row, so no barrier is needed.
+constexpr int kAsyncGroup = 8;
+
 template <int D, typename T>
-__global__ void __launch_bounds__(32 * kWarps, 4) short_conv_kernel(const __grid_constant__ ConvParams p) {
+__global__ void __launch_bounds__(32 * kWarps) short_conv_kernel(const __grid_constant__ ConvParams p) {
     constexpr int kC = D / 32;
+    constexpr int kLane = kC * (int)sizeof(T);      // bytes of one row held by a lane
+    constexpr int kBuf = kAsyncGroup * 32 * kLane;  // one group of rows of one warp
+    extern __shared__ __align__(16) uint8_t stage_raw[];
     if (*p.status == KDA_ERR_INVALID_ARGUMENT) return;  // set by the schedule kernel
-    const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint8_t *stage = stage_raw + wid * 2 * kBuf + lane * kLane;  // this lane's pieces
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + wid;
     const int64_t nruns = (p.Ttot + kRun - 1) / kRun;
     const int64_t per_stream = nruns * p.H;
     if (gw >= 3 * per_stream) return;
@@ -161,7 +182,7 @@ __global__ void __launch_bounds__(32 * kWarps, 4) short_conv_kernel(const __grid
     int n = seq_of(p, t_begin);
     int64_t start = seq_start(p, n), end = seq_start(p, n + 1);
     float win[3][kC] = {};
-    auto load_window = [&](int64_t t) {  // the three inputs before token t of sequence n
+    auto load_window = [&](int64_t t) {
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
             const int64_t q = t - 3 + j;
@@ -177,39 +198,50 @@ __global__ void __launch_bounds__(32 * kWarps, 4) short_conv_kernel(const __grid
             }
         }
     };
-    load_window(t_begin);
-    // kGroup rows are loaded before any of them is used, so that each warp
-    // keeps that many loads in flight
-    for (int64_t tg = t_begin; tg < t_end; tg += kGroup) {
-        float xg[kGroup][kC] = {};
+    // rows of group g -> buffer g % 2 (each lane copies, and later reads back,
+    // only its own piece of each row)
+    auto prefetch = [&](int64_t tg, int buf) {
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
+        for (int g = 0; g < kAsyncGroup; ++g) {
             const size_t i = ((size_t)(tg + g) * p.H + h) * D + c0;
-            if (tg + g < t_end && in_bounds(p.status, i + kC - 1, n_tok)) load_lane<kC>(x, i, xg[g]);
+            if (tg + g < t_end && in_bounds(p.status, i + kC - 1, n_tok))
+                cp_async<kLane>(stage + buf * kBuf + g * 32 * kLane, x + i);
         }
-        if (tg + kGroup <= t_end && tg + kGroup <= end) {
-            // the whole group inside the current sequence: no branches, so that
-            // the rows' arithmetic and reductions interleave
-            float yg[kGroup][kC];
+        cp_commit();
+    };
+    load_window(t_begin);
+    prefetch(t_begin, 0);
+    int buf = 0;
+    for (int64_t tg = t_begin; tg < t_end; tg += kAsyncGroup, buf ^= 1) {
+        if (tg + kAsyncGroup < t_end) {
+            prefetch(tg + kAsyncGroup, buf ^ 1);
+            cp_wait<1>();
+        } else {
+            cp_wait<0>();
+        }
+        const uint8_t *rows = stage + buf * kBuf;
+        if (tg + kAsyncGroup <= t_end && tg + kAsyncGroup <= end) {
+            // the whole group inside the current sequence: no branches
+            T *yp = y + ((size_t)tg * p.H + h) * D + c0;
+            const size_t step = (size_t)p.H * D;
 #pragma unroll
-            for (int g = 0; g < kGroup; ++g) {
-                conv_row<kC, sizeof(T) == 2>(w, win, xg[g], norm, p.eps, yg[g]);
+            for (int g = 0; g < kAsyncGroup; ++g) {
+                float xt[kC], yv[kC];
+                load_lane<kC>(reinterpret_cast<const T *>(rows + g * 32 * kLane), 0, xt);
+                conv_row<kC, sizeof(T) == 2>(w, win, xt, norm, p.eps, yv);
+                if (in_bounds(p.status, ((size_t)(tg + g) * p.H + h) * D + c0 + kC - 1, n_tok))
+                    store_lane<kC>(yp + g * step, 0, yv);
 #pragma unroll
                 for (int e = 0; e < kC; ++e) {
                     win[0][e] = win[1][e];
                     win[1][e] = win[2][e];
-                    win[2][e] = xg[g][e];
+                    win[2][e] = xt[e];
                 }
-            }
-#pragma unroll
-            for (int g = 0; g < kGroup; ++g) {
-                const size_t i = ((size_t)(tg + g) * p.H + h) * D + c0;
-                if (in_bounds(p.status, i + kC - 1, n_tok)) store_lane<kC>(y, i, yg[g]);
             }
             continue;
         }
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
+        for (int g = 0; g < kAsyncGroup; ++g) {
             const int64_t t = tg + g;
             if (t >= t_end) break;
             if (t == end) {  // the run enters the next non-empty sequence
@@ -218,15 +250,16 @@ __global__ void __launch_bounds__(32 * kWarps, 4) short_conv_kernel(const __grid
                 end = seq_start(p, n + 1);
                 load_window(t);
             }
+            float xt[kC], yv[kC];
+            load_lane<kC>(reinterpret_cast<const T *>(stage + buf * kBuf + g * 32 * kLane), 0, xt);
+            conv_row<kC, sizeof(T) == 2>(w, win, xt, norm, p.eps, yv);
             const size_t i = ((size_t)t * p.H + h) * D + c0;
-            float yv[kC];
-            conv_row<kC, sizeof(T) == 2>(w, win, xg[g], norm, p.eps, yv);
             if (in_bounds(p.status, i + kC - 1, n_tok)) store_lane<kC>(y, i, yv);
 #pragma unroll
             for (int e = 0; e < kC; ++e) {
                 win[0][e] = win[1][e];
                 win[1][e] = win[2][e];
-                win[2][e] = xg[g][e];
+                win[2][e] = xt[e];
             }
         }
     }
@@ -313,8 +346,13 @@ cudaError_t launch_typed(const ConvParams &p, bool step, cudaStream_t s) {
         return cudaGetLastError();
     }
     const int64_t warps = 3 * ((p.Ttot + kRun - 1) / kRun) * p.H;
-    if (warps > 0)
-        short_conv_kernel<D, T><<<(unsigned)((warps + kWarps - 1) / kWarps), 32 * kWarps, 0, s>>>(p);
+    const int smem = kWarps * 2 * kAsyncGroup * D * (int)sizeof(T);
+    if (warps > 0) {
+        cudaError_t e0 = cudaFuncSetAttribute(short_conv_kernel<D, T>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e0 != cudaSuccess) return e0;
+        short_conv_kernel<D, T><<<(unsigned)((warps + kWarps - 1) / kWarps), 32 * kWarps, smem, s>>>(p);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !p.conv_T) return e;
     const size_t total = (size_t)p.N * 3 * p.H * D;
