@@ -670,7 +670,26 @@ def prologue_sub(kda, args, stream, pk):
                           "roofline": hbm_roof(alg, ms, pk),
                           "note": "the 28 MB conv state fits in L2, so repeated steps may "
                                   "re-read it from L2"}
-    del xd, yd, conv
+    # the whole layer step for one token: prologue, recurrence and epilogue in
+    # one kernel, against the prologue step followed by the gated decode step
+    wd = make_workload("decode", seed=args.seed, device="cuda")
+    x = wd["tokens"][0]
+    gate = (2 * torch.randn((N, H, d), generator=gen, device="cuda")).to(torch.bfloat16)
+    nw = torch.rand(d, generator=gen, device="cuda") + 0.5
+    y = torch.empty_like(gate)
+    fused = time_calls(lambda: kda.kda_decode_layer_step(
+        *xd, *ws, conv, x["log_alpha"], x["beta"], wd["S"], gate, nw, y=y, stream=stream),
+        100, stream)
+
+    def separate():
+        kda.kda_short_conv_step(*xd, *ws, conv, q=yd[0], k=yd[1], v=yd[2], stream=stream)
+        kda.kda_decode_step_gated(yd[0], yd[1], yd[2], x["log_alpha"], x["beta"], wd["S"], g=gate,
+                                  norm_weight=nw, y=y, stream=stream)
+    sep = time_calls(separate, 100, stream)
+    out["layer_step"] = {"workload": "one decode token, N=64 sessions H=96 d=128 bf16: "
+                                     "prologue, recurrence on the 403 MB state, epilogue",
+                         "fused_us": round(fused * 1e3, 2), "separate_us": round(sep * 1e3, 2)}
+    del xd, yd, conv, wd
     torch.cuda.empty_cache()
     return out
 

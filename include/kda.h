@@ -351,6 +351,27 @@ kda_status_t kda_short_conv_step(const void *xq, const void *xk, const void *xv,
                                  void *k, void *v, void *stream);
 
 /*
+ * One decode token per session through the whole KDA layer step in one kernel
+ * ("Kimi K3" (gentlecold) section 9.2: the inference kernel fuses the short
+ * convolution, the input normalisation, the recurrence and the output
+ * normalisation): the input prologue of kda_short_conv_step from the projected
+ * inputs xq, xk, xv and the conv state, then the step of kda_decode_step, then
+ * the epilogue of kda_decode_step_gated into y.  Layouts as there: xq, xk, xv,
+ * g, y [N, H, d] dtype; wq, wk, wv [H, d, 4] fp32; conv [N, 3, 3, H, d] fp32 and
+ * S [N, H, d, d] fp32, both updated in place; log_alpha [N, H, d], beta [N, H]
+ * fp32; norm_weight [d] or NULL; l2_eps the prologue's L2Norm epsilon, eps the
+ * RMSNorm's.  q, k and v stay in fp32 inside the kernel, so the result agrees
+ * with the three separate calls up to the rounding of q, k, v to the io dtype.
+ * Pointers 16-byte aligned.  No workspace.  Errors as kda_short_conv_step.
+ */
+kda_status_t kda_decode_layer_step(const void *xq, const void *xk, const void *xv,
+                                   const float *wq, const float *wk, const float *wv, float *conv,
+                                   float l2_eps, const float *log_alpha, const float *beta,
+                                   float *S, int N, int H, int d, kda_dtype_t dtype,
+                                   const void *g, const float *norm_weight, float eps, void *y,
+                                   void *stream);
+
+/*
  * Speculative-decode verification and commit ("Kimi K3 深度拆解" section 9.2:
  * the draft tokens' projected inputs are kept instead of a copy of the state
  * per draft position; after verification the accepted tokens are replayed on

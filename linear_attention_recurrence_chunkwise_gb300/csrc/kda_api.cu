@@ -243,6 +243,34 @@ kda_status_t kda_short_conv_step(const void *xq, const void *xk, const void *xv,
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status_t kda_decode_layer_step(const void *xq, const void *xk, const void *xv,
+                                   const float *wq, const float *wk, const float *wv, float *conv,
+                                   float l2_eps, const float *log_alpha, const float *beta,
+                                   float *S, int N, int H, int d, kda_dtype_t dtype,
+                                   const void *g, const float *norm_weight, float eps, void *y,
+                                   void *stream) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (N < 0 || H <= 0 || d <= 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!(eps >= 0.f) || eps > 3.0e38f || !(l2_eps >= 0.f) || l2_eps > 3.0e38f)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (d != 64 && d != 128) return KDA_ERR_UNSUPPORTED;
+    if ((int64_t)N * H > INT32_MAX / 9) return KDA_ERR_INVALID_ARGUMENT;
+    if (N == 0) return KDA_OK;
+    const void *x[3] = {xq, xk, xv};
+    const float *w[3] = {wq, wk, wv};
+    for (int i = 0; i < 3; ++i)
+        if (!x[i] || !w[i] || !aligned16(x[i]) || !aligned16(w[i])) return KDA_ERR_INVALID_ARGUMENT;
+    if (!conv || !log_alpha || !beta || !S || !g || !y || !aligned16(conv) ||
+        !aligned16(log_alpha) || !aligned(beta, 4) || !aligned16(S) || !aligned16(g) ||
+        !aligned16(y) || (norm_weight && !aligned(norm_weight, 4)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (fault_injected()) return KDA_ERR_CUDA;
+    const cudaError_t e = kda::launch_decode_layer(x, w, conv, l2_eps, log_alpha, beta, S, N, H, d,
+                                                   dtype, g, norm_weight, eps, y,
+                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status_t kda_fwd_gated(const void *q, const void *k, const void *v, const float *log_alpha,
                            const float *beta, const float *S0, const int32_t *cu_seqlens,
                            int B, int T, int H, int d_k, int d_v, int N, kda_dtype_t dtype,

@@ -113,6 +113,91 @@ __global__ void __launch_bounds__(128) decode_step_kernel(
   }
 }
 
+// The layer's input prologue computed in the step (kPro): q, k = L2Norm(Swish(
+// ShortConv(x))), v = Swish(ShortConv(x_v)) from the projected inputs x of the
+// session's token and the conv state (the three previous inputs per stream),
+// which the step then moves on by one token ("Kimi K3" (gentlecold) section 9.2:
+// the inference kernel fuses the short convolution, the input normalisation,
+// the recurrence and the output normalisation; the prologue's arithmetic is
+// the one kda_short_conv_step runs).
+struct PrologueArgs {
+    const void *x[3];  // xq, xk, xv [N][H][D]
+    const float *w[3];  // taps [H][D][4], w[3] on the current token
+    float *conv;        // [N][3][3][H][D], updated in place
+    int H;
+    float l2_eps;
+};
+
+__device__ __forceinline__ float swish(float c, bool bf16_out) {
+    return bf16_out ? c * sigmoid_bf16out(c) : __fdividef(c, 1.f + __expf(-c));
+}
+
+// four consecutive elements of an input row as floats
+__device__ __forceinline__ void load4(const float *p, size_t i, float (&f)[4]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p + i);
+    f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16 *p, size_t i, float (&f)[4]) {
+    const uint2 a = *reinterpret_cast<const uint2 *>(p + i);
+    f[0] = __uint_as_float(a.x << 16), f[1] = __uint_as_float(a.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(a.y << 16), f[3] = __uint_as_float(a.y & 0xFFFF0000u);
+}
+
+// q or k (stream s) of pair (n, h) on this lane's channels c = 32 i + 4 l8 + e.
+// The four row groups of the warp hold the same channels, so row group `sub`
+// computes slice i = sub (four channels per lane) and the lanes gather the
+// other slices by shuffles; the L2 norm's sum runs over the whole warp.
+template <int D, typename Tin>
+__device__ __forceinline__ void prologue_qk(const PrologueArgs &pro, int s, int n, int h, int sub,
+                                            int l8, float (&out)[D / 8]) {
+    constexpr int kVec = D / 32;  // slices of 32 channels
+    const size_t HD = (size_t)pro.H * D;
+    float mine[4] = {0.f, 0.f, 0.f, 0.f};
+    float ss = 0.f;
+    if (sub < kVec) {
+        const int c = 32 * sub + 4 * l8;
+        const float *st = pro.conv + ((size_t)n * 3 + s) * 3 * HD + (size_t)h * D + c;
+        const float *w = pro.w[s] + ((size_t)h * D + c) * 4;
+        float s0[4], s1[4], s2[4], xc[4];
+        load4(st, 0, s0);
+        load4(st, HD, s1);
+        load4(st, 2 * HD, s2);
+        load4(static_cast<const Tin *>(pro.x[s]), ((size_t)n * pro.H + h) * D + c, xc);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 t = *reinterpret_cast<const float4 *>(w + 4 * e);
+            float cv = t.w * xc[e];
+            cv = fmaf(t.z, s2[e], cv);
+            cv = fmaf(t.y, s1[e], cv);
+            cv = fmaf(t.x, s0[e], cv);
+            mine[e] = swish(cv, sizeof(Tin) == 2);
+            ss = fmaf(mine[e], mine[e], ss);
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    const float t = ss + pro.l2_eps;
+    const float r = t > 0.f ? rsqrtf(t) : 0.f;
+#pragma unroll
+    for (int i = 0; i < kVec; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            out[4 * i + e] = r * __shfl_sync(0xffffffffu, mine[e], 8 * i + l8);
+}
+
+// v of pair (n, h) on value channel `row`
+template <int D, typename Tin>
+__device__ __forceinline__ float prologue_v(const PrologueArgs &pro, int n, int h, int row) {
+    const size_t HD = (size_t)pro.H * D;
+    const float *st = pro.conv + ((size_t)n * 3 + 2) * 3 * HD + (size_t)h * D + row;
+    const float4 t = *reinterpret_cast<const float4 *>(pro.w[2] + ((size_t)h * D + row) * 4);
+    float cv = t.w * to_f(static_cast<const Tin *>(pro.x[2])[((size_t)n * pro.H + h) * D + row]);
+    cv = fmaf(t.z, st[2 * HD], cv);
+    cv = fmaf(t.y, st[HD], cv);
+    cv = fmaf(t.x, st[0], cv);
+    return swish(cv, sizeof(Tin) == 2);
+}
+
 // The same step with the layer's output epilogue fused: y_v = sigmoid(g_v)
 // w_v o_v / sqrt(mean(o^2) + eps) is written instead of o (head-wise RMSNorm
 // and sigmoid gate, "Kimi K3 模型结构（1）" output section).  The four warps of a
@@ -126,12 +211,12 @@ __global__ void __launch_bounds__(128) decode_step_kernel(
 // at the smallest pair index wait for a pair that every warp has passed and
 // posted, whose last poster releases it without waiting (it is bounded in
 // time all the same).
-template <int D, typename Tin>
+template <int D, typename Tin, bool kPro>
 __global__ void __launch_bounds__(128) decode_step_gated_kernel(
     const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
     const float *__restrict__ log_alpha, const float *__restrict__ beta,
     float *__restrict__ S, Tin *__restrict__ y, int NH, const Tin *__restrict__ gate,
-    const float *__restrict__ norm_w, float eps) {
+    const float *__restrict__ norm_w, float eps, const __grid_constant__ PrologueArgs pro) {
     constexpr int kLanesPerRow = 8;
     constexpr int kPerLane = D / kLanesPerRow;
     constexpr int kVec = kPerLane / 4;
@@ -163,13 +248,25 @@ __global__ void __launch_bounds__(128) decode_step_gated_kernel(
     const size_t vec = (size_t)p * D;
     float kk[kPerLane], qq[kPerLane], aa[kPerLane];
     float kq = 0.f;
+    int pn = 0, ph = 0;  // the pair's session and head (prologue)
+    if constexpr (kPro) {
+        pn = p / pro.H;
+        ph = p % pro.H;
+        prologue_qk<D, Tin>(pro, 0, pn, ph, sub, l8, qq);
+        prologue_qk<D, Tin>(pro, 1, pn, ph, sub, l8, kk);
+    }
+    // v of the warp's rows (D / 4 of them), one per lane, handed out by shuffles
+    const float vlane = kPro && lane < kRowsPerWarp
+                            ? prologue_v<D, Tin>(pro, pn, ph, warp * kRowsPerWarp + lane) : 0.f;
 #pragma unroll
     for (int i4 = 0; i4 < kVec; ++i4)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int c = 32 * i4 + 4 * l8 + e;
-            kk[4 * i4 + e] = to_f(k[vec + c]);
-            qq[4 * i4 + e] = to_f(q[vec + c]);
+            if constexpr (!kPro) {
+                kk[4 * i4 + e] = to_f(k[vec + c]);
+                qq[4 * i4 + e] = to_f(q[vec + c]);
+            }
             aa[4 * i4 + e] = expf(log_alpha[vec + c]);
             kq = fmaf(kk[4 * i4 + e], qq[4 * i4 + e], kq);
         }
@@ -207,7 +304,9 @@ __global__ void __launch_bounds__(128) decode_step_gated_kernel(
             rk += __shfl_xor_sync(0xffffffffu, rk, m);
             rq += __shfl_xor_sync(0xffffffffu, rq, m);
         }
-        const float u = b * (to_f(v[vec + row]) - rk);
+        const float vr = kPro ? __shfl_sync(0xffffffffu, vlane, row - warp * kRowsPerWarp)
+                              : to_f(v[vec + row]);
+        const float u = b * (vr - rk);
 #pragma unroll
         for (int i4 = 0; i4 < kVec; ++i4) {
             s[i4].x = fmaf(u, kk[4 * i4 + 0], s[i4].x);
@@ -241,6 +340,25 @@ __global__ void __launch_bounds__(128) decode_step_gated_kernel(
             const float sg = sizeof(Tin) == 4 ? sigmoid_f32(gv) : sigmoid_bf16out(gv);
             y[vec + t] = from_f<Tin>(o_row[bf][t] * rs * (norm_w ? norm_w[t] : 1.f) * sg);
         }
+        if constexpr (kPro) {
+            // every warp has read the pair's conv state: move it on by one
+            // token, (x_{t-2}, x_{t-1}, x_t) per stream
+            const size_t HD = (size_t)pro.H * D;
+#pragma unroll
+            for (int s3 = 0; s3 < 3; ++s3) {
+                const int c = 4 * lane;
+                if (c < D) {
+                    float *st = pro.conv + ((size_t)pn * 3 + s3) * 3 * HD + (size_t)ph * D + c;
+                    const float4 a1 = *reinterpret_cast<const float4 *>(st + HD);
+                    const float4 a2 = *reinterpret_cast<const float4 *>(st + 2 * HD);
+                    float xc[4];
+                    load4(static_cast<const Tin *>(pro.x[s3]), ((size_t)pn * pro.H + ph) * D + c, xc);
+                    *reinterpret_cast<float4 *>(st) = a1;
+                    *reinterpret_cast<float4 *>(st + HD) = a2;
+                    *reinterpret_cast<float4 *>(st + 2 * HD) = make_float4(xc[0], xc[1], xc[2], xc[3]);
+                }
+            }
+        }
         __syncwarp();  // all lanes have read the buffer
         if (lane == 0) {
             __threadfence_block();
@@ -250,10 +368,11 @@ __global__ void __launch_bounds__(128) decode_step_gated_kernel(
   }
 }
 
-template <int D, typename Tin, bool kGated>
+template <int D, typename Tin, bool kGated, bool kPro = false>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const float *la,
                          const float *beta, float *S, int NH, void *o, cudaStream_t s,
-                         const void *gate, const float *norm_w, float eps) {
+                         const void *gate, const float *norm_w, float eps,
+                         const PrologueArgs &pro = PrologueArgs{}) {
     // resident blocks on the whole GPU, looked up once per device (threads that
     // race here all compute and store the same value)
     constexpr int kMaxDevices = 64;
@@ -268,7 +387,7 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
             e = kGated ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                             &per, decode_step_gated_kernel<D, Tin>, 128, 0)
+                             &per, decode_step_gated_kernel<D, Tin, kPro>, 128, 0)
                        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                              &per, decode_step_kernel<D, Tin>, 128, 0);
         if (e != cudaSuccess) return e;
@@ -277,10 +396,10 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
     }
     const int grid = NH < res ? NH : res;
     if constexpr (kGated)
-        decode_step_gated_kernel<D, Tin><<<grid, 128, 0, s>>>(
+        decode_step_gated_kernel<D, Tin, kPro><<<grid, 128, 0, s>>>(
             static_cast<const Tin *>(q), static_cast<const Tin *>(k),
                                   static_cast<const Tin *>(v), la, beta, S, static_cast<Tin *>(o),
-                                  NH, static_cast<const Tin *>(gate), norm_w, eps);
+                                  NH, static_cast<const Tin *>(gate), norm_w, eps, pro);
     else
         decode_step_kernel<D, Tin><<<grid, 128, 0, s>>>(
             static_cast<const Tin *>(q), static_cast<const Tin *>(k),
@@ -289,6 +408,33 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
 }
 
 }  // namespace
+
+cudaError_t launch_decode_layer(const void *const x[3], const float *const w[3], float *conv,
+                                float l2_eps, const float *log_alpha, const float *beta,
+                                float *S, int N, int H, int d, kda_dtype_t dt, const void *gate,
+                                const float *norm_w, float eps, void *y, cudaStream_t s) {
+    const int NH = N * H;
+    if (NH == 0) return cudaSuccess;
+    PrologueArgs pro{};
+    for (int i = 0; i < 3; ++i) {
+        pro.x[i] = x[i];
+        pro.w[i] = w[i];
+    }
+    pro.conv = conv;
+    pro.H = H;
+    pro.l2_eps = l2_eps;
+    if (d == 128)
+        return dt == KDA_BF16
+                   ? launch_typed<128, __nv_bfloat16, true, true>(nullptr, nullptr, nullptr, log_alpha,
+                                                                  beta, S, NH, y, s, gate, norm_w, eps, pro)
+                   : launch_typed<128, float, true, true>(nullptr, nullptr, nullptr, log_alpha, beta,
+                                                          S, NH, y, s, gate, norm_w, eps, pro);
+    return dt == KDA_BF16
+               ? launch_typed<64, __nv_bfloat16, true, true>(nullptr, nullptr, nullptr, log_alpha, beta,
+                                                             S, NH, y, s, gate, norm_w, eps, pro)
+               : launch_typed<64, float, true, true>(nullptr, nullptr, nullptr, log_alpha, beta, S,
+                                                     NH, y, s, gate, norm_w, eps, pro);
+}
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v,
                           const float *log_alpha, const float *beta, float *S, int N,

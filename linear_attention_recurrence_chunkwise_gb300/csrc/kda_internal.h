@@ -169,6 +169,13 @@ cudaError_t launch_short_conv(const void *const x[3], const float *const w[3], c
                               const int32_t *cu_seqlens, int64_t Ttot, int T, int H, int d, int N,
                               kda_dtype_t dt, float eps, void *const y[3], float *conv_T,
                               int32_t *status, bool step, cudaStream_t s);
+// One token per session through the whole layer step: the input prologue from the
+// projected inputs x[0..2] and the conv state (moved on in place), the decode step
+// (S in place) and the output epilogue into y.
+cudaError_t launch_decode_layer(const void *const x[3], const float *const w[3], float *conv,
+                                float l2_eps, const float *log_alpha, const float *beta,
+                                float *S, int N, int H, int d, kda_dtype_t dt, const void *gate,
+                                const float *norm_w, float eps, void *y, cudaStream_t s);
 // y = gated RMSNorm of o over rows of d channels (y may alias o).
 cudaError_t launch_gated_rmsnorm(const void *o, const void *gate, const float *norm_w,
                                  float eps, int64_t rows, int d, kda_dtype_t dt, void *y,

@@ -34,7 +34,7 @@ EXPORTED = ["kda_fwd_workspace_bytes", "kda_fwd", "kda_fwd_engine", "kda_fwd_noa
             "kda_fwd_cp", "kda_fwd_cp_workspace_bytes", "kda_fwd_cp_segments",
             "kda_decode_step", "kda_verify_tokens", "kda_commit_tokens",
             "kda_fwd_gated", "kda_decode_step_gated", "kda_gated_rmsnorm",
-            "kda_short_conv", "kda_short_conv_step",
+            "kda_short_conv", "kda_short_conv_step", "kda_decode_layer_step",
             "kda_read_device_status", "kda_state_bytes", "kda_status_string"]
 KDA_NOALLOC_MAX_SEQS = 16384
 KDA_MAX_DRAFT_TOKENS = 16
@@ -103,6 +103,9 @@ def load_library(path: str) -> ctypes.CDLL:
     lib.kda_short_conv_step.restype = ci
     lib.kda_short_conv_step.argtypes = [vp, vp, vp, fp, fp, fp, fp, ci, ci, ci, ci, cf, vp, vp,
                                         vp, vp]
+    lib.kda_decode_layer_step.restype = ci
+    lib.kda_decode_layer_step.argtypes = [vp, vp, vp, fp, fp, fp, fp, cf, fp, fp, fp, ci, ci, ci,
+                                          ci, vp, fp, cf, vp, vp]
     lib.kda_read_device_status.restype = ci
     lib.kda_read_device_status.argtypes = [vp, sz, vp]
     lib.kda_state_bytes.restype = sz
@@ -371,6 +374,41 @@ def kda_short_conv_step(xq, xk, xv, wq, wk, wv, conv, *, eps: float = 1e-6, q=No
     if rc != KDA_OK:
         raise KdaError(rc, "kda_short_conv_step")
     return outs[0], outs[1], outs[2]
+
+
+def kda_decode_layer_step(xq, xk, xv, wq, wk, wv, conv, log_alpha, beta, S, g,
+                          norm_weight=None, eps: float = 1e-6, l2_eps: float = 1e-6, *, y=None,
+                          stream=None, lib=None):
+    """One decode token per session through the layer step in one kernel:
+    prologue (conv state moved on in place), recurrence (S in place) and output
+    epilogue.  x, g: [N, H, d]; conv [N, 3, 3, H, d]; S [N, H, d, d].  Returns y."""
+    dev, dt, H, d = _prologue_checks(xq, xk, xv, wq, wk, wv)
+    if xq.dim() != 3:
+        raise ValueError("x must be [N, H, d]")
+    N = xq.shape[0]
+    _check(conv, "conv", torch.float32, dev)
+    _check_shape(conv, "conv", (N, 3, 3, H, d))
+    _check(log_alpha, "log_alpha", torch.float32, dev)
+    _check_shape(log_alpha, "log_alpha", (N, H, d))
+    _check(beta, "beta", torch.float32, dev)
+    _check_shape(beta, "beta", (N, H))
+    _check(S, "S", torch.float32, dev)
+    _check_shape(S, "S", (N, H, d, d))
+    _check(g, "g", dt, dev)
+    _check_shape(g, "g", (N, H, d))
+    _check(norm_weight, "norm_weight", torch.float32, dev)
+    _check_shape(norm_weight, "norm_weight", (d,))
+    if y is None:
+        y = torch.empty((N, H, d), dtype=dt, device=dev)
+    _check(y, "y", dt, dev)
+    _check_shape(y, "y", (N, H, d))
+    rc = (lib or load()).kda_decode_layer_step(
+        _ptr(xq), _ptr(xk), _ptr(xv), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(conv), float(l2_eps),
+        _ptr(log_alpha), _ptr(beta), _ptr(S), N, H, d, _dtype_code(dt), _ptr(g),
+        _ptr(norm_weight), float(eps), _ptr(y), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_layer_step")
+    return y
 
 
 def kda_fwd_cp_workspace_bytes(N: int, H: int, d_k: int, d_v: int, segments: int) -> int:

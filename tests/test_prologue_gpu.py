@@ -2,7 +2,8 @@
 against the fp64 oracle: whole sequences (fixed length and packed, with and
 without an initial conv state, the final state written over the initial one),
 decode steps chained through the state, pieces chained through the state, the
-full prefill shape on every head, and the bounds-checked build.
+full prefill shape on every head, the bounds-checked build, and the decode
+layer step that fuses the prologue, the recurrence and the output epilogue.
 Tolerances (max-abs error / max |oracle|): fp32 1e-5, bf16 outputs 1e-2 (one
 bf16 rounding of the result); conv states are copies of inputs and compare
 exactly."""
@@ -161,3 +162,41 @@ def test_short_conv_bounds_checked_build(kda):
     torch.cuda.synchronize()
     ref = oracle.prologue(*[t[:, None] for t in tok], *ws, got[3], eps=1e-6)
     check((q[:, None], k[:, None], v[:, None], state), ref, "f32")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_layer_step(kda, dtype, d):
+    """Three decode tokens through kda_decode_layer_step (prologue, recurrence
+    and epilogue in one kernel) against the oracle's prologue -> decode step ->
+    gated RMSNorm, and against the three separate calls; the conv state is the
+    same copy of the inputs on every path."""
+    N, H = 6, 3
+    g = torch.Generator(device="cpu").manual_seed(d + (dtype == "bf16"))
+    r = lambda *s, sc=1.0: (sc * torch.randn(s, generator=g)).to(DEV)
+    ws = [r(H, d, 4, sc=0.5) for _ in range(3)]
+    nw = (torch.rand(d, generator=g) + 0.5).to(DEV)
+    conv0, S0 = r(N, 3, 3, H, d), r(N, H, d, d, sc=0.02)
+    conv_f, S_f = conv0.clone(), S0.clone()
+    conv_s, S_s = conv0.clone(), S0.clone()
+    conv_o, S_o = conv0.double().cpu().numpy(), S0.double().cpu().numpy()
+    tol_y = 1e-4 if dtype == "f32" else 2e-2
+    for step in range(3):
+        xs = [r(N, H, d).to(DT[dtype]) for _ in range(3)]
+        la = -torch.rand((N, H, d), generator=g).to(DEV) * 0.1
+        beta = torch.sigmoid(r(N, H))
+        gate = r(N, H, d, sc=2.0).to(DT[dtype])
+        y_f = kda.kda_decode_layer_step(*xs, *ws, conv_f, la, beta, S_f, gate, nw, eps=1e-5,
+                                        l2_eps=1e-6)
+        q, k, v = kda.kda_short_conv_step(*xs, *ws, conv_s, eps=1e-6)
+        y_s = kda.kda_decode_step_gated(q, k, v, la, beta, S_s, g=gate, norm_weight=nw,
+                                        eps=1e-5)
+        torch.cuda.synchronize()
+        qo, ko, vo, conv_o = oracle.prologue(*[x[:, None] for x in xs], *ws, conv_o, eps=1e-6)
+        o_o, S_o = oracle.decode_step(qo[:, 0], ko[:, 0], vo[:, 0], la, beta, S_o)
+        y_o = oracle.gated_rmsnorm(o_o, gate, nw, eps=1e-5)
+        assert rel_err(y_f, y_o) < tol_y, step
+        assert rel_err(y_f, y_s.double().cpu().numpy()) < tol_y, step
+        assert np.array_equal(conv_f.double().cpu().numpy(), conv_o)
+        assert torch.equal(conv_f, conv_s)
+    assert rel_err(S_f, S_o) < (1e-4 if dtype == "f32" else 1e-2)
