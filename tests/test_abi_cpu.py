@@ -242,6 +242,34 @@ def test_short_conv_argument_errors(kda):
     assert step(N=0) == 0                                      # nothing to do
 
 
+def test_decode_layer_step_argument_errors(kda):
+    """kda_decode_layer_step validates sizes, eps, pointers and alignment on the
+    host, before any launch."""
+    lib = kda.load()
+    E_INV, E_UNS = 1, 2
+
+    def call(**kw):
+        a = dict(x=P[0], w=P[1], conv=P[2], l2=1e-6, la=P[3], b=P[4], S=P[5], N=2, H=2, d=128,
+                 dt=1, g=P[6], nw=None, eps=1e-6, y=P[7])
+        a.update(kw)
+        return lib.kda_decode_layer_step(a["x"], a["x"], a["x"], a["w"], a["w"], a["w"],
+                                         a["conv"], a["l2"], a["la"], a["b"], a["S"], a["N"],
+                                         a["H"], a["d"], a["dt"], a["g"], a["nw"], a["eps"],
+                                         a["y"], None)
+
+    assert call(d=32) == E_UNS
+    assert call(dt=3) == E_INV
+    assert call(N=-1) == E_INV
+    assert call(H=0) == E_INV
+    assert call(l2=-1.0) == E_INV
+    assert call(eps=float("inf")) == E_INV
+    assert call(conv=None) == E_INV
+    assert call(g=None) == E_INV
+    assert call(S=ctypes.c_void_p(0x10008)) == E_INV          # misaligned
+    assert call(b=ctypes.c_void_p(0x10002)) == E_INV          # beta: 4-byte aligned
+    assert call(N=0) == 0                                      # nothing to do
+
+
 def test_failure_injection_reports_cuda_error(kda, monkeypatch):
     """The host-only injection hook turns a valid call into KDA_ERR_CUDA
     without enqueueing anything."""
