@@ -380,13 +380,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
         const int64_t t0 = start + (int64_t)n * C;
         const int valid = min(C, len - n * C);
         // ---------------------------------------------- a1, a2: gates and operands
-        // from the staged rows: thread c < 64 takes channel c of k, q and the
-        // gates, thread 64 + v channel v of V and beta of token v
-        if (tid < D) {
-            const int c = tid;
+        // from the staged rows: thread (half, c) takes channel c of tokens
+        // 32 half .. 32 half + 31 -- its k, q, v and gates; the second half
+        // first sums the first half's log-decays for its starting G -- and
+        // thread t < 64 the beta of token t
+        {
+            const int c = tid & (D - 1), half = tid >> 6;
+            const int t_begin = 32 * half;
             float G = 0.f;
+            if (half) {
+#pragma unroll 8
+                for (int t = 0; t < 32; ++t) G += t < valid ? raw_la[t * D + c] : 0.f;
+            }
 #pragma unroll 4
-            for (int t = 0; t < C; ++t) {
+            for (int t = t_begin; t < t_begin + 32; ++t) {
                 const bool live = t < valid;
                 G += live ? raw_la[t * D + c] : 0.f;
                 const float kf = live ? ld(raw_k, t * D + c) : 0.f;
@@ -397,17 +404,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
                 put(sm.xq, 16384, 64 + t, c, qf * gf);
                 put(sm.kb, 8192, t, c, kf * gi);
                 put(sm.kv, 16384, t, c, kh);
+                put(sm.kv + 8192, 16384, t, c, live && !vzero ? ld(raw_v, t * D + c) : 0.f);
                 if (t == C - 1) sm.gam[c] = gf;
             }
-            if (!(G >= -kLogDecayLimit)) *reinterpret_cast<volatile int *>(&sm.domain) = 1;
-        } else {
-            const int vv = tid - D;
-#pragma unroll 4
-            for (int t = 0; t < C; ++t) {
-                const bool live = t < valid && !vzero;
-                put(sm.kv + 8192, 16384, t, vv, live ? ld(raw_v, t * D + vv) : 0.f);
-            }
-            sm.bet[vv] = vv < valid ? sm.rbet[vv] : 0.f;
+            if (half && !(G >= -kLogDecayLimit)) *reinterpret_cast<volatile int *>(&sm.domain) = 1;
+            if (tid < C) sm.bet[tid] = tid < valid ? sm.rbet[tid] : 0.f;
         }
         publish_smem();
         if (*reinterpret_cast<volatile int *>(&sm.domain)) break;  // (read by all after the barrier)
