@@ -221,23 +221,53 @@ __global__ void __launch_bounds__(32 * kWarps) short_conv_kernel(const __grid_co
         }
         const uint8_t *rows = stage + buf * kBuf;
         if (tg + kAsyncGroup <= t_end && tg + kAsyncGroup <= end) {
-            // the whole group inside the current sequence: no branches
+            // the whole group inside the current sequence: no branches; the
+            // L2 norms of its eight tokens from one reduce-scatter of their
+            // partial sums (lane l ends with token (l >> 2) & 7's total) and
+            // eight shuffles back, in place of a butterfly per token
             T *yp = y + ((size_t)tg * p.H + h) * D + c0;
             const size_t step = (size_t)p.H * D;
+            float yg[kAsyncGroup][kC], ss[kAsyncGroup];
 #pragma unroll
             for (int g = 0; g < kAsyncGroup; ++g) {
-                float xt[kC], yv[kC];
+                float xt[kC];
                 load_lane<kC>(reinterpret_cast<const T *>(rows + g * 32 * kLane), 0, xt);
-                conv_row<kC, sizeof(T) == 2>(w, win, xt, norm, p.eps, yv);
-                if (in_bounds(p.status, ((size_t)(tg + g) * p.H + h) * D + c0 + kC - 1, n_tok))
-                    store_lane<kC>(yp + g * step, 0, yv);
+                conv_row<kC, sizeof(T) == 2>(w, win, xt, false, 0.f, yg[g]);
+                ss[g] = 0.f;
 #pragma unroll
                 for (int e = 0; e < kC; ++e) {
+                    ss[g] = fmaf(yg[g][e], yg[g][e], ss[g]);
                     win[0][e] = win[1][e];
                     win[1][e] = win[2][e];
                     win[2][e] = xt[e];
                 }
             }
+            if (norm) {
+#pragma unroll
+                for (int len = 4; len >= 1; len >>= 1) {  // lane bits 4, 3, 2 halve the set
+                    const bool up = lane & (4 * len);
+#pragma unroll
+                    for (int i = 0; i < len; ++i) {
+                        const float keep = up ? ss[i + len] : ss[i];
+                        const float send = up ? ss[i] : ss[i + len];
+                        ss[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4 * len);
+                    }
+                }
+                ss[0] += __shfl_xor_sync(0xffffffffu, ss[0], 2);
+                ss[0] += __shfl_xor_sync(0xffffffffu, ss[0], 1);
+                const float t = ss[0] + p.eps;
+                const float r = t > 0.f ? rsqrtf(t) : 0.f;
+#pragma unroll
+                for (int g = 0; g < kAsyncGroup; ++g) {
+                    const float rg = __shfl_sync(0xffffffffu, r, 4 * g);
+#pragma unroll
+                    for (int e = 0; e < kC; ++e) yg[g][e] *= rg;
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < kAsyncGroup; ++g)
+                if (in_bounds(p.status, ((size_t)(tg + g) * p.H + h) * D + c0 + kC - 1, n_tok))
+                    store_lane<kC>(yp + g * step, 0, yg[g]);
             continue;
         }
 #pragma unroll
