@@ -394,7 +394,10 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const floa
         res = sms * (per > 0 ? per : 1);
         resident[dev].store(res, std::memory_order_relaxed);
     }
-    const int grid = NH < res ? NH : res;
+    // as many pairs per block as the resident blocks need, spread evenly:
+    // k = ceil(NH / res) pairs per block on ceil(NH / k) blocks
+    const int per_block = (NH + res - 1) / res;
+    const int grid = (NH + per_block - 1) / per_block;
     if constexpr (kGated)
         decode_step_gated_kernel<D, Tin, kPro><<<grid, 128, 0, s>>>(
             static_cast<const Tin *>(q), static_cast<const Tin *>(k),
