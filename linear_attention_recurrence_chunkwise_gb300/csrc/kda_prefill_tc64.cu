@@ -25,11 +25,19 @@
 // results land in lanes 64-127, and lanes 0-63 of those operands stay zero.
 // So warps 0-1 (tensor-memory lanes 0-63) read out A and W^T, warps 2-3
 // (lanes 64-127) M, U^T, O^T and the state.  One CTA of 128 threads per
-// (sequence, head) walks the chunks one at a time; one thread issues the MMAs.
+// (sequence, head) walks the chunks one at a time; one thread issues the MMAs
+// and the TMA copies of the next chunk's rows (issued as soon as the current
+// chunk's rows have been read, landing while the chunk computes).  The
+// operand phase gives each thread two channels of 16 tokens (bf16 pairs
+// packed two values per instruction, 32-bit stores); the solve inverts the
+// four 16 x 16 diagonal blocks of I + A by substitution, then assembles the
+// two 32 x 32 halves and their lower-left block by fp32 block products over
+// all four warps.
 // A (sequence, head) with a chunk whose cumulative log-decay leaves [-80, 0]
 // (exp(-G) past fp32 range) is recomputed token by token from S0 instead.
 // Every mbarrier wait is bounded; a timeout records KDA_ERR_TIMEOUT.
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include "kda_internal.h"
@@ -51,7 +59,8 @@ constexpr uint32_t kColO = 128;   // O^T in lanes 64-127                  (64 fp
 constexpr uint32_t kColS = 192;   // S^T master in lanes 64-127           (64 fp32)
 constexpr uint32_t kColSb = 256;  // S^T bf16 pairs: hi 32 columns, lo 32 (A operand)
 constexpr uint32_t kColUb = 320;  // U^T bf16 pairs: hi 32 columns, lo 32 (A operand)
-constexpr int LDA = C + 1;        // fp32 row stride of the solve matrix
+constexpr int LDA = C + 4;        // fp32 row stride of A (rows start on 16 bytes)
+constexpr int LDT = 36;           // fp32 row stride of the solve's 32 x 32 blocks
 
 struct __align__(1024) Tc64Smem {
     uint8_t xq[32768];  // [Kh; Qh] K-major, 128 rows x 64 channels: hi tile | lo tile
@@ -59,22 +68,24 @@ struct __align__(1024) Tc64Smem {
     uint8_t kv[32768];  // [Kh | V] MN-major A of [W^T; U~^T]: per part (hi | lo) the
                         // key block [j][c] then the value block [j][v] (8 KB each)
     uint8_t tp[16384];  // T' [r][j] K-major: hi | lo
-    uint8_t wn[16384];  // -W as [c][r] (MN-major B of U): hi | lo
+    uint8_t wn[16384];  // -W as [c][r] (MN-major B of U): hi | lo; during the solve,
+                        // its 32 x 32 blocks T1, T2 and P (fp32, rows of LDT)
     uint8_t mm[16384];  // M [r][j] K-major: hi | lo
-    uint8_t raw[4 * C * 256];  // the next chunk's rows as they are in memory (cp.async):
+    uint8_t raw[4 * C * 256];  // the next chunk's rows as they are in memory (TMA):
                                // log_alpha, k, q, v, 64 rows each of 64 elements
     float a[C * LDA];   // beta-scaled A (fp32); staging of the token-by-token pass
+    float gpart[4][D];  // log2-decay sums of each quarter of the chunk's tokens
     float gam[D];
     float bet[C];
-    float rbet[C];      // the next chunk's beta
-    uint64_t bar_mma, bar_fin;
+    float rbet[C];      // the next chunk's beta (cp.async)
+    uint64_t bar_mma, bar_fin, bar_ld;
     uint32_t tmem_base;
     int abort;
     int domain;
 };
 
 // Wait for a phase within the time limit, whatever the abort flag says (the
-// teardown's wait for the last MMAs).
+// teardown's waits for the last MMAs and the last row copy).
 __device__ __forceinline__ void wait_bounded(uint64_t &bar, uint32_t parity) {
     if (mbar_try_wait(smem_u32(&bar), parity)) return;
     const uint64_t t0 = globaltimer_ns();
@@ -82,12 +93,8 @@ __device__ __forceinline__ void wait_bounded(uint64_t &bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > kWaitLimitNs) return;
 }
 
-// Global -> shared copies that complete asynchronously (cp.async; waited for
-// with cp_async_wait_all before a barrier).
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-                 : "memory");
-}
+// Global -> shared copy of 4 bytes that completes asynchronously (cp.async;
+// waited for with cp_async_wait_all before a barrier).
 __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
                  : "memory");
@@ -99,17 +106,32 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // byte offset of element (row, col) of a 64-column tile part (128-byte rows)
 __device__ __forceinline__ uint32_t at(int row, int col) { return sw128_offset(row, col); }
 
-__device__ __forceinline__ void split(float x, __nv_bfloat16 &hi, __nv_bfloat16 &lo) {
-    hi = __float2bfloat16_rn(x);
-    lo = __float2bfloat16_rn(x - __bfloat162float(hi));  // x - hi is exact in fp32
+// x0, x1 -> hi = their bf16 values as a pair (x0 in the low half) and lo =
+// the bf16 pair of what is left (x - hi is exact in fp32), both rounded to
+// nearest: one conversion instruction per pair
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    hi = pack_bf16(x0, x1);
+    lo = pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xFFFF0000u));
 }
 
-// element (row, col) of a hi / lo tile pair whose lo part starts `part` bytes on
-__device__ __forceinline__ void put(uint8_t *tile, uint32_t part, int row, int col, float x) {
-    __nv_bfloat16 hi, lo;
-    split(x, hi, lo);
-    *reinterpret_cast<__nv_bfloat16 *>(tile + at(row, col)) = hi;
-    *reinterpret_cast<__nv_bfloat16 *>(tile + part + at(row, col)) = lo;
+// columns col, col + 1 (col even) of one row of a tile pair whose lo part
+// starts `part` bytes on
+__device__ __forceinline__ void put2(uint8_t *tile, uint32_t part, int row, int col, float x0,
+                                     float x1) {
+    uint32_t h, l;
+    split2(x0, x1, h, l);
+    *reinterpret_cast<uint32_t *>(tile + at(row, col)) = h;
+    *reinterpret_cast<uint32_t *>(tile + part + at(row, col)) = l;
+}
+
+// columns col .. col + 3 (col a multiple of 4) of one row of a tile pair
+__device__ __forceinline__ void put4(uint8_t *tile, uint32_t part, int row, int col,
+                                     const float4 &x) {
+    uint32_t h0, l0, h1, l1;
+    split2(x.x, x.y, h0, l0);
+    split2(x.z, x.w, h1, l1);
+    *reinterpret_cast<uint2 *>(tile + at(row, col)) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2 *>(tile + part + at(row, col)) = make_uint2(l0, l1);
 }
 
 // columns col .. col + 7 (col a multiple of 8) of one row of a tile pair
@@ -117,13 +139,7 @@ __device__ __forceinline__ void put8(uint8_t *tile, uint32_t part, int row, int 
                                      const float *x) {
     uint32_t h[4], l[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __nv_bfloat16 h0, l0, h1, l1;
-        split(x[2 * i], h0, l0);
-        split(x[2 * i + 1], h1, l1);
-        h[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        l[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-    }
+    for (int i = 0; i < 4; ++i) split2(x[2 * i], x[2 * i + 1], h[i], l[i]);
     *reinterpret_cast<uint4 *>(tile + at(row, col)) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4 *>(tile + part + at(row, col)) = make_uint4(l[0], l[1], l[2], l[3]);
 }
@@ -133,13 +149,17 @@ __device__ __forceinline__ void put8(uint8_t *tile, uint32_t part, int row, int 
 __device__ __forceinline__ void split_pairs(const uint32_t (&x)[32], uint32_t (&h)[16],
                                             uint32_t (&l)[16]) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        __nv_bfloat16 h0, l0, h1, l1;
-        split(__uint_as_float(x[2 * i]), h0, l0);
-        split(__uint_as_float(x[2 * i + 1]), h1, l1);
-        h[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        l[i] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-    }
+    for (int i = 0; i < 16; ++i)
+        split2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]), h[i], l[i]);
+}
+
+// acc (4 columns) += x * the row y of a 32 x 32 block
+__device__ __forceinline__ void axpy4(float4 &acc, float x, const float *y) {
+    const float4 b = *reinterpret_cast<const float4 *>(y);
+    acc.x = fmaf(x, b.x, acc.x);
+    acc.y = fmaf(x, b.y, acc.y);
+    acc.z = fmaf(x, b.z, acc.z);
+    acc.w = fmaf(x, b.w, acc.w);
 }
 
 // The three-term product over K = 64: for each K slice g of 16, hi.hi, hi.lo,
@@ -249,7 +269,12 @@ __device__ void serial_pass(const FwdParams &p, Tc64Smem &sm, int64_t start, int
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc64_kernel(const __grid_constant__ FwdParams p,
+                        const __grid_constant__ CUtensorMap tm_la,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Tc64Smem &sm = *reinterpret_cast<Tc64Smem *>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -272,9 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
                     sref.S_T[sref.off + i] = state_init(sref, i / D, i % D, D);
         return;
     }
-    const T *q = static_cast<const T *>(p.q);
-    const T *k = static_cast<const T *>(p.k);
-    const T *v = static_cast<const T *>(p.v);
     T *o = static_cast<T *>(p.o);
 
     volatile int *abort = &sm.abort;
@@ -283,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
         sm.domain = 0;
         mbar_init(smem_u32(&sm.bar_mma), 1);
         mbar_init(smem_u32(&sm.bar_fin), 1);
+        mbar_init(smem_u32(&sm.bar_ld), 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -342,37 +365,41 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
     const uint32_t id_mk = idesc_bf16(128, 64, true, false);   // MN-major A
     const uint32_t id_km = idesc_bf16(128, 64, false, true);   // MN-major B
 
-    // chunk m's rows of log_alpha, k, q, v and its beta -> sm.raw / sm.rbet (all
-    // threads, 16-byte copies; rows past the sequence end are not copied)
-    constexpr int kRow = D * (int)sizeof(T);  // bytes of one k / q / v row
-    float *raw_la = reinterpret_cast<float *>(sm.raw);
+    // chunk m's rows of log_alpha, k, q, v -> sm.raw by TMA (thread 0; tiles of
+    // 64 tokens x one head x 64 channels, zero past the last token; rows past
+    // the sequence's end belong to the next one and are masked when read) and
+    // its beta -> sm.rbet (cp.async, threads t < rows of the chunk)
+    const float *raw_la = reinterpret_cast<const float *>(sm.raw);
     const T *raw_k = reinterpret_cast<const T *>(sm.raw + C * 256);
     const T *raw_q = reinterpret_cast<const T *>(sm.raw + 2 * C * 256);
     const T *raw_v = reinterpret_cast<const T *>(sm.raw + 3 * C * 256);
-    auto prefetch = [&](int m) {
+    constexpr uint32_t kTile = C * D * sizeof(T);
+    int ld_issued = 0;  // row copies issued by thread 0 (one bar_ld phase each)
+    auto issue_rows = [&](int m) {
+        const int tm = (int)(start + (int64_t)m * C);
+        const uint32_t bar = smem_u32(&sm.bar_ld);
+        mbar_arrive_expect_tx(bar, C * D * 4 + (vzero ? 2 : 3) * kTile);
+        tma_load_3d(smem_u32(sm.raw), &tm_la, bar, 0, h, tm);
+        tma_load_3d(smem_u32(sm.raw + C * 256), &tm_k, bar, 0, h, tm);
+        tma_load_3d(smem_u32(sm.raw + 2 * C * 256), &tm_q, bar, 0, h, tm);
+        if (!vzero) tma_load_3d(smem_u32(sm.raw + 3 * C * 256), &tm_v, bar, 0, h, tm);
+        ++ld_issued;
+    };
+    auto stage_beta = [&](int m) {
         const int64_t tm = start + (int64_t)m * C;
-        const int vm = min(C, len - m * C);
-        for (int i = tid; i < vm * 16; i += kThreads) {  // log_alpha: 16 pieces per row
-            const int t = i >> 4, c4 = (i & 15) * 4;
-            const size_t g = ((size_t)(tm + t) * p.H + h) * D + c4;
-            if (in_bounds(p.status, g + 3, n_tok)) cp_async16(raw_la + t * D + c4, p.log_alpha + g);
-        }
-        constexpr int kPieces = kRow / 16;
-        for (int i = tid; i < 3 * vm * kPieces; i += kThreads) {
-            const int w = i / (vm * kPieces), r = i % (vm * kPieces);
-            const int t = r / kPieces, e = (r % kPieces) * (16 / (int)sizeof(T));
-            if (w == 2 && vzero) continue;
-            const T *src = w == 0 ? k : w == 1 ? q : v;
-            const size_t g = ((size_t)(tm + t) * p.H + h) * D + e;
-            if (in_bounds(p.status, g + 16 / sizeof(T) - 1, n_tok))
-                cp_async16(sm.raw + (w + 1) * C * 256 + t * kRow + e * sizeof(T), src + g);
-        }
-        if (tid < vm) {
+        if (tid < min(C, len - m * C)) {
             const size_t bi = (size_t)(tm + tid) * p.H + h;
             if (in_bounds(p.status, bi, n_beta)) cp_async4(&sm.rbet[tid], p.beta + bi);
         }
     };
-    prefetch(0);
+    if (tid == 0) {
+        prefetch_tensormap(&tm_la);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_v);
+        issue_rows(0);
+    }
+    stage_beta(0);
     cp_async_wait_all();
     __syncthreads();
 
@@ -380,39 +407,87 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
         const int64_t t0 = start + (int64_t)n * C;
         const int valid = min(C, len - n * C);
         // ---------------------------------------------- a1, a2: gates and operands
-        // from the staged rows: thread (half, c) takes channel c of tokens
-        // 32 half .. 32 half + 31 -- its k, q, v and gates; the second half
-        // first sums the first half's log-decays for its starting G -- and
-        // thread t < 64 the beta of token t
+        // thread (quarter w, pair c2) takes channels 2 c2, 2 c2 + 1 of tokens
+        // 16 w .. 16 w + 15: their log2-decays summed per quarter first (the
+        // quarter's starting G is the sum of the quarters before it), then Gamma
+        // and 1 / Gamma by ex2 on the cumulative log2-decay, and k, q, v as bf16
+        // pairs, two channels per 32-bit store; thread t < 64 takes the beta of
+        // token t
+        mbar_wait(smem_u32(&sm.bar_ld), n & 1, abort);
         {
-            const int c = tid & (D - 1), half = tid >> 6;
-            const int t_begin = 32 * half;
-            float G = 0.f;
-            if (half) {
-#pragma unroll 8
-                for (int t = 0; t < 32; ++t) G += t < valid ? raw_la[t * D + c] : 0.f;
+            const int c2 = tid & 31, w = tid >> 5, c = 2 * c2;
+            constexpr float kLog2e = 1.4426950408889634f;
+            float l0[16], l1[16];
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = 16 * w + i;
+                const float2 la = t < valid ? *reinterpret_cast<const float2 *>(raw_la + t * D + c)
+                                            : make_float2(0.f, 0.f);
+                l0[i] = la.x * kLog2e;
+                l1[i] = la.y * kLog2e;
+                s0 += l0[i];
+                s1 += l1[i];
             }
-#pragma unroll 4
-            for (int t = t_begin; t < t_begin + 32; ++t) {
-                const bool live = t < valid;
-                G += live ? raw_la[t * D + c] : 0.f;
-                const float kf = live ? ld(raw_k, t * D + c) : 0.f;
-                const float qf = live ? ld(raw_q, t * D + c) : 0.f;
-                const float gf = expf(G), gi = expf(-G);
-                const float kh = kf * gf;
-                put(sm.xq, 16384, t, c, kh);
-                put(sm.xq, 16384, 64 + t, c, qf * gf);
-                put(sm.kb, 8192, t, c, kf * gi);
-                put(sm.kv, 16384, t, c, kh);
-                put(sm.kv + 8192, 16384, t, c, live && !vzero ? ld(raw_v, t * D + c) : 0.f);
-                if (t == C - 1) sm.gam[c] = gf;
-            }
-            if (half && !(G >= -kLogDecayLimit)) *reinterpret_cast<volatile int *>(&sm.domain) = 1;
+            *reinterpret_cast<float2 *>(&sm.gpart[w][c]) = make_float2(s0, s1);
             if (tid < C) sm.bet[tid] = tid < valid ? sm.rbet[tid] : 0.f;
+            __syncthreads();
+            float G0 = 0.f, G1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < 3; ++u)
+                if (u < w) {
+                    const float2 g = *reinterpret_cast<const float2 *>(&sm.gpart[u][c]);
+                    G0 += g.x;
+                    G1 += g.y;
+                }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = 16 * w + i;
+                const bool live = t < valid;
+                G0 += l0[i];
+                G1 += l1[i];
+                const float g0 = ex2_approx(G0), g1 = ex2_approx(G1);
+                const float r0 = ex2_approx(-G0), r1 = ex2_approx(-G1);
+                float k0 = 0.f, k1 = 0.f, q0 = 0.f, q1 = 0.f, v0 = 0.f, v1 = 0.f;
+                if (live) {
+                    if constexpr (sizeof(T) == 4) {
+                        const float2 kk = *reinterpret_cast<const float2 *>(raw_k + t * D + c);
+                        const float2 qq = *reinterpret_cast<const float2 *>(raw_q + t * D + c);
+                        k0 = kk.x, k1 = kk.y, q0 = qq.x, q1 = qq.y;
+                        if (!vzero) {
+                            const float2 vv = *reinterpret_cast<const float2 *>(raw_v + t * D + c);
+                            v0 = vv.x, v1 = vv.y;
+                        }
+                    } else {
+                        const uint32_t kk = *reinterpret_cast<const uint32_t *>(raw_k + t * D + c);
+                        const uint32_t qq = *reinterpret_cast<const uint32_t *>(raw_q + t * D + c);
+                        k0 = __uint_as_float(kk << 16), k1 = __uint_as_float(kk & 0xFFFF0000u);
+                        q0 = __uint_as_float(qq << 16), q1 = __uint_as_float(qq & 0xFFFF0000u);
+                        if (!vzero) {
+                            const uint32_t vv = *reinterpret_cast<const uint32_t *>(raw_v + t * D + c);
+                            v0 = __uint_as_float(vv << 16), v1 = __uint_as_float(vv & 0xFFFF0000u);
+                        }
+                    }
+                }
+                const float kh0 = k0 * g0, kh1 = k1 * g1;
+                put2(sm.xq, 16384, t, c, kh0, kh1);
+                put2(sm.xq, 16384, 64 + t, c, q0 * g0, q1 * g1);
+                put2(sm.kb, 8192, t, c, k0 * r0, k1 * r1);
+                put2(sm.kv, 16384, t, c, kh0, kh1);
+                put2(sm.kv + 8192, 16384, t, c, v0, v1);
+                if (t == C - 1) *reinterpret_cast<float2 *>(&sm.gam[c]) = make_float2(g0, g1);
+            }
+            constexpr float kLimit2 = kLogDecayLimit * kLog2e;
+            if (w == 3 && !(G0 >= -kLimit2 && G1 >= -kLimit2))
+                *reinterpret_cast<volatile int *>(&sm.domain) = 1;
         }
         publish_smem();
         if (*reinterpret_cast<volatile int *>(&sm.domain)) break;  // (read by all after the barrier)
-        if (n + 1 < nchunks) prefetch(n + 1);  // the staged rows have been read
+        // the staged rows have been read: the next chunk's may land
+        if (n + 1 < nchunks) {
+            if (tid == 0 && !*abort) issue_rows(n + 1);
+            stage_beta(n + 1);
+        }
 
         // ---------------------------------------------- a3, a5: R = [Kh; Qh] Kb^T
         if (tid == 0) {
@@ -431,7 +506,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
                 if (top) {  // A[r][j] = beta_r R[r][j]; only j < r is read
                     const float br = sm.bet[L];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) sm.a[L * LDA + 32 * half + j] = br * __uint_as_float(x[j]);
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(&sm.a[L * LDA + 32 * half + j]) =
+                            make_float4(br * __uint_as_float(x[j]), br * __uint_as_float(x[j + 1]),
+                                        br * __uint_as_float(x[j + 2]),
+                                        br * __uint_as_float(x[j + 3]));
                 } else {    // M[r][j] = R[64 + r][j], j <= r
                     const int r = L - 64;
 #pragma unroll
@@ -451,26 +530,135 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
         __syncthreads();
 
         // ---------------------------------------------- a4: T' = (I + A)^-1 diag(beta)
-        // thread j < 64: column j of T = (I + A)^-1 by forward substitution
-        // (T[r][j] = -sum_{s < r} A[r][s] T[s][j] below the diagonal), two
-        // partial sums to halve the dependency chain; then T'[r][j] = T[r][j] beta_j
-        if (tid < C) {
-            const int j = tid;
-            float x[C];
+        // T = (I + A)^-1 by blocks: the four 16 x 16 diagonal blocks D_b by
+        // forward substitution; the two 32 x 32 diagonal halves T1 = [D0 0; E0 D1]
+        // and T2 = [D2 0; E1 D3] with E0 = -D1 (A10 D0), E1 = -D3 (A32 D2); the
+        // lower-left half T21 = -T2 (A21 T1).  fp32 throughout; T1, T2 and the
+        // products in between live in the -W tile's bytes (free until W^T lands).
+        {
+            float *T1 = reinterpret_cast<float *>(sm.wn), *T2 = T1 + 32 * LDT, *P = T2 + 32 * LDT;
+            if (tid < 64) {  // column jj of D_b: y = (I + A_bb)^-1 e_jj
+                const int b = tid >> 4, jj = tid & 15;
+                const float *Ab = sm.a + 16 * b * LDA + 16 * b;
+                float y[16];
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                float s0 = 0.f, s1 = 0.f;
+                for (int i = 0; i < 16; ++i) {
+                    float acc = i == jj ? 1.f : 0.f;
 #pragma unroll
-                for (int s = 0; s + 1 < r; s += 2) {
-                    s0 = fmaf(sm.a[r * LDA + s], x[s], s0);
-                    s1 = fmaf(sm.a[r * LDA + s + 1], x[s + 1], s1);
+                    for (int s4 = 0; s4 < i; s4 += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(Ab + i * LDA + s4);
+                        acc = fmaf(-a4.x, y[s4], acc);
+                        if (s4 + 1 < i) acc = fmaf(-a4.y, y[s4 + 1], acc);
+                        if (s4 + 2 < i) acc = fmaf(-a4.z, y[s4 + 2], acc);
+                        if (s4 + 3 < i) acc = fmaf(-a4.w, y[s4 + 3], acc);
+                    }
+                    y[i] = acc;
                 }
-                if (r & 1) s0 = fmaf(sm.a[r * LDA + r - 1], x[r - 1], s0);
-                x[r] = r < j ? 0.f : r == j ? 1.f : -(s0 + s1);
-            }
-            const float bj = sm.bet[j];
+                float *Db = (b < 2 ? T1 : T2) + (b & 1) * 16 * (LDT + 1);
 #pragma unroll
-            for (int r = 0; r < C; ++r) put(sm.tp, 8192, r, j, x[r] * bj);
+                for (int i = 0; i < 16; ++i) Db[i * LDT + jj] = y[i];
+            } else {  // the zero upper-right blocks of T1 and T2
+                const int u = tid - 64;
+#pragma unroll
+                for (int e = u; e < 128; e += 64)
+                    *reinterpret_cast<float4 *>((e < 64 ? T1 : T2) + ((e >> 2) & 15) * LDT + 16 +
+                                                4 * (e & 3)) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            __syncthreads();
+            // thread (m, rr, cq): row rr, columns 4 cq .. 4 cq + 3 of the 16 x 16
+            // product m (0: the T1 half, 1: the T2 half)
+            const int m = tid >> 6, rr = (tid >> 2) & 15, cq = tid & 3;
+            float *Tm = m ? T2 : T1;
+            {  // P_m = A_(2m+1, 2m) D_2m  -> rows 16 m .. of P
+                const float *x = sm.a + (16 + 32 * m + rr) * LDA + 32 * m;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k4 = 0; k4 < 16; k4 += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(x + k4);
+                    axpy4(acc, a4.x, Tm + (k4 + 0) * LDT + 4 * cq);
+                    axpy4(acc, a4.y, Tm + (k4 + 1) * LDT + 4 * cq);
+                    axpy4(acc, a4.z, Tm + (k4 + 2) * LDT + 4 * cq);
+                    axpy4(acc, a4.w, Tm + (k4 + 3) * LDT + 4 * cq);
+                }
+                *reinterpret_cast<float4 *>(P + (16 * m + rr) * LDT + 4 * cq) = acc;
+            }
+            __syncthreads();
+            {  // E_m = -D_(2m+1) P_m  -> rows 16 .. 31, columns 0 .. 15 of the half
+                const float *x = Tm + (16 + rr) * LDT + 16;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k4 = 0; k4 < 16; k4 += 4) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(x + k4);
+                    axpy4(acc, d4.x, P + (16 * m + k4 + 0) * LDT + 4 * cq);
+                    axpy4(acc, d4.y, P + (16 * m + k4 + 1) * LDT + 4 * cq);
+                    axpy4(acc, d4.z, P + (16 * m + k4 + 2) * LDT + 4 * cq);
+                    axpy4(acc, d4.w, P + (16 * m + k4 + 3) * LDT + 4 * cq);
+                }
+                *reinterpret_cast<float4 *>(Tm + (16 + rr) * LDT + 4 * cq) =
+                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            }
+            __syncthreads();
+            // thread (rp, cq8): rows 2 rp, 2 rp + 1, columns 4 cq8 .. 4 cq8 + 3 of a
+            // 32 x 32 block
+            const int rp = tid >> 3, cq8 = tid & 7;
+            const int r0 = 2 * rp, col = 4 * cq8;
+            {  // P = A21 T1
+                const float *x0 = sm.a + (32 + r0) * LDA, *x1 = x0 + LDA;
+                float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+#pragma unroll
+                for (int k4 = 0; k4 < 32; k4 += 4) {
+                    const float4 a0 = *reinterpret_cast<const float4 *>(x0 + k4);
+                    const float4 a1 = *reinterpret_cast<const float4 *>(x1 + k4);
+                    const float *y = T1 + k4 * LDT + col;
+                    axpy4(acc0, a0.x, y);
+                    axpy4(acc1, a1.x, y);
+                    axpy4(acc0, a0.y, y + LDT);
+                    axpy4(acc1, a1.y, y + LDT);
+                    axpy4(acc0, a0.z, y + 2 * LDT);
+                    axpy4(acc1, a1.z, y + 2 * LDT);
+                    axpy4(acc0, a0.w, y + 3 * LDT);
+                    axpy4(acc1, a1.w, y + 3 * LDT);
+                }
+                *reinterpret_cast<float4 *>(P + r0 * LDT + col) = acc0;
+                *reinterpret_cast<float4 *>(P + (r0 + 1) * LDT + col) = acc1;
+            }
+            __syncthreads();
+            {  // T21 = -T2 P, and T' = T diag(beta) written as bf16 pairs: rows
+               // 0-31 [T1 0], rows 32-63 [T21 T2]
+                const float *x0 = T2 + r0 * LDT, *x1 = x0 + LDT;
+                float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+#pragma unroll
+                for (int k4 = 0; k4 < 32; k4 += 4) {
+                    const float4 a0 = *reinterpret_cast<const float4 *>(x0 + k4);
+                    const float4 a1 = *reinterpret_cast<const float4 *>(x1 + k4);
+                    const float *y = P + k4 * LDT + col;
+                    axpy4(acc0, a0.x, y);
+                    axpy4(acc1, a1.x, y);
+                    axpy4(acc0, a0.y, y + LDT);
+                    axpy4(acc1, a1.y, y + LDT);
+                    axpy4(acc0, a0.z, y + 2 * LDT);
+                    axpy4(acc1, a1.z, y + 2 * LDT);
+                    axpy4(acc0, a0.w, y + 3 * LDT);
+                    axpy4(acc1, a1.w, y + 3 * LDT);
+                }
+                const float4 bl = *reinterpret_cast<const float4 *>(&sm.bet[col]);
+                const float4 bh = *reinterpret_cast<const float4 *>(&sm.bet[32 + col]);
+                auto scaled = [](const float4 &t, const float4 &b, float sg) {
+                    return make_float4(sg * t.x * b.x, sg * t.y * b.y, sg * t.z * b.z, sg * t.w * b.w);
+                };
+                const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = r0 + e;
+                    const float4 &acc = e ? acc1 : acc0;
+                    put4(sm.tp, 8192, r, col,
+                         scaled(*reinterpret_cast<const float4 *>(T1 + r * LDT + col), bl, 1.f));
+                    put4(sm.tp, 8192, r, 32 + col, zero);
+                    put4(sm.tp, 8192, 32 + r, col, scaled(acc, bl, -1.f));
+                    put4(sm.tp, 8192, 32 + r, 32 + col,
+                         scaled(*reinterpret_cast<const float4 *>(T2 + r * LDT + col), bh, 1.f));
+                }
+            }
         }
         publish_smem();
 
@@ -584,10 +772,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
             }
         }
     }
-    // teardown: every MMA issued has completed before tensor memory is freed
+    // teardown: every MMA issued has completed before tensor memory is freed,
+    // and the last row copy has landed (it is in flight only after a timeout)
     if (tid == 0) {
         mma_commit(smem_u32(&sm.bar_fin));
         wait_bounded(sm.bar_fin, 0);
+        if (ld_issued > 0) wait_bounded(sm.bar_ld, (ld_issued - 1) & 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -599,18 +789,51 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc64_kernel(const __grid_
     if (domain && !sm.abort) serial_pass<T>(p, sm, start, len, h, sref);
 }
 
+// [Ttot][H][64] rows (fp32 or bf16) as a 3-D tensor, tile = 64 channels x one
+// head x 64 tokens, unswizzled (the tile is dense in shared memory, row t at
+// t * 64 elements); tokens past Ttot read as zero.
+bool make_rows_map(CUtensorMap *map, const void *base, bool fp32, int H, int64_t Ttot) {
+    static PFN_cuTensorMapEncodeTiled_v12000 enc = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    if (!enc) return false;
+    const cuuint64_t eb = fp32 ? 4 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)Ttot};
+    cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)H * D * eb};
+    cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
+    cuuint32_t elem[3] = {1, 1, 1};
+    return enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void *>(base), dims, strides, box, elem,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc64(const FwdParams &p, kda_dtype_t dt, cudaStream_t s) {
     if ((size_t)p.N * p.H == 0) return cudaSuccess;
     if (p.Ttot > INT32_MAX || p.dk != D || p.dv != D) return cudaErrorInvalidValue;
+    if (p.Ttot == 0) return launch_prefill_simt(p, dt, s);  // every sequence empty
+    const bool f32 = dt == KDA_F32;
+    CUtensorMap ml, mk, mq, mv;
+    if (!make_rows_map(&ml, p.log_alpha, true, p.H, p.Ttot) ||
+        !make_rows_map(&mk, p.k, f32, p.H, p.Ttot) || !make_rows_map(&mq, p.q, f32, p.H, p.Ttot) ||
+        !make_rows_map(&mv, p.v, f32, p.H, p.Ttot))
+        return cudaErrorInvalidValue;
     const size_t smem = sizeof(Tc64Smem) + 1024;
     const unsigned blocks = (unsigned)((size_t)p.N * p.H);
-    auto kern = dt == KDA_F32 ? prefill_tc64_kernel<float> : prefill_tc64_kernel<__nv_bfloat16>;
+    auto kern = f32 ? prefill_tc64_kernel<float> : prefill_tc64_kernel<__nv_bfloat16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<blocks, kThreads, smem, s>>>(p);
+    kern<<<blocks, kThreads, smem, s>>>(p, ml, mk, mq, mv);
     return cudaGetLastError();
 }
 
