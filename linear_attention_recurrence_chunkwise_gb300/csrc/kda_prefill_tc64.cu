@@ -7,9 +7,13 @@
 //   G = in-chunk inclusive cumsum of log_alpha, Gamma = exp(G), gamma = Gamma_63
 //   Kh = K . Gamma,  Qh = Q . Gamma,  Kb = K / Gamma
 //   R = [Kh; Qh] Kb^T:  A = StrictTril(diag(beta) R_top),  M = Tril(R_bottom)
-//   T' = (I + A)^-1 diag(beta)                      (fp32 forward substitution)
-//   [W^T; U~^T] = [Kh^T; V^T] T'^T
-//   U^T = U~^T - S^T W^T,  O^T = S^T Qh^T + U^T M^T,  S^T <- (S^T + U^T Kb) Diag(gamma)
+//   [Z^T | O^T] = S^T [Kh; Qh]^T                    (issued with R, before the solve)
+//   T' = (I + A)^-1 diag(beta)                      (fp32, by blocks)
+//   U^T = (V^T - Z^T) T'^T,  O^T += U^T M^T,  S^T <- (S^T + U^T Kb) Diag(gamma)
+//
+// U = T' (V - Kh S) is the chunk form's U~ - W S with W = T' Kh and U~ = T' V,
+// taken in the order that needs no W: the product with the state runs while
+// the solve does, and one product follows it instead of two.
 //
 // fp32 accuracy from the bf16 tensor cores: each operand x is held as the pair
 // hi = bf16(x), lo = bf16(x - hi), which leaves x - hi - lo within 2^-17 |x|,
@@ -19,12 +23,11 @@
 // of a 64-wide head have the shape of the two 64-channel slabs of a 128-wide
 // bf16 head and use the same 128-byte-swizzled layouts and descriptors.
 //
-// Every MMA has M = 128: R stacks the Kh and Qh rows, [W^T; U~^T] stacks the
-// key and value features; the products whose left operand has 64 rows (S^T and
-// U^T, bf16 pairs read from tensor memory) hold them in lanes 64-127, so their
-// results land in lanes 64-127, and lanes 0-63 of those operands stay zero.
-// So warps 0-1 (tensor-memory lanes 0-63) read out A and W^T, warps 2-3
-// (lanes 64-127) M, U^T, O^T and the state.  One CTA of 128 threads per
+// Every MMA has M = 128: R stacks the Kh and Qh rows; the products whose left
+// operand has 64 rows (S^T, V^T - Z^T and U^T, bf16 pairs read from tensor
+// memory) hold them in lanes 64-127, so their results land in lanes 64-127, and
+// lanes 0-63 of those operands stay zero.  So warps 0-1 (tensor-memory lanes
+// 0-63) read out A, warps 2-3 (lanes 64-127) M, Z^T, U^T, O^T and the state.  One CTA of 128 threads per
 // (sequence, head) walks the chunks one at a time; one thread issues the MMAs
 // and the TMA copies of the next chunk's rows (issued as soon as the current
 // chunk's rows have been read, landing while the chunk computes).  The
@@ -54,23 +57,23 @@ constexpr int kThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns (128 lanes each)
 constexpr uint32_t kColR = 0;     // R = [Kh; Qh] Kb^T                    (64 fp32)
-constexpr uint32_t kColWU = 64;   // [W^T; U~^T], then lanes 64-127 U^T   (64 fp32)
+constexpr uint32_t kColZ = 64;    // Z^T, then U^T, in lanes 64-127       (64 fp32)
 constexpr uint32_t kColO = 128;   // O^T in lanes 64-127                  (64 fp32)
+static_assert(kColO == kColZ + 64, "[Z^T | O^T] is one product of N = 128");
 constexpr uint32_t kColS = 192;   // S^T master in lanes 64-127           (64 fp32)
 constexpr uint32_t kColSb = 256;  // S^T bf16 pairs: hi 32 columns, lo 32 (A operand)
-constexpr uint32_t kColUb = 320;  // U^T bf16 pairs: hi 32 columns, lo 32 (A operand)
+constexpr uint32_t kColUb = 320;  // V^T - Z^T, then U^T, as bf16 pairs: hi 32 columns,
+                                  // lo 32 (A operand)
 constexpr int LDA = C + 4;        // fp32 row stride of A (rows start on 16 bytes)
 constexpr int LDT = 36;           // fp32 row stride of the solve's 32 x 32 blocks
 
 struct __align__(1024) Tc64Smem {
     uint8_t xq[32768];  // [Kh; Qh] K-major, 128 rows x 64 channels: hi tile | lo tile
     uint8_t kb[16384];  // Kb [j][c]: hi | lo; K-major B of R, MN-major B of the S update
-    uint8_t kv[32768];  // [Kh | V] MN-major A of [W^T; U~^T]: per part (hi | lo) the
-                        // key block [j][c] then the value block [j][v] (8 KB each)
     uint8_t tp[16384];  // T' [r][j] K-major: hi | lo
-    uint8_t wn[16384];  // -W as [c][r] (MN-major B of U): hi | lo; during the solve,
-                        // its 32 x 32 blocks T1, T2 and P (fp32, rows of LDT)
     uint8_t mm[16384];  // M [r][j] K-major: hi | lo
+    float vt[C * D];    // V [t][v] in fp32 (for V^T - Z^T)
+    float ts[4096];     // the solve's 32 x 32 blocks T1, T2 and P (fp32, rows of LDT)
     uint8_t raw[4 * C * 256];  // the next chunk's rows as they are in memory (TMA):
                                // log_alpha, k, q, v, 64 rows each of 64 elements
     float a[C * LDA];   // beta-scaled A (fp32); staging of the token-by-token pass
@@ -78,7 +81,7 @@ struct __align__(1024) Tc64Smem {
     float gam[D];
     float bet[C];
     float rbet[C];      // the next chunk's beta (cp.async)
-    uint64_t bar_mma, bar_fin, bar_ld;
+    uint64_t bar_mma, bar_fin, bar_ld, bar_zo;
     uint32_t tmem_base;
     int abort;
     int domain;
@@ -306,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&sm.bar_mma), 1);
         mbar_init(smem_u32(&sm.bar_fin), 1);
         mbar_init(smem_u32(&sm.bar_ld), 1);
+        mbar_init(smem_u32(&sm.bar_zo), 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -359,11 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
     }
 
-    const uint32_t a_xq = smem_u32(sm.xq), a_kb = smem_u32(sm.kb), a_kv = smem_u32(sm.kv);
-    const uint32_t a_tp = smem_u32(sm.tp), a_wn = smem_u32(sm.wn), a_mm = smem_u32(sm.mm);
-    const uint32_t id_kk = idesc_bf16(128, 64, false, false);  // K-major A and B
-    const uint32_t id_mk = idesc_bf16(128, 64, true, false);   // MN-major A
-    const uint32_t id_km = idesc_bf16(128, 64, false, true);   // MN-major B
+    const uint32_t a_xq = smem_u32(sm.xq), a_kb = smem_u32(sm.kb);
+    const uint32_t a_tp = smem_u32(sm.tp), a_mm = smem_u32(sm.mm);
+    const uint32_t id_kk = idesc_bf16(128, 64, false, false);   // K-major A and B
+    const uint32_t id_kk2 = idesc_bf16(128, 128, false, false); // the same, N = 128
+    const uint32_t id_km = idesc_bf16(128, 64, false, true);    // MN-major B
 
     // chunk m's rows of log_alpha, k, q, v -> sm.raw by TMA (thread 0; tiles of
     // 64 tokens x one head x 64 channels, zero past the last token; rows past
@@ -469,12 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                const float kh0 = k0 * g0, kh1 = k1 * g1;
-                put2(sm.xq, 16384, t, c, kh0, kh1);
+                put2(sm.xq, 16384, t, c, k0 * g0, k1 * g1);
                 put2(sm.xq, 16384, 64 + t, c, q0 * g0, q1 * g1);
                 put2(sm.kb, 8192, t, c, k0 * r0, k1 * r1);
-                put2(sm.kv, 16384, t, c, kh0, kh1);
-                put2(sm.kv + 8192, 16384, t, c, v0, v1);
+                *reinterpret_cast<float2 *>(&sm.vt[t * D + c]) = make_float2(v0, v1);
                 if (t == C - 1) *reinterpret_cast<float2 *>(&sm.gam[c]) = make_float2(g0, g1);
             }
             constexpr float kLimit2 = kLogDecayLimit * kLog2e;
@@ -489,12 +491,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             stage_beta(n + 1);
         }
 
-        // ---------------------------------------------- a3, a5: R = [Kh; Qh] Kb^T
+        // ---------------------------------------------- a3, a5: R = [Kh; Qh] Kb^T,
+        // then [Z^T | O^T] = S^T [Kh; Qh]^T (completes on its own barrier)
         if (tid == 0) {
             tc_fence_after();
             mma3_ss(tmem + kColR, desc_sw128(a_xq, 16, 1024), 1024, 2, desc_sw128(a_kb, 16, 1024),
                     512, 2, id_kk, false);
             mma_commit(smem_u32(&sm.bar_mma));
+            mma3_ts(tmem + kColZ, tmem + kColSb, desc_sw128(a_xq, 16, 1024), 1024, 2, id_kk2,
+                    false);
+            mma_commit(smem_u32(&sm.bar_zo));
         }
         __syncwarp();
         mma_done();
@@ -533,10 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // T = (I + A)^-1 by blocks: the four 16 x 16 diagonal blocks D_b by
         // forward substitution; the two 32 x 32 diagonal halves T1 = [D0 0; E0 D1]
         // and T2 = [D2 0; E1 D3] with E0 = -D1 (A10 D0), E1 = -D3 (A32 D2); the
-        // lower-left half T21 = -T2 (A21 T1).  fp32 throughout; T1, T2 and the
-        // products in between live in the -W tile's bytes (free until W^T lands).
+        // lower-left half T21 = -T2 (A21 T1), in fp32.  Meanwhile warps 2-3 form
+        // V^T - Z^T as bf16 pairs, the left operand of U^T.
         {
-            float *T1 = reinterpret_cast<float *>(sm.wn), *T2 = T1 + 32 * LDT, *P = T2 + 32 * LDT;
+            float *T1 = sm.ts, *T2 = T1 + 32 * LDT, *P = T2 + 32 * LDT;
             if (tid < 64) {  // column jj of D_b: y = (I + A_bb)^-1 e_jj
                 const int b = tid >> 4, jj = tid & 15;
                 const float *Ab = sm.a + 16 * b * LDA + 16 * b;
@@ -557,7 +563,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float *Db = (b < 2 ? T1 : T2) + (b & 1) * 16 * (LDT + 1);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) Db[i * LDT + jj] = y[i];
-            } else {  // the zero upper-right blocks of T1 and T2
+            } else {  // V^T - Z^T (lane 64 + v: row v), and the zero upper-right
+                      // blocks of T1 and T2
+                mbar_wait(smem_u32(&sm.bar_zo), n & 1, abort);
+                tc_fence_after();
+                const int vv = L - 64;
+                uint32_t x[32], hp[16], lp[16];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    tmem_ld32(tmem + lane_addr + kColZ + 32 * half, x);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        x[j] = __float_as_uint(sm.vt[(32 * half + j) * D + vv] - __uint_as_float(x[j]));
+                    split_pairs(x, hp, lp);
+                    tmem_st16(tmem + lane_addr + kColUb + 16 * half, hp);
+                    tmem_st16(tmem + lane_addr + kColUb + 32 + 16 * half, lp);
+                }
+                tmem_wait_st();
                 const int u = tid - 64;
 #pragma unroll
                 for (int e = u; e < 128; e += 64)
@@ -662,38 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         publish_smem();
 
-        // ---------------------------------------------- [W^T; U~^T] = [Kh^T; V^T] T'^T
+        // ---------------------------------------------- a6: U^T = (V^T - Z^T) T'^T
         if (tid == 0) {
             tc_fence_after();
-            mma3_ss(tmem + kColWU, desc_sw128(a_kv, 8192, 1024), 1024, 128,
-                    desc_sw128(a_tp, 16, 1024), 512, 2, id_mk, false);
-            mma_commit(smem_u32(&sm.bar_mma));
-        }
-        __syncwarp();
-        mma_done();
-        if (top) {  // -W as [c][r]: lane c holds row c of W^T
-            uint32_t x[32];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld32(tmem + lane_addr + kColWU + 32 * half, x);
-#pragma unroll
-                for (int j8 = 0; j8 < 32; j8 += 8) {
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(x[j8 + e]);
-                    put8(sm.wn, 8192, L, 32 * half + j8, f);
-                }
-            }
-        }
-        publish_smem();
-
-        // ---------------------------------------------- a6: U^T = U~^T - S^T W^T, O^T = S^T Qh^T
-        if (tid == 0) {
-            tc_fence_after();
-            mma3_ts(tmem + kColWU, tmem + kColSb, desc_sw128(a_wn, 8192, 1024), 512, 128, id_km,
-                    true);
-            mma3_ts(tmem + kColO, tmem + kColSb, desc_sw128(a_xq + 8192, 16, 1024), 1024, 2, id_kk,
-                    false);
+            mma3_ts(tmem + kColZ, tmem + kColUb, desc_sw128(a_tp, 16, 1024), 512, 2, id_kk, false);
             mma_commit(smem_u32(&sm.bar_mma));
         }
         __syncwarp();
@@ -702,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t x[32], hp[16], lp[16];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                tmem_ld32(tmem + lane_addr + kColWU + 32 * half, x);
+                tmem_ld32(tmem + lane_addr + kColZ + 32 * half, x);
                 split_pairs(x, hp, lp);
                 tmem_st16(tmem + lane_addr + kColUb + 16 * half, hp);
                 tmem_st16(tmem + lane_addr + kColUb + 32 + 16 * half, lp);
@@ -751,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_wait_st();
         }
-        cp_async_wait_all();  // the next chunk's rows have landed
+        cp_async_wait_all();  // the next chunk's beta has landed
         tc_fence_before();
         __syncthreads();
     }
