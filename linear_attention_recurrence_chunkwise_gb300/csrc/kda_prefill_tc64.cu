@@ -77,8 +77,8 @@ struct __align__(1024) Tc64Smem {
     uint8_t raw[4 * C * 256];  // the next chunk's rows as they are in memory (TMA):
                                // log_alpha, k, q, v, 64 rows each of 64 elements
     float a[C * LDA];   // beta-scaled A (fp32); staging of the token-by-token pass
-    float gpart[4][D];  // log2-decay sums of each quarter of the chunk's tokens
-    float gam[D];
+    float gpart[1][D];  // log2-decay sums of the first half of the chunk's tokens
+    float gam[2][D];    // gamma of the chunk (even, odd)
     float bet[C];
     float rbet[C];      // the next chunk's beta (cp.async)
     uint64_t bar_mma, bar_fin, bar_ld, bar_zo;
@@ -403,87 +403,86 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tm_v);
         issue_rows(0);
     }
+    // ------------------------------------------------ a1, a2: gates and operands
+    // of chunk m, by warps 0-1 (the first chunk's before the loop, every other
+    // one while warps 2-3 write out the chunk before it): thread (w, c2) takes
+    // channels 2 c2, 2 c2 + 1 of tokens 32 w .. 32 w + 31 -- their log2-decays
+    // summed per half first (the second half starts from the first half's
+    // sum), then Gamma and 1 / Gamma by ex2 on the cumulative log2-decay, and
+    // k, q as bf16 pairs, two channels per 32-bit store, v in fp32; thread t
+    // takes the beta of token t.
+    auto operands = [&](int m) {
+        const int valid = min(C, len - m * C);
+        const int c2 = tid & 31, w = tid >> 5, c = 2 * c2;
+        constexpr float kLog2e = 1.4426950408889634f;
+        mbar_wait(smem_u32(&sm.bar_ld), m & 1, abort);
+        cp_async_wait_all();  // this thread's beta copy
+        sm.bet[tid] = tid < valid ? sm.rbet[tid] : 0.f;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {
+            const int t = 32 * w + i;
+            if (t < valid) {
+                const float2 la = *reinterpret_cast<const float2 *>(raw_la + t * D + c);
+                s0 = fmaf(la.x, kLog2e, s0);
+                s1 = fmaf(la.y, kLog2e, s1);
+            }
+        }
+        if (w == 0) *reinterpret_cast<float2 *>(&sm.gpart[0][c]) = make_float2(s0, s1);
+        named_bar_sync(1, 64);
+        float G0 = 0.f, G1 = 0.f;
+        if (w) {
+            const float2 g = *reinterpret_cast<const float2 *>(&sm.gpart[0][c]);
+            G0 = g.x;
+            G1 = g.y;
+        }
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {
+            const int t = 32 * w + i;
+            const bool live = t < valid;
+            float k0 = 0.f, k1 = 0.f, q0 = 0.f, q1 = 0.f, v0 = 0.f, v1 = 0.f;
+            if (live) {
+                const float2 la = *reinterpret_cast<const float2 *>(raw_la + t * D + c);
+                G0 = fmaf(la.x, kLog2e, G0);
+                G1 = fmaf(la.y, kLog2e, G1);
+                if constexpr (sizeof(T) == 4) {
+                    const float2 kk = *reinterpret_cast<const float2 *>(raw_k + t * D + c);
+                    const float2 qq = *reinterpret_cast<const float2 *>(raw_q + t * D + c);
+                    k0 = kk.x, k1 = kk.y, q0 = qq.x, q1 = qq.y;
+                    if (!vzero) {
+                        const float2 vv = *reinterpret_cast<const float2 *>(raw_v + t * D + c);
+                        v0 = vv.x, v1 = vv.y;
+                    }
+                } else {
+                    const uint32_t kk = *reinterpret_cast<const uint32_t *>(raw_k + t * D + c);
+                    const uint32_t qq = *reinterpret_cast<const uint32_t *>(raw_q + t * D + c);
+                    k0 = __uint_as_float(kk << 16), k1 = __uint_as_float(kk & 0xFFFF0000u);
+                    q0 = __uint_as_float(qq << 16), q1 = __uint_as_float(qq & 0xFFFF0000u);
+                    if (!vzero) {
+                        const uint32_t vv = *reinterpret_cast<const uint32_t *>(raw_v + t * D + c);
+                        v0 = __uint_as_float(vv << 16), v1 = __uint_as_float(vv & 0xFFFF0000u);
+                    }
+                }
+            }
+            const float g0 = ex2_approx(G0), g1 = ex2_approx(G1);
+            const float r0 = ex2_approx(-G0), r1 = ex2_approx(-G1);
+            put2(sm.xq, 16384, t, c, k0 * g0, k1 * g1);
+            put2(sm.xq, 16384, 64 + t, c, q0 * g0, q1 * g1);
+            put2(sm.kb, 8192, t, c, k0 * r0, k1 * r1);
+            *reinterpret_cast<float2 *>(&sm.vt[t * D + c]) = make_float2(v0, v1);
+            if (t == C - 1) *reinterpret_cast<float2 *>(&sm.gam[m & 1][c]) = make_float2(g0, g1);
+        }
+        constexpr float kLimit2 = kLogDecayLimit * kLog2e;
+        if (w == 1 && !(G0 >= -kLimit2 && G1 >= -kLimit2))
+            *reinterpret_cast<volatile int *>(&sm.domain) = 1;
+    };
     stage_beta(0);
-    cp_async_wait_all();
-    __syncthreads();
+    if (tid < 64) operands(0);
+    publish_smem();
 
     for (int n = 0; n < nchunks; ++n) {
         const int64_t t0 = start + (int64_t)n * C;
         const int valid = min(C, len - n * C);
-        // ---------------------------------------------- a1, a2: gates and operands
-        // thread (quarter w, pair c2) takes channels 2 c2, 2 c2 + 1 of tokens
-        // 16 w .. 16 w + 15: their log2-decays summed per quarter first (the
-        // quarter's starting G is the sum of the quarters before it), then Gamma
-        // and 1 / Gamma by ex2 on the cumulative log2-decay, and k, q, v as bf16
-        // pairs, two channels per 32-bit store; thread t < 64 takes the beta of
-        // token t
-        mbar_wait(smem_u32(&sm.bar_ld), n & 1, abort);
-        {
-            const int c2 = tid & 31, w = tid >> 5, c = 2 * c2;
-            constexpr float kLog2e = 1.4426950408889634f;
-            float l0[16], l1[16];
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int t = 16 * w + i;
-                const float2 la = t < valid ? *reinterpret_cast<const float2 *>(raw_la + t * D + c)
-                                            : make_float2(0.f, 0.f);
-                l0[i] = la.x * kLog2e;
-                l1[i] = la.y * kLog2e;
-                s0 += l0[i];
-                s1 += l1[i];
-            }
-            *reinterpret_cast<float2 *>(&sm.gpart[w][c]) = make_float2(s0, s1);
-            if (tid < C) sm.bet[tid] = tid < valid ? sm.rbet[tid] : 0.f;
-            __syncthreads();
-            float G0 = 0.f, G1 = 0.f;
-#pragma unroll
-            for (int u = 0; u < 3; ++u)
-                if (u < w) {
-                    const float2 g = *reinterpret_cast<const float2 *>(&sm.gpart[u][c]);
-                    G0 += g.x;
-                    G1 += g.y;
-                }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int t = 16 * w + i;
-                const bool live = t < valid;
-                G0 += l0[i];
-                G1 += l1[i];
-                const float g0 = ex2_approx(G0), g1 = ex2_approx(G1);
-                const float r0 = ex2_approx(-G0), r1 = ex2_approx(-G1);
-                float k0 = 0.f, k1 = 0.f, q0 = 0.f, q1 = 0.f, v0 = 0.f, v1 = 0.f;
-                if (live) {
-                    if constexpr (sizeof(T) == 4) {
-                        const float2 kk = *reinterpret_cast<const float2 *>(raw_k + t * D + c);
-                        const float2 qq = *reinterpret_cast<const float2 *>(raw_q + t * D + c);
-                        k0 = kk.x, k1 = kk.y, q0 = qq.x, q1 = qq.y;
-                        if (!vzero) {
-                            const float2 vv = *reinterpret_cast<const float2 *>(raw_v + t * D + c);
-                            v0 = vv.x, v1 = vv.y;
-                        }
-                    } else {
-                        const uint32_t kk = *reinterpret_cast<const uint32_t *>(raw_k + t * D + c);
-                        const uint32_t qq = *reinterpret_cast<const uint32_t *>(raw_q + t * D + c);
-                        k0 = __uint_as_float(kk << 16), k1 = __uint_as_float(kk & 0xFFFF0000u);
-                        q0 = __uint_as_float(qq << 16), q1 = __uint_as_float(qq & 0xFFFF0000u);
-                        if (!vzero) {
-                            const uint32_t vv = *reinterpret_cast<const uint32_t *>(raw_v + t * D + c);
-                            v0 = __uint_as_float(vv << 16), v1 = __uint_as_float(vv & 0xFFFF0000u);
-                        }
-                    }
-                }
-                put2(sm.xq, 16384, t, c, k0 * g0, k1 * g1);
-                put2(sm.xq, 16384, 64 + t, c, q0 * g0, q1 * g1);
-                put2(sm.kb, 8192, t, c, k0 * r0, k1 * r1);
-                *reinterpret_cast<float2 *>(&sm.vt[t * D + c]) = make_float2(v0, v1);
-                if (t == C - 1) *reinterpret_cast<float2 *>(&sm.gam[c]) = make_float2(g0, g1);
-            }
-            constexpr float kLimit2 = kLogDecayLimit * kLog2e;
-            if (w == 3 && !(G0 >= -kLimit2 && G1 >= -kLimit2))
-                *reinterpret_cast<volatile int *>(&sm.domain) = 1;
-        }
-        publish_smem();
         if (*reinterpret_cast<volatile int *>(&sm.domain)) break;  // (read by all after the barrier)
         // the staged rows have been read: the next chunk's may land
         if (n + 1 < nchunks) {
@@ -737,17 +736,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int half = 0; half < 2; ++half) {
                 tmem_ld32(tmem + lane_addr + kColS + 32 * half, x);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * sm.gam[32 * half + c]);
+                for (int c = 0; c < 32; ++c)
+                    x[c] = __float_as_uint(__uint_as_float(x[c]) * sm.gam[n & 1][32 * half + c]);
                 tmem_st32(tmem + lane_addr + kColS + 32 * half, x);
                 split_pairs(x, hp, lp);
                 tmem_st16(tmem + lane_addr + kColSb + 16 * half, hp);
                 tmem_st16(tmem + lane_addr + kColSb + 32 + 16 * half, lp);
             }
             tmem_wait_st();
+        } else if (n + 1 < nchunks) {
+            operands(n + 1);
         }
-        cp_async_wait_all();  // the next chunk's beta has landed
-        tc_fence_before();
-        __syncthreads();
+        publish_smem();
     }
     const bool domain = sm.domain;
 
