@@ -380,6 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kTile = C * D * sizeof(T);
     int ld_issued = 0;  // row copies issued by thread 0 (one bar_ld phase each)
     auto issue_rows = [&](int m) {
+#if KDA_TEST_SKIP_ARRIVE
+        if (m == 1) return;  // test-only build: chunk 1's rows never arrive, so its wait runs out
+#endif
         const int tm = (int)(start + (int64_t)m * C);
         const uint32_t bar = smem_u32(&sm.bar_ld);
         mbar_arrive_expect_tx(bar, C * D * 4 + (vzero ? 2 : 3) * kTile);
