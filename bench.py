@@ -429,6 +429,7 @@ def run_ours(args, world, rank):
             line["prologue"] = prologue_sub(kda, args, stream, pk)
             line["wide_gates"] = wide_gates_sub(kda, args, stream, pk)
             line["long"] = long_sub(kda, args, stream, pk, cpu)
+            line["tiny"] = tiny_sub(kda, args, stream, pk, cpu)
             line["varlen"] = varlen_sub(kda, args, stream, pk, cpu)
     else:
         line["e2e"] = e2e_decode(kda, w, max(2, min(args.steps, 20)), stream, world)
@@ -717,6 +718,46 @@ def wide_gates_sub(kda, args, stream, pk):
         del prob, o, ST
     out["note"] = ("tensorcore: heads with such chunks are recomputed token by token; "
                    "tensorcore_wide: such chunks take the blocked path on the tensor cores")
+    torch.cuda.empty_cache()
+    return out
+
+
+def tiny_sub(kda, args, stream, pk, cpu=False):
+    """The tiny fp32 recurrence, B=1, H=2, T=256, d=64: the d = 64 tensor-core
+    engine that AUTO runs for fp32 at d = 64, the CUDA-core engine beside it,
+    and both at the prefill size (B=1, H=96, T=8192, d=64, fp32)."""
+    w = make_workload("tiny", seed=args.seed, device="cuda")
+    p = w["prob"]
+    o = torch.empty_like(p.v)
+    ST = torch.empty((p.n_seq, w["H"], w["d"], w["d"]), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.kda_fwd_workspace_bytes(p.n_seq), dtype=torch.uint8, device="cuda")
+
+    def per_engine(q, k, v, la, beta, o, ST, reps):
+        return {eng: time_calls(lambda: kda.kda_fwd(q, k, v, la, beta, None, o=o, S_T=ST,
+                                                     workspace=ws, engine=eng, stream=stream),
+                                reps, stream)
+                for eng in ("tensorcore", "cudacore")}
+    t = per_engine(p.q, p.k, p.v, p.log_alpha, p.beta, o, ST, 200)
+    roof = prefill_roofline(w, t["tensorcore"], pk)
+    roof["traffic"] = traffic_for("prefill_tc64", "tiny")
+    roof["note"] = "latency-bound: 2 CTAs walk their 4 chunks in series"
+    out = {"metric": "tokens/s", "value": round(w["Ttot"] / (t["tensorcore"] / 1e3), 1),
+           "unit": "tokens/s", "workload": w["label"] + " (tensor-core engine)",
+           "ms_per_call": round(t["tensorcore"], 4),
+           "cudacore_ms_per_call": round(t["cudacore"], 4), "roofline": roof}
+    big = I.prefill_problem(1, 8192, 96, 64, 64, "f32", (-0.5, -0.001), None, args.seed, "cuda")
+    ob = torch.empty_like(big.v)
+    STb = torch.empty((1, 96, 64, 64), dtype=torch.float32, device="cuda")
+    tb = per_engine(big.q, big.k, big.v, big.log_alpha, big.beta, ob, STb, 10)
+    wb = dict(kind="prefill", prob=big, Ttot=8192, H=96, d=64, label="")
+    out["prefill_size"] = {"workload": "prefill B=1 H=96 T=8192 d=64 fp32, S0=0",
+                           "tensorcore_ms": round(tb["tensorcore"], 4),
+                           "cudacore_ms": round(tb["cudacore"], 4),
+                           "tokens_per_s": round(8192 / (tb["tensorcore"] / 1e3), 1),
+                           "roofline": hbm_roof(prefill_alg_bytes(wb), tb["tensorcore"], pk)}
+    if cpu:
+        out["cpu_baseline"] = cpu_baseline(w, args, target_s=2.0)
+    del w, p, o, ST, big, ob, STb
     torch.cuda.empty_cache()
     return out
 
