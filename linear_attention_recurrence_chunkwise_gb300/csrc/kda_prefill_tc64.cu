@@ -27,15 +27,17 @@
 // operand has 64 rows (S^T, V^T - Z^T and U^T, bf16 pairs read from tensor
 // memory) hold them in lanes 64-127, so their results land in lanes 64-127, and
 // lanes 0-63 of those operands stay zero.  So warps 0-1 (tensor-memory lanes
-// 0-63) read out A, warps 2-3 (lanes 64-127) M, Z^T, U^T, O^T and the state.  One CTA of 128 threads per
-// (sequence, head) walks the chunks one at a time; one thread issues the MMAs
-// and the TMA copies of the next chunk's rows (issued as soon as the current
-// chunk's rows have been read, landing while the chunk computes).  The
-// operand phase gives each thread two channels of 16 tokens (bf16 pairs
-// packed two values per instruction, 32-bit stores); the solve inverts the
-// four 16 x 16 diagonal blocks of I + A by substitution, then assembles the
-// two 32 x 32 halves and their lower-left block by fp32 block products over
-// all four warps.
+// 0-63) read out A, warps 2-3 (lanes 64-127) M, Z^T, U^T, O^T and the state.
+//
+// One CTA of 128 threads per (sequence, head) walks the chunks one at a time;
+// one thread issues the MMAs and the TMA copies of the next chunk's rows (issued
+// as soon as the current chunk's rows have been read, landing while the chunk
+// computes).  The operand pass of the next chunk runs on warps 0-1 while warps
+// 2-3 write out the current chunk's outputs and state: each thread takes two
+// channels of 32 tokens (bf16 pairs packed two values per instruction, 32-bit
+// stores).  The solve inverts the four 16 x 16 diagonal blocks of I + A by
+// substitution, then assembles the two 32 x 32 halves and their lower-left
+// block by fp32 block products over all four warps.
 // A (sequence, head) with a chunk whose cumulative log-decay leaves [-80, 0]
 // (exp(-G) past fp32 range) is recomputed token by token from S0 instead.
 // Every mbarrier wait is bounded; a timeout records KDA_ERR_TIMEOUT.
@@ -77,7 +79,7 @@ struct __align__(1024) Tc64Smem {
     uint8_t raw[4 * C * 256];  // the next chunk's rows as they are in memory (TMA):
                                // log_alpha, k, q, v, 64 rows each of 64 elements
     float a[C * LDA];   // beta-scaled A (fp32); staging of the token-by-token pass
-    float gpart[1][D];  // log2-decay sums of the first half of the chunk's tokens
+    float gpart[D];     // log2-decay sums of the first half of the chunk's tokens
     float gam[2][D];    // gamma of the chunk (even, odd)
     float bet[C];
     float rbet[C];      // the next chunk's beta (cp.async)
@@ -431,11 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s1 = fmaf(la.y, kLog2e, s1);
             }
         }
-        if (w == 0) *reinterpret_cast<float2 *>(&sm.gpart[0][c]) = make_float2(s0, s1);
+        if (w == 0) *reinterpret_cast<float2 *>(&sm.gpart[c]) = make_float2(s0, s1);
         named_bar_sync(1, 64);
         float G0 = 0.f, G1 = 0.f;
         if (w) {
-            const float2 g = *reinterpret_cast<const float2 *>(&sm.gpart[0][c]);
+            const float2 g = *reinterpret_cast<const float2 *>(&sm.gpart[c]);
             G0 = g.x;
             G1 = g.y;
         }
